@@ -1,0 +1,442 @@
+"""Plain, slow CPU oracle for decode attention over a losslessly compressed BF16 paged KV cache.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and ``--impl reference`` legs may import this module.  The product path (the CUDA library under
+``decode_attention_compressed_gb300/`` and its Python binding) never imports or calls it, and this
+module imports nothing from the product path.
+
+What it follows (the pages are summaries of three papers; the subject is ZipFusion):
+
+* "ZipFusion: Fusing Lossless KV Decompression with Attention for Efficient LLM Decoding",
+  §II.A (KV Cache and BF16): a BF16 value is 1 sign bit, 8 exponent bits, 7 fraction bits, and
+  lossless means every bit pattern comes back.
+* same page, §III.B (Lossless KV Cache Format) and Fig. 2: a 512-value block is eligible when every
+  exponent lies in [b, b+15], b being the block's minimum exponent rounded down to an even number;
+  each value keeps its low byte (exponent LSB + 7 fraction bits) verbatim plus a 4-bit code made of
+  the sign and a 3-bit exponent offset; two codes share a byte; low bytes come first, then codes;
+  an eligible block takes 768 bytes instead of 1024, metadata excluded; other blocks stay raw.
+* same page, §III.C (Attention over the Compressed KV Cache): keys and values are laid out for
+  their operand roles in QK^T and PV; raw blocks need no reconstruction.
+* same page, §III.D (KV Cache Management and Scheduling): pages stay uncompressed while partially
+  filled; a full page is compressed later and keeps its page id.
+* same page, §IV.B (Attention Kernel Performance): attention over split chunks is finished by a
+  split-result merge.
+
+Where the pages leave a choice open, this module takes the readings listed in the design notes
+(block shape, operand storage order, nibble pairing, metadata word, escape list, natural-log LSE).
+Everything is computed per block / per head with NumPy in float64; there is no blocking, fusion or
+reordering beyond what the definitions state.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+HEAD_DIM = 128
+TILE_TOKENS = 16            # a block spans 16 consecutive tokens of one page ...
+GROUP_CHANNELS = 32         # ... and 32 consecutive channels of one head
+BLOCK_VALUES = TILE_TOKENS * GROUP_CHANNELS   # 512 values (ZipFusion §III.B)
+GROUPS_PER_TILE = HEAD_DIM // GROUP_CHANNELS  # 4
+LOW_AT, CODES_AT, HEADER_AT, ESCAPES_AT = 0, 512, 768, 772
+SLOT_BYTES = 784            # 768 payload bytes (ZipFusion §III.B) + 4-byte header + 6 x 2-byte escapes
+RAW_BLOCK_BYTES = 1024
+MAX_ESCAPES = 6
+FORMAT_VERSION = 1
+DIR_COMPRESSED = -1
+DIR_INVALID = -2
+
+# status bits mirrored from the library's documented device status word
+ST_BAD_PAGE_ID = 0x1
+ST_BAD_RAW_SLOT = 0x2
+ST_BAD_N_VALID = 0x4
+
+
+# ----------------------------------------------------------------------------------------------
+# BF16 fields (ZipFusion §II.A)
+# ----------------------------------------------------------------------------------------------
+def bf16_fields(x: np.ndarray):
+    """Split BF16 bit patterns into (sign, biased exponent, low byte).
+
+    The low byte holds the exponent's least significant bit and the 7 fraction bits.
+    """
+    x = np.asarray(x, dtype=np.uint16).astype(np.int64)
+    return x >> 15, (x >> 7) & 0xFF, x & 0xFF
+
+
+def bf16_to_f64(x: np.ndarray) -> np.ndarray:
+    """Exact widening of BF16 bit patterns to float64 (BF16 is the top half of a float32)."""
+    x = np.asarray(x, dtype=np.uint16)
+    return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------------------------
+# Storage order of a block (layout for the operand roles, ZipFusion §III.C)
+# ----------------------------------------------------------------------------------------------
+def fragment_cell(lane: int, r: int):
+    """(row, col) of element r (0..7) held by `lane` in a 16x16 16-bit A operand of the
+    warp-level m16n8k16 MMA (PTX ISA, "Matrix Fragments for mma.m16n8k16", fragment A):
+    lanes are split as groupID = lane/4, threadID_in_group = lane%4; elements a0..a7 sit at
+    rows groupID (+8 for a2,a3,a6,a7) and columns 2*threadID_in_group + (0|1) (+8 for a4..a7)."""
+    g, t = lane // 4, lane % 4
+    row = g + 8 * ((r // 2) % 2)
+    col = 2 * t + (r % 2) + 8 * (r // 4)
+    return row, col
+
+
+def storage_order(role: str) -> np.ndarray:
+    """Storage position p[tau, gamma] of token tau (0..15) and channel gamma (0..31) of a block.
+
+    p = 16*lane + 8*half + r, where (lane, r) is the A-operand cell that holds the value:
+    for keys the A operand is K itself (rows = tokens, columns = channels 16*half..16*half+15);
+    for values the A operand is V transposed (rows = channels 16*half.., columns = tokens).
+    """
+    if role not in ("k", "v"):
+        raise ValueError("role must be 'k' or 'v'")
+    pos = np.full((TILE_TOKENS, GROUP_CHANNELS), -1, dtype=np.int64)
+    for lane in range(32):
+        for half in range(2):
+            for r in range(8):
+                row, col = fragment_cell(lane, r)
+                p = 16 * lane + 8 * half + r
+                if role == "k":
+                    tau, gamma = row, 16 * half + col
+                else:
+                    tau, gamma = col, 16 * half + row
+                pos[tau, gamma] = p
+    return pos
+
+
+_ORDER = {"k": storage_order("k"), "v": storage_order("v")}
+
+
+def to_storage(block: np.ndarray, role: str) -> np.ndarray:
+    """Natural [16][32] block -> 512 values in storage order."""
+    block = np.asarray(block, dtype=np.uint16)
+    assert block.shape == (TILE_TOKENS, GROUP_CHANNELS)
+    x = np.empty(BLOCK_VALUES, dtype=np.uint16)
+    x[_ORDER[role].ravel()] = block.ravel()
+    return x
+
+
+def from_storage(x: np.ndarray, role: str) -> np.ndarray:
+    """512 values in storage order -> natural [16][32] block."""
+    x = np.asarray(x, dtype=np.uint16)
+    return x[_ORDER[role]]
+
+
+# ----------------------------------------------------------------------------------------------
+# Block codec (ZipFusion §III.B, extended by an escape list)
+# ----------------------------------------------------------------------------------------------
+def block_base(e: np.ndarray):
+    """Even base exponent b of a block and the list of escaped storage positions.
+
+    ZipFusion §III.B: b = minimum exponent rounded down to even; eligible iff max <= b + 15.
+    When that fails, this format anchors the window at the top instead (the smallest even b with
+    max <= b + 15) and lists the values below the window as escapes.
+    """
+    emin, emax = int(e.min()), int(e.max())
+    b = emin & ~1
+    if emax > b + 15:
+        b = (emax - 14) & ~1
+    escapes = np.nonzero(e < b)[0]
+    return b, escapes
+
+
+def encode_block(block: np.ndarray, role: str):
+    """Encode one natural [16][32] block of BF16 bit patterns.
+
+    Returns the 784-byte slot (np.uint8) or None when more than 6 values fall outside the window
+    (the block must then be stored raw).
+    Slot: [0,512) low bytes in storage order; [512,768) codes, byte 4m+k = code[8m+k] |
+    code[8m+k+4] << 4; [768,772) little-endian header = b/2 | n_escapes << 8 | version << 24;
+    [772,784) six little-endian u16 escapes (p << 7 | exponent >> 1), ascending p, unused = 0.
+    """
+    x = to_storage(block, role)
+    s, e, lo = bf16_fields(x)
+    eh = e >> 1
+    b, escapes = block_base(e)
+    if len(escapes) > MAX_ESCAPES:
+        return None
+    off = eh - b // 2
+    off[escapes] = 0
+    assert off.min() >= 0 and off.max() <= 7
+    code = (s << 3) | off
+    slot = np.zeros(SLOT_BYTES, dtype=np.uint8)
+    slot[LOW_AT:LOW_AT + 512] = lo
+    pairs = code.reshape(64, 8)
+    slot[CODES_AT:CODES_AT + 256] = (pairs[:, 0:4] | (pairs[:, 4:8] << 4)).ravel()
+    header = (b // 2) | (len(escapes) << 8) | (FORMAT_VERSION << 24)
+    slot[HEADER_AT:HEADER_AT + 4] = np.frombuffer(int(header).to_bytes(4, "little"), np.uint8)
+    for i, p in enumerate(escapes):
+        entry = (int(p) << 7) | int(eh[p])
+        slot[ESCAPES_AT + 2 * i:ESCAPES_AT + 2 * i + 2] = np.frombuffer(entry.to_bytes(2, "little"), np.uint8)
+    return slot
+
+
+def parse_header(slot: np.ndarray):
+    """(b/2, escape count, escape list [(p, exponent>>1)]) of a slot; raises on a malformed one."""
+    slot = np.asarray(slot, dtype=np.uint8)
+    header = int.from_bytes(slot[HEADER_AT:HEADER_AT + 4].tobytes(), "little")
+    half_base, n_esc, version = header & 0x7F, (header >> 8) & 0xFF, header >> 24
+    if version != FORMAT_VERSION or (header & 0x00FFF880) != 0 or n_esc > MAX_ESCAPES:
+        raise ValueError(f"malformed block header {header:#010x}")
+    esc = []
+    for i in range(MAX_ESCAPES):
+        entry = int.from_bytes(slot[ESCAPES_AT + 2 * i:ESCAPES_AT + 2 * i + 2].tobytes(), "little")
+        if i < n_esc:
+            esc.append((entry >> 7, entry & 0x7F))
+        elif entry != 0:
+            raise ValueError("nonzero unused escape entry")
+    ps = [p for p, _ in esc]
+    if ps != sorted(set(ps)):
+        raise ValueError("escape positions must be strictly ascending")
+    return half_base, n_esc, esc
+
+
+def decode_block(slot: np.ndarray, role: str) -> np.ndarray:
+    """Inverse of encode_block: 784-byte slot -> natural [16][32] BF16 bit patterns.
+
+    High byte = sign << 7 | (b/2 + offset); an escaped value takes its listed exponent>>1
+    instead.  High byte << 8 | low byte gives the original pattern (ZipFusion §III.B: no rounding).
+    """
+    slot = np.asarray(slot, dtype=np.uint8)
+    half_base, _, esc = parse_header(slot)
+    lo = slot[LOW_AT:LOW_AT + 512].astype(np.int64)
+    packed = slot[CODES_AT:CODES_AT + 256].astype(np.int64).reshape(64, 4)
+    code = np.concatenate([packed & 0xF, packed >> 4], axis=1).ravel()
+    hi = ((code >> 3) << 7) | (half_base + (code & 7))
+    for p, eh in esc:
+        hi[p] = (hi[p] & 0x80) | eh
+    x = ((hi << 8) | lo).astype(np.uint16)
+    return from_storage(x, role)
+
+
+# ----------------------------------------------------------------------------------------------
+# Page heads: a page of P tokens for one KV head holds P/16 tiles x 4 channel groups of blocks
+# ----------------------------------------------------------------------------------------------
+def page_blocks(page: np.ndarray):
+    """Natural blocks of a [P][128] page head, in record order (tile-major, then channel group)."""
+    P = page.shape[0]
+    for tile in range(P // TILE_TOKENS):
+        for grp in range(GROUPS_PER_TILE):
+            yield page[TILE_TOKENS * tile:TILE_TOKENS * (tile + 1), GROUP_CHANNELS * grp:GROUP_CHANNELS * (grp + 1)]
+
+
+def encode_page_head(k_page: np.ndarray, v_page: np.ndarray, n_valid: int, force_raw: bool = False):
+    """Encode one page head.  Returns ("comp", k_record, v_record) with 784-byte slots, or
+    ("raw", k_record, v_record) with 512 BF16 values per block in storage order.
+
+    The page stays raw when it is partially filled (ZipFusion §III.D), when any of its K or V
+    blocks cannot be encoded, or when the caller asks for raw storage.
+    """
+    P = k_page.shape[0]
+    if not force_raw and n_valid == P:
+        slots_k = [encode_block(b, "k") for b in page_blocks(k_page)]
+        slots_v = [encode_block(b, "v") for b in page_blocks(v_page)]
+        if all(s is not None for s in slots_k + slots_v):
+            return "comp", np.concatenate(slots_k), np.concatenate(slots_v)
+    raw_k = np.concatenate([to_storage(b, "k") for b in page_blocks(k_page)])
+    raw_v = np.concatenate([to_storage(b, "v") for b in page_blocks(v_page)])
+    return "raw", raw_k, raw_v
+
+
+def decode_page_head(kind: str, k_record: np.ndarray, v_record: np.ndarray, P: int):
+    """Inverse of encode_page_head: -> ([P][128], [P][128]) BF16 bit patterns."""
+    k = np.empty((P, HEAD_DIM), dtype=np.uint16)
+    v = np.empty((P, HEAD_DIM), dtype=np.uint16)
+    i = 0
+    for tile in range(P // TILE_TOKENS):
+        for grp in range(GROUPS_PER_TILE):
+            rows = slice(TILE_TOKENS * tile, TILE_TOKENS * (tile + 1))
+            cols = slice(GROUP_CHANNELS * grp, GROUP_CHANNELS * (grp + 1))
+            if kind == "comp":
+                k[rows, cols] = decode_block(k_record[SLOT_BYTES * i:SLOT_BYTES * (i + 1)], "k")
+                v[rows, cols] = decode_block(v_record[SLOT_BYTES * i:SLOT_BYTES * (i + 1)], "v")
+            else:
+                k[rows, cols] = from_storage(k_record[BLOCK_VALUES * i:BLOCK_VALUES * (i + 1)], "k")
+                v[rows, cols] = from_storage(v_record[BLOCK_VALUES * i:BLOCK_VALUES * (i + 1)], "v")
+            i += 1
+    return k, v
+
+
+@dataclass
+class Cache:
+    """Host model of one layer's compressed paged cache, byte-for-byte the library's layout.
+
+    k_comp/v_comp: [num_pages][Hkv][P/16 * 4 * 784] uint8 (slot of each page id)
+    k_raw/v_raw:   [num_raw][Hkv][P/16 * 4 * 512] uint16 (raw slots, storage order)
+    dir:           [num_pages][Hkv] int32: -1 compressed, r >= 0 raw slot r, -2 invalid
+    """
+    num_pages: int
+    num_kv_heads: int
+    page_size: int
+    num_raw: int
+
+    def __post_init__(self):
+        P, H = self.page_size, self.num_kv_heads
+        nblk = (P // TILE_TOKENS) * GROUPS_PER_TILE
+        self.k_comp = np.zeros((self.num_pages, H, nblk * SLOT_BYTES), np.uint8)
+        self.v_comp = np.zeros_like(self.k_comp)
+        self.k_raw = np.zeros((self.num_raw, H, nblk * BLOCK_VALUES), np.uint16)
+        self.v_raw = np.zeros_like(self.k_raw)
+        self.dir = np.full((self.num_pages, H), DIR_INVALID, np.int32)
+        self.status = 0
+
+
+def encode_pages(cache: Cache, src_k, src_v, page_ids, n_valid, raw_slots, force_raw=False):
+    """Write n source pages ([n][Hkv][P][128] BF16 bits) into the cache under their page ids.
+
+    A page head that stays raw goes to raw slot raw_slots[i]; if that slot is missing or out of
+    range, its directory entry becomes invalid and the status word records it.
+    """
+    P = cache.page_size
+    for i, pid in enumerate(page_ids):
+        pid, nv, slot = int(pid), int(n_valid[i]), int(raw_slots[i])
+        if not 0 <= pid < cache.num_pages:
+            cache.status |= ST_BAD_PAGE_ID
+            continue
+        if not 0 <= nv <= P:
+            cache.status |= ST_BAD_N_VALID
+            cache.dir[pid, :] = DIR_INVALID
+            continue
+        for h in range(cache.num_kv_heads):
+            kind, rk, rv = encode_page_head(src_k[i, h], src_v[i, h], nv, force_raw)
+            if kind == "comp":
+                cache.k_comp[pid, h] = rk
+                cache.v_comp[pid, h] = rv
+                cache.dir[pid, h] = DIR_COMPRESSED
+            elif 0 <= slot < cache.num_raw:
+                cache.k_raw[slot, h] = rk
+                cache.v_raw[slot, h] = rv
+                cache.dir[pid, h] = slot
+            else:
+                cache.dir[pid, h] = DIR_INVALID
+                cache.status |= ST_BAD_RAW_SLOT
+
+
+def read_page_head(cache: Cache, pid: int, h: int):
+    """Decoded ([P][128], [P][128]) BF16 bits of page `pid`, head `h`; None if invalid."""
+    d = int(cache.dir[pid, h])
+    if d == DIR_COMPRESSED:
+        return decode_page_head("comp", cache.k_comp[pid, h], cache.v_comp[pid, h], cache.page_size)
+    if 0 <= d < cache.num_raw:
+        return decode_page_head("raw", cache.k_raw[d, h], cache.v_raw[d, h], cache.page_size)
+    return None
+
+
+def decompress(cache: Cache, page_ids):
+    """[n][Hkv][P][128] K and V bit patterns of the given pages (zeros for invalid entries)."""
+    n, H, P = len(page_ids), cache.num_kv_heads, cache.page_size
+    k = np.zeros((n, H, P, HEAD_DIM), np.uint16)
+    v = np.zeros_like(k)
+    for i, pid in enumerate(page_ids):
+        for h in range(H):
+            kv = read_page_head(cache, int(pid), h)
+            if kv is not None:
+                k[i, h], v[i, h] = kv
+    return k, v
+
+
+# ----------------------------------------------------------------------------------------------
+# Attention (float64 over the exact BF16 values)
+# ----------------------------------------------------------------------------------------------
+def attention_one(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """Single-query softmax attention in float64.
+
+    s_t = scale * sum_c q_c K[t,c];  w_t = exp(s_t - m) / sum_u exp(s_u - m) with m = max s;
+    out = sum_t w_t V[t];  lse = m + ln sum_u exp(s_u - m).  Empty context: out = 0, lse = -inf.
+    Returns (out [D], lse, w [T]).
+    """
+    q = np.asarray(q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1]), -math.inf, np.zeros(0)
+    s = scale * (K @ q)
+    m = s.max()
+    e = np.exp(s - m)
+    z = e.sum()
+    w = e / z
+    return w @ V, m + math.log(z), w
+
+
+def attention_dense(q_bits, k_seqs, v_seqs, scale: float):
+    """Decode attention over per-request dense caches.
+
+    q_bits [B][Hq][D] BF16 bits; k_seqs[b], v_seqs[b]: [L_b][Hkv][D] BF16 bits.
+    Query head h reads KV head h // (Hq / Hkv) (grouped-query attention).
+    Returns out [B][Hq][D] float64 and lse [B][Hq] float64 (natural log).
+    """
+    B, Hq, D = q_bits.shape
+    q = bf16_to_f64(q_bits)
+    out = np.zeros((B, Hq, D))
+    lse = np.full((B, Hq), -math.inf)
+    for b in range(B):
+        K = bf16_to_f64(k_seqs[b])
+        V = bf16_to_f64(v_seqs[b])
+        Hkv = K.shape[1]
+        group = Hq // Hkv
+        for h in range(Hq):
+            g = h // group
+            out[b, h], lse[b, h], _ = attention_one(q[b, h], K[:, g, :], V[:, g, :], scale)
+    return out, lse
+
+
+def gather_sequence(cache: Cache, page_table_row, seq_len: int, heads=None):
+    """Decoded [L][Hkv][128] K and V of one request: token t lives in page
+    page_table_row[t // P] at slot t % P.  `heads` restricts which KV heads are decoded
+    (others stay zero)."""
+    P, H = cache.page_size, cache.num_kv_heads
+    heads = range(H) if heads is None else heads
+    npages = -(-seq_len // P)
+    K = np.zeros((npages * P, H, HEAD_DIM), np.uint16)
+    V = np.zeros_like(K)
+    for i in range(npages):
+        pid = int(page_table_row[i])
+        for h in heads:
+            kv = read_page_head(cache, pid, h)
+            if kv is None:
+                raise ValueError(f"page {pid} head {h} has no valid storage")
+            K[i * P:(i + 1) * P, h], V[i * P:(i + 1) * P, h] = kv
+    return K[:seq_len], V[:seq_len]
+
+
+def decode_attention(q_bits, cache: Cache, page_table, seq_lens, scale: float, pairs=None):
+    """Decode attention over the compressed paged cache (what zf_decode_attn computes).
+
+    `pairs`, if given, is a list of (b, h) query heads to evaluate (others are left 0 / -inf);
+    it lets tests check sampled outputs of very large workloads one by one.
+    """
+    B, Hq, D = q_bits.shape
+    Hkv = cache.num_kv_heads
+    group = Hq // Hkv
+    out = np.zeros((B, Hq, D))
+    lse = np.full((B, Hq), -math.inf)
+    want = sorted(pairs) if pairs is not None else [(b, h) for b in range(B) for h in range(Hq)]
+    q = bf16_to_f64(q_bits)
+    by_b = {}
+    for b, h in want:
+        by_b.setdefault(b, []).append(h)
+    for b, hs in by_b.items():
+        heads = sorted({h // group for h in hs})
+        K, V = gather_sequence(cache, page_table[b], int(seq_lens[b]), heads)
+        K, V = bf16_to_f64(K), bf16_to_f64(V)
+        for h in hs:
+            g = h // group
+            out[b, h], lse[b, h], _ = attention_one(q[b, h], K[:, g, :], V[:, g, :], scale)
+    return out, lse
+
+
+def merge_partials(outs, lses):
+    """Split-result merge: lse = ln sum_i exp(lse_i); out = sum_i exp(lse_i - lse) out_i,
+    where out_i is the normalised output of chunk i."""
+    lses = np.asarray(lses, np.float64)
+    if len(lses) == 0 or np.all(np.isneginf(lses)):
+        return np.zeros(np.asarray(outs).shape[-1]), -math.inf
+    m = lses.max()
+    w = np.exp(lses - m)
+    lse = m + math.log(w.sum())
+    out = sum(math.exp(l - lse) * np.asarray(o, np.float64) for o, l in zip(outs, lses))
+    return out, lse

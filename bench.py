@@ -1,0 +1,533 @@
+"""Benchmark: decode-attention microseconds per decode step over the compressed BF16 paged KV cache,
+with KV GB/s (compressed and effective-uncompressed), the fraction of the measured HBM peak, and
+the same step on the dense-BF16 kernel.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one decode step of the workload: for every layer, zf_decode_attn over that layer's
+compressed cache (the long-context workload also appends one token per request through
+zf_encode_pages each step).  Inputs are resident in HBM; the per-step KV bytes exceed L2, so no
+extra flush is needed.  Prints one JSON line on rank 0.  N > 1 runs N independent replicas (one
+per GPU, weak scaling); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")     # the CPU baseline runs the oracle on one core
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & KV GB/s (compressed, % of HBM peak) vs dense BF16 path"
+DEFAULT_WORKLOAD = "llama7b_mha_8192"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_compressed_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it was
+    taken on the current kernel sources (same source hash); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        w = line.split()
+        if len(w) >= 4 and not line.startswith("#") and w[0] == workload and w[3] == want:
+            return float(w[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            w = [x.strip() for x in line.split(",")]
+            if len(w) >= 9:
+                try:
+                    rows.append((float(w[1]), float(w[2]), w[5], w[6], w[7], w[8]))
+                except ValueError:
+                    pass
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[2:]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------ GPU arm
+def tile_bytes(layer, dirs, compressed: bool) -> int:
+    """Algorithmic bytes one attention launch reads: per (request, kv head), every 16-token tile
+    holding context tokens costs 6272 bytes (compressed page) or 8192 bytes (raw page), plus q,
+    page table, seq_lens, out and lse."""
+    import torch
+    w = layer.workload
+    P = w.page_size
+    lens = layer.seq_lens.cpu().to(torch.int64)
+    table = layer.page_table.cpu().to(torch.int64)
+    total = 0
+    for b in range(w.batch):
+        L = int(lens[b])
+        npg = -(-L // P)
+        tiles = torch.clamp(L - torch.arange(npg) * P, max=P)
+        tiles = (tiles + 15) // 16
+        if compressed:
+            raw = (dirs[table[b, :npg]] >= 0).to(torch.int64)          # [npg][Hkv]
+            per = tiles[:, None] * torch.where(raw.bool(), 8192, 6272)
+            total += int(per.sum())
+        else:
+            total += int(tiles.sum()) * 8192 * w.num_kv_heads
+    total += w.batch * w.num_q_heads * 128 * 2 + table.numel() * 4 + w.batch * 4
+    total += w.batch * w.num_q_heads * (128 * 4 + 4)
+    return total
+
+
+def dense_equiv_bytes(layer) -> int:
+    """Bytes the same context occupies as dense BF16 (2 x 128 x 2 per token and kv head)."""
+    w = layer.workload
+    return int(layer.seq_lens.to("cpu").sum()) * w.num_kv_heads * 512
+
+
+def setup_layers(zf, I, w, device):
+    import torch
+    layers = []
+    for l in range(w.layers):
+        layer = I.make_layer(w, layer=l, device=device)
+        npg = layer.num_pages
+        tails = torch.nonzero(layer.n_valid < w.page_size).flatten().cpu().tolist()
+        extra = 0
+        if w.name == "long_ctx":
+            extra = 8 * w.batch       # spare page ids for the appended tokens
+        raw_slots = [-1] * npg
+        for j, p in enumerate(tails):
+            raw_slots[p] = j
+        cache = zf.Cache(npg + extra, w.num_kv_heads, w.page_size, len(tails) + 4 * w.batch + 8, device=device)
+        zf.encode_pages(cache, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, raw_slots)
+        dense = zf.Cache(npg + extra, w.num_kv_heads, w.page_size, npg + extra, device=device, compressed=False)
+        zf.encode_pages(dense, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, list(range(npg)),
+                        force_raw=True)
+        torch.cuda.synchronize()
+        if cache.status_word() or dense.status_word():
+            raise RuntimeError("encode reported a device error")
+        dirs = cache.dir.cpu()
+        entry = dict(layer=layer, cache=cache, dense=dense, dirs=dirs, num_pages=npg)
+        if w.name != "long_ctx":
+            layer.k_pages = layer.v_pages = None          # the caches hold the data now
+        layers.append(entry)
+    return layers
+
+
+def prefill_encode_ms(zf, I, device):
+    """Time a full-prefill encode: 8192 tokens x 32 layers, 8 kv heads, 64-token pages."""
+    import torch
+    w = I.scaled(I.WORKLOADS["long_ctx"], batch=1, ctx=8192)
+    layer = I.make_layer(w, device=device)
+    npg = layer.num_pages
+    caches = [zf.Cache(npg, w.num_kv_heads, w.page_size, 8, device=device) for _ in range(32)]
+    ids = torch.arange(npg, dtype=torch.int32, device=device)
+    nv = layer.n_valid.to(device)
+    rs = torch.full((npg,), -1, dtype=torch.int32, device=device)
+    for c in caches[:2]:
+        zf.encode_pages(c, layer.k_pages, layer.v_pages, ids, nv, rs)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for c in caches:
+        zf.encode_pages(c, layer.k_pages, layer.v_pages, ids, nv, rs)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    src_bytes = 2 * layer.k_pages.numel() * 2 * 32
+    return ms, src_bytes / (ms * 1e-3) / 1e9
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from decode_attention_compressed_gb300 import build as B
+    from decode_attention_compressed_gb300 import inputs as I
+
+    B.build()
+    from decode_attention_compressed_gb300 import zf
+
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
+    w = I.WORKLOADS[args.workload]
+    layers = setup_layers(zf, I, w, device)
+    stream = torch.cuda.current_stream()
+    outs = [(torch.empty(w.batch, w.num_q_heads, 128, device=device),
+             torch.empty(w.batch, w.num_q_heads, device=device)) for _ in layers]
+
+    append = None
+    max_pages = int(layers[0]["layer"].page_table.shape[1])
+    if w.name == "long_ctx":
+        append = LongContextAppend(zf, I, w, layers[0], device, 2 * (args.steps + args.warmup))
+        max_pages = int(append.table.shape[1])
+    ws_bytes = zf.workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.page_size, max_pages)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+
+    def step(dense=False, events=None):
+        if append is not None and not dense:
+            append.step()
+        for i, ent in enumerate(layers):
+            lay = ent["layer"]
+            use_append = append is not None and not dense
+            lens = append.lens if use_append else lay.seq_lens
+            table = append.table if use_append else lay.page_table
+            if events is not None:
+                events[i][0].record()
+            zf.decode_attn(ent["dense"] if dense else ent["cache"], lay.q, table, lens, lay.scale,
+                           out=outs[i][0], lse=outs[i][1], workspace=workspace, dense=dense)
+            if events is not None:
+                events[i][1].record()
+
+    def timed(dense=False, steps=args.steps, warmup=args.warmup):
+        for _ in range(warmup):
+            step(dense)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        per_call = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in layers] for _ in range(steps)]
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local_rank) as clk:
+            s.record()
+            for k in range(steps):
+                step(dense, per_call[k])
+            e.record()
+            torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms = s.elapsed_time(e)
+        calls = [a.elapsed_time(b) for row in per_call for (a, b) in row]
+        if world > 1:
+            t = torch.tensor([ms], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms / steps, statistics.mean(calls), clk.summary()
+
+    if append is not None:
+        append.reset()
+    ms_step, call_ms, clocks = timed(False)
+    if append is not None:
+        append.reset()
+    dense_ms_step, dense_call_ms, dense_clocks = timed(True)
+
+    # end to end through the public API: q (and seq_lens) from pinned host memory, out + lse back
+    q_host = [ent["layer"].q.cpu().pin_memory() for ent in layers]
+    lens_host = [ent["layer"].seq_lens.cpu().pin_memory() for ent in layers]
+    out_host = [(torch.empty(o.shape, pin_memory=True), torch.empty(l.shape, pin_memory=True)) for o, l in outs]
+    q_dev = [torch.empty_like(ent["layer"].q) for ent in layers]
+    lens_dev = [torch.empty_like(ent["layer"].seq_lens) for ent in layers]
+
+    def e2e_step():
+        for i, ent in enumerate(layers):
+            lay = ent["layer"]
+            q_dev[i].copy_(q_host[i], non_blocking=True)
+            lens_dev[i].copy_(lens_host[i], non_blocking=True)
+            zf.decode_attn(ent["cache"], q_dev[i], lay.page_table, lens_dev[i], lay.scale, out=outs[i][0],
+                           lse=outs[i][1], workspace=workspace)
+            out_host[i][0].copy_(outs[i][0], non_blocking=True)
+            out_host[i][1].copy_(outs[i][1], non_blocking=True)
+
+    if append is None:
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.steps):
+            e2e_step()
+        e.record()
+        torch.cuda.synchronize()
+        e2e_ms = s.elapsed_time(e) / args.steps
+        h2d = sum(q.numel() * 2 + l.numel() * 4 for q, l in zip(q_host, lens_host))
+        d2h = sum(o.numel() * 4 + l.numel() * 4 for o, l in out_host)
+    else:
+        e2e_ms, h2d, d2h = None, 0, 0
+
+    comp_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], True) for ent in layers)
+    dense_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], False) for ent in layers)
+    uncompressed = sum(dense_equiv_bytes(ent["layer"]) for ent in layers)
+    stored = sum(ent["cache"].compressed_bytes() for ent in layers)
+    dense_stored = sum(ent["dense"].compressed_bytes() for ent in layers)
+    per_launch = comp_bytes / len(layers)
+    peak, peak_kind = read_peaks()
+    achieved = per_launch / (call_ms * 1e-3) / 1e9
+    status = [ent["cache"].status_word() | ent["dense"].status_word() for ent in layers]
+    if any(status):
+        raise RuntimeError(f"device status word set: {status}")
+    extra = {}
+    if append is not None:
+        extra["append_encode_per_step"] = {"requests": w.batch, "calls": 1}
+        extra["prefill_encode_ms"], extra["prefill_encode_src_gbs"] = prefill_encode_ms(zf, I, device)
+    result = dict(
+        metric=METRIC, value=round(ms_step * 1e3, 3), unit="us/step", n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=False, scaling="weak",
+        vs_baseline=None, dtype="bf16", data="synthetic (seeded, distributions of the workload)",
+        config={"workload": w.name, "note": w.note, "batch": w.batch, "q_heads": w.num_q_heads,
+                "kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": w.page_size, "ctx": w.ctx,
+                "layers_per_step": w.layers, "parallelism": "replicas" if world > 1 else "single",
+                "l2": f"no flush: {comp_bytes / 1e9:.2f} GB of compressed KV read per step "
+                      f"(> {L2_BYTES / 2**20:.0f} MiB L2)"},
+        kv_gbs_compressed=round(comp_bytes / (ms_step * 1e-3) / 1e9, 1),
+        kv_gbs_effective_uncompressed=round(uncompressed / (ms_step * 1e-3) / 1e9, 1),
+        pct_of_hbm_peak=round(100 * comp_bytes / (ms_step * 1e-3) / 1e9 / peak, 1),
+        pct_of_8tbs_spec=round(100 * comp_bytes / (ms_step * 1e-3) / 1e9 / SPEC_HBM_GBS, 1),
+        compression_ratio=round(dense_stored / stored, 4),
+        bytes_read_ratio=round(dense_bytes / comp_bytes, 4),
+        dense={"us_per_step": round(dense_ms_step * 1e3, 3), "kv_gbs": round(dense_bytes / (dense_ms_step * 1e-3) / 1e9, 1),
+               "pct_of_hbm_peak": round(100 * dense_bytes / (dense_ms_step * 1e-3) / 1e9 / peak, 1),
+               "call_us": round(dense_call_ms * 1e3, 3), "clocks": dense_clocks},
+        speedup_vs_dense=round(dense_ms_step / ms_step, 4),
+        roofline={"kernel": "attn_kernel<compressed> + merge_kernel (one zf_decode_attn call)", "bound": "hbm",
+                  "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                  "peak_source": peak_kind, "bytes_per_launch": int(per_launch), "call_us": round(call_ms * 1e3, 3),
+                  "traffic": read_traffic(w.name)},
+        e2e={"value": round(e2e_ms * 1e3, 3) if e2e_ms else None, "unit": "us/step", "h2d_bytes_per_step": h2d,
+             "d2h_bytes_per_step": d2h},
+        gpu_launches=args.steps * len(layers) * 2 + (args.steps if append is not None else 0),
+        clocks=clocks, **extra,
+    )
+    return result
+
+
+class LongContextAppend:
+    """Long-context step: every request appends one token to its tail page and that page is
+    re-encoded through zf_encode_pages (raw while partial, compressed once it is full).
+
+    All requests have the same length, so the tail page index is shared.  Tail pages (natural
+    layout) come from a seeded staging buffer [new page][request][Hkv][P][128]; per-step lengths,
+    fill counts and page ids are precomputed device arrays, so a step launches only the encode
+    and the attention kernels."""
+
+    def __init__(self, zf, I, w, ent, device, max_steps):
+        import torch
+        self.zf, self.w, self.ent = zf, w, ent
+        lay = ent["layer"]
+        P, B = w.page_size, w.batch
+        L0 = [int(x) for x in lay.seq_lens.cpu()]
+        assert len(set(L0)) == 1, "append path expects equal request lengths"
+        L0 = L0[0]
+        base_pages = lay.page_table.shape[1]
+        self.new_pages = (L0 % P + max_steps) // P + 1
+        spare0 = ent["num_pages"]
+        ids = torch.arange(self.new_pages * B, dtype=torch.int32).reshape(self.new_pages, B) + spare0
+        self.table = torch.cat([lay.page_table.cpu(), ids.t()], dim=1).contiguous().to(device)
+        steps = torch.arange(1, max_steps + 1)
+        lens = L0 + steps
+        self.page_of_step = ((lens - 1) // P - (L0 + P - 1) // P).tolist()
+        self.lens_all = lens[:, None].expand(max_steps, B).to(torch.int32).contiguous().to(device)
+        self.fill_all = ((lens - 1) % P + 1)[:, None].expand(max_steps, B).to(torch.int32).contiguous().to(device)
+        self.ids_all = ids.to(device)
+        self.raw_slots = torch.arange(B, dtype=torch.int32, device=device)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.seed * 1000 + 999)
+        shape = (self.new_pages, B, w.num_kv_heads, P, 128)
+        self.src_k = torch.randn(shape, generator=gen, device=device).to(torch.bfloat16).view(torch.int16)
+        self.src_v = torch.randn(shape, generator=gen, device=device).to(torch.bfloat16).view(torch.int16)
+        self.max_steps = max_steps
+        self.base_lens = lay.seq_lens
+        self.reset()
+
+    def reset(self):
+        self.n = 0
+        self.lens = self.base_lens
+
+    def step(self):
+        import ctypes
+        import torch
+        if self.n >= self.max_steps:
+            raise RuntimeError("more append steps than planned")
+        j = self.page_of_step[self.n]
+        d = self.ent["cache"].desc()
+        P = ctypes.c_void_p
+        code = self.zf.lib().zf_encode_pages(
+            ctypes.byref(d), P(self.src_k[j].data_ptr()), P(self.src_v[j].data_ptr()), P(self.ids_all[j].data_ptr()),
+            P(self.fill_all[self.n].data_ptr()), P(self.raw_slots.data_ptr()), self.w.batch, 0,
+            torch.cuda.current_stream().cuda_stream)
+        if code != 0:
+            raise RuntimeError(f"zf_encode_pages failed: {code}")
+        self.lens = self.lens_all[self.n]
+        self.n += 1
+
+
+# ------------------------------------------------------------------------------ CPU oracle arm
+def oracle_sample(I, O, w, heads, seed_layer=0):
+    """Oracle cache for request 0 of layer 0 restricted to `heads` kv heads (built untimed), and a
+    callable that runs the oracle's decode attention for the query heads of those kv heads."""
+    import numpy as np
+    import torch
+    layer = I.make_layer(w, layer=seed_layer, device="cpu")
+    P = w.page_size
+    L = int(layer.seq_lens[0])
+    pages = layer.page_table[0, : -(-L // P)].to(torch.long)
+    kb = layer.k_pages[pages][:, :heads].numpy().view(np.uint16)
+    vb = layer.v_pages[pages][:, :heads].numpy().view(np.uint16)
+    npg = len(pages)
+    oc = O.Cache(num_pages=npg, num_kv_heads=heads, page_size=P, num_raw=npg)
+    O.encode_pages(oc, kb, vb, list(range(npg)), layer.n_valid[pages].numpy(), list(range(npg)))
+    q = layer.q[:1, : heads * w.group].numpy().view(np.uint16)
+    table = np.arange(npg, dtype=np.int32)[None]
+    lens = np.array([L])
+
+    def run():
+        return O.decode_attention(q, oc, table, lens, layer.scale)
+    return run
+
+
+def cpu_baseline(w, target_s=12.0):
+    """Time the oracle (as it stands) on a bounded sample: some kv heads of request 0, layer 0;
+    scale to microseconds per full decode step (all requests, heads and layers)."""
+    from decode_attention_compressed_gb300 import inputs as I
+    from oracle import zf_oracle as O
+    heads = 1
+    run = oracle_sample(I, O, w, heads)
+    t0 = time.perf_counter()
+    run()
+    one = time.perf_counter() - t0
+    reps = max(1, int(target_s / max(one, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        run()
+    per = (time.perf_counter() - t0) / reps
+    scale = w.batch * w.num_kv_heads * w.layers / heads
+    lens_note = "request 0" if w.ctx_min is None else "request 0 (lengths vary; scaled by batch)"
+    return {"value": round(per * scale * 1e6, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+            "sample": f"{reps}x oracle decode attention of 1 kv head ({w.group} query heads), {lens_note}, "
+                      f"layer 0 of {w.name}; scaled x{scale:.0f} to the full step"}
+
+
+def run_reference(args, rank):
+    from decode_attention_compressed_gb300 import inputs as I
+    from oracle import zf_oracle as O
+    if rank != 0:
+        return None
+    w = I.WORKLOADS[args.workload]
+    run = oracle_sample(I, O, w, 1)
+    scale = w.batch * w.num_kv_heads * w.layers
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    per = (time.perf_counter() - t0) / args.steps * scale
+    v = round(per * 1e6, 1)
+    return dict(metric=METRIC, value=v, unit="us/step", n_gpus=0, steps=args.steps, warmup=args.warmup,
+                ms_per_step=round(per * 1e3, 3), higher_is_better=False, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic (seeded, distributions of the workload)",
+                config={"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                        "page_size": w.page_size, "ctx": w.ctx, "layers_per_step": w.layers},
+                impl="reference",
+                cpu_baseline={"value": v, "unit": "us/step", "cores": 1, "kind": "oracle",
+                              "sample": f"each step: oracle decode attention of 1 kv head ({w.group} query heads) "
+                                        f"of request 0, layer 0, scaled x{scale} to the full step"},
+                e2e={"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        from decode_attention_compressed_gb300 import inputs as I
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(I.WORKLOADS[args.workload])
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

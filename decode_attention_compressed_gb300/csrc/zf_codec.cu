@@ -1,0 +1,305 @@
+// zf_encode_pages and zf_decompress: page compression and its bit-exact inverse.
+//
+// ZipFusion §III.B (Lossless KV Cache Format, Fig. 2): a block is compressed when its exponents
+// fit [b, b+15], b = minimum exponent rounded down to even; each value keeps its low byte and a
+// 4-bit code (sign, exponent offset).  This format adds up to six escapes for blocks whose range
+// is wider (window anchored at the maximum exponent).  ZipFusion §III.D: partial pages stay raw;
+// full pages are compressed under their page id.
+//
+// One CTA encodes one (page, kv head): each warp classifies and encodes whole blocks into shared
+// memory, then the CTA decides compressed vs raw for the page head and writes it out with
+// coalesced 16-byte stores.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zf_device.cuh"
+#include "zf_host.h"
+
+namespace zf {
+
+constexpr int kCodecWarps = 8;
+constexpr int kCodecThreads = kCodecWarps * 32;
+
+struct CodecArgs {
+  uint8_t* k_comp;
+  uint8_t* v_comp;
+  uint16_t* k_raw;
+  uint16_t* v_raw;
+  int32_t* dir;
+  int32_t* status;
+  const uint16_t* src_k;   // encode: source pages; decompress: unused
+  const uint16_t* src_v;
+  uint16_t* dst_k;         // decompress: destination pages
+  uint16_t* dst_v;
+  const int32_t* page_ids;
+  const int32_t* n_valid;
+  const int32_t* raw_slots;
+  int32_t num_pages, hkv, page_size, num_raw, flags;
+};
+
+// Natural-layout address of this lane's 16 values of block (tile, group): token tau = lane/2,
+// channels 32*group + 16*(lane%2) .. +15 of a [P][128] page head.
+__device__ __forceinline__ size_t natural_offset(int tile, int group, int lane) {
+  return static_cast<size_t>(16 * tile + (lane >> 1)) * ZF_HEAD_DIM + 32 * group + 16 * (lane & 1);
+}
+
+__global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int P = a.page_size;
+  const int nblk = P / 4;                    // blocks per K (or V) page head
+  uint8_t* comp = smem;                      // [2*nblk][784]
+  uint16_t* raw = reinterpret_cast<uint16_t*>(smem + 2 * nblk * kSlotBytes);   // [2*nblk][512]
+  int* fail = reinterpret_cast<int*>(raw + 2 * nblk * 512);
+
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pid = a.page_ids[i];
+  const int nv = a.n_valid[i];
+  if (pid < 0 || pid >= a.num_pages) {
+    if (threadIdx.x == 0) report(a.status, ZF_DEV_BAD_PAGE_ID);
+    return;
+  }
+  if (nv < 0 || nv > P) {
+    if (threadIdx.x == 0) {
+      report(a.status, ZF_DEV_BAD_N_VALID);
+      a.dir[static_cast<size_t>(pid) * a.hkv + h] = ZF_DIR_INVALID;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) *fail = 0;
+  __syncthreads();
+
+  const size_t head_elems = static_cast<size_t>(P) * ZF_HEAD_DIM;
+  for (int blk = warp; blk < 2 * nblk; blk += kCodecWarps) {
+    const bool is_value = blk >= nblk;
+    const int bi = is_value ? blk - nblk : blk;
+    const int tile = bi >> 2, group = bi & 3;
+    const uint16_t* src = (is_value ? a.src_v : a.src_k) + (static_cast<size_t>(i) * a.hkv + h) * head_elems +
+                          natural_offset(tile, group, lane);
+    const uint4 x0 = *reinterpret_cast<const uint4*>(src);
+    const uint4 x1 = *reinterpret_cast<const uint4*>(src + 8);
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+
+    // exponent range of the block
+    uint32_t emin = 255, emax = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t v = (w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+      const uint32_t e = (v >> 7) & 0xFFu;
+      emin = min(emin, e);
+      emax = max(emax, e);
+    }
+    emin = __reduce_min_sync(0xFFFFFFFFu, emin);
+    emax = __reduce_max_sync(0xFFFFFFFFu, emax);
+    uint32_t base = emin & ~1u;
+    if (emax > base + 15) base = (emax - 14) & ~1u;
+
+    // scatter into storage order (this block's raw form)
+    uint16_t* rblk = raw + blk * 512;
+    const int tau = lane >> 1, g0 = 16 * (lane & 1);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint16_t v = static_cast<uint16_t>((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+      rblk[block_position(is_value, tau, g0 + j)] = v;
+    }
+    __syncwarp();
+
+    // this lane now owns storage positions 16*lane .. 16*lane+15
+    const uint4 y0 = *reinterpret_cast<const uint4*>(rblk + 16 * lane);
+    const uint4 y1 = *reinterpret_cast<const uint4*>(rblk + 16 * lane + 8);
+    const uint32_t u[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    uint32_t code[16], lo[16], eh[16];
+    uint32_t esc_mask = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t v = (u[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+      const uint32_t e = (v >> 7) & 0xFFu;
+      lo[j] = v & 0xFFu;
+      eh[j] = e >> 1;
+      const bool esc = e < base;
+      esc_mask |= static_cast<uint32_t>(esc) << j;
+      code[j] = ((v >> 15) << 3) | (esc ? 0u : eh[j] - (base >> 1));
+    }
+    const uint32_t cnt = __popc(esc_mask);
+    uint32_t before = cnt;                       // inclusive scan over lanes
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, before, d);
+      if (lane >= d) before += t;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, before, 31);
+    before -= cnt;
+    if (total > ZF_MAX_ESCAPES) {
+      if (lane == 0) atomicOr(fail, 1);
+      continue;
+    }
+    uint8_t* slot = comp + blk * kSlotBytes;
+    uint4 lob;
+    lob.x = lo[0] | lo[1] << 8 | lo[2] << 16 | lo[3] << 24;
+    lob.y = lo[4] | lo[5] << 8 | lo[6] << 16 | lo[7] << 24;
+    lob.z = lo[8] | lo[9] << 8 | lo[10] << 16 | lo[11] << 24;
+    lob.w = lo[12] | lo[13] << 8 | lo[14] << 16 | lo[15] << 24;
+    *reinterpret_cast<uint4*>(slot + 16 * lane) = lob;
+    uint2 cw;
+    cw.x = (code[0] | code[4] << 4) | (code[1] | code[5] << 4) << 8 | (code[2] | code[6] << 4) << 16 |
+           (code[3] | code[7] << 4) << 24;
+    cw.y = (code[8] | code[12] << 4) | (code[9] | code[13] << 4) << 8 | (code[10] | code[14] << 4) << 16 |
+           (code[11] | code[15] << 4) << 24;
+    *reinterpret_cast<uint2*>(slot + 512 + 8 * lane) = cw;
+    uint16_t* escs = reinterpret_cast<uint16_t*>(slot + kEscapesAt);
+    if (lane < ZF_MAX_ESCAPES && static_cast<uint32_t>(lane) >= total) escs[lane] = 0;
+    uint32_t k = before;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (esc_mask & (1u << j)) {
+        escs[k] = static_cast<uint16_t>(((16 * lane + j) << 7) | eh[j]);
+        ++k;
+      }
+    }
+    if (lane == 0)
+      *reinterpret_cast<uint32_t*>(slot + kHeaderAt) =
+          (base >> 1) | (total << 8) | (static_cast<uint32_t>(ZF_FORMAT_VERSION) << 24);
+  }
+  __syncthreads();
+
+  const bool store_raw = (a.flags & ZF_ENCODE_FORCE_RAW) || nv < P || *fail;
+  const size_t dir_at = static_cast<size_t>(pid) * a.hkv + h;
+  if (!store_raw) {
+    const size_t rec = static_cast<size_t>(nblk) * kSlotBytes;     // bytes per K (or V) record
+    uint8_t* dk = a.k_comp + (static_cast<size_t>(pid) * a.hkv + h) * rec;
+    uint8_t* dv = a.v_comp + (static_cast<size_t>(pid) * a.hkv + h) * rec;
+    const int n16 = static_cast<int>(rec / 16);
+    for (int t = threadIdx.x; t < 2 * n16; t += kCodecThreads) {
+      const uint4 val = reinterpret_cast<const uint4*>(comp)[t];
+      if (t < n16) reinterpret_cast<uint4*>(dk)[t] = val;
+      else reinterpret_cast<uint4*>(dv)[t - n16] = val;
+    }
+    if (threadIdx.x == 0) a.dir[dir_at] = ZF_DIR_COMPRESSED;
+    return;
+  }
+  const int rs = a.raw_slots ? a.raw_slots[i] : -1;
+  if (rs < 0 || rs >= a.num_raw) {
+    if (threadIdx.x == 0) {
+      a.dir[dir_at] = ZF_DIR_INVALID;
+      report(a.status, ZF_DEV_BAD_RAW_SLOT);
+    }
+    return;
+  }
+  const size_t rec = static_cast<size_t>(nblk) * 512;            // uint16 per K (or V) record
+  uint16_t* dk = a.k_raw + (static_cast<size_t>(rs) * a.hkv + h) * rec;
+  uint16_t* dv = a.v_raw + (static_cast<size_t>(rs) * a.hkv + h) * rec;
+  const int n16 = static_cast<int>(rec / 8);
+  for (int t = threadIdx.x; t < 2 * n16; t += kCodecThreads) {
+    const uint4 val = reinterpret_cast<const uint4*>(raw)[t];
+    if (t < n16) reinterpret_cast<uint4*>(dk)[t] = val;
+    else reinterpret_cast<uint4*>(dv)[t - n16] = val;
+  }
+  if (threadIdx.x == 0) a.dir[dir_at] = rs;
+}
+
+__global__ void __launch_bounds__(kCodecThreads) decompress_kernel(CodecArgs a) {
+  __shared__ __align__(16) uint16_t stage[kCodecWarps][512];
+  const int P = a.page_size;
+  const int nblk = P / 4;
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pid = a.page_ids[i];
+  int kind = 2;                         // 0 compressed, 1 raw, 2 invalid
+  int slot = 0;
+  if (pid >= 0 && pid < a.num_pages) {
+    const int d = a.dir[static_cast<size_t>(pid) * a.hkv + h];
+    if (d == ZF_DIR_COMPRESSED) {
+      kind = 0;
+      slot = pid;
+    } else if (d >= 0 && d < a.num_raw) {
+      kind = 1;
+      slot = d;
+    }
+  }
+  if (kind == 2 && threadIdx.x == 0)
+    report(a.status, (pid >= 0 && pid < a.num_pages) ? ZF_DEV_BAD_DIR : ZF_DEV_BAD_PAGE_ID);
+
+  const size_t head_elems = static_cast<size_t>(P) * ZF_HEAD_DIM;
+  for (int blk = warp; blk < 2 * nblk; blk += kCodecWarps) {
+    const bool is_value = blk >= nblk;
+    const int bi = is_value ? blk - nblk : blk;
+    const int tile = bi >> 2, group = bi & 3;
+    uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (kind == 0) {
+      const uint8_t* base = (is_value ? a.v_comp : a.k_comp) +
+                            (static_cast<size_t>(slot) * a.hkv + h) * nblk * kSlotBytes + static_cast<size_t>(bi) * kSlotBytes;
+      rebuild_lane(base, lane, v);
+    } else if (kind == 1) {
+      const uint16_t* base = (is_value ? a.v_raw : a.k_raw) +
+                             (static_cast<size_t>(slot) * a.hkv + h) * nblk * 512 + static_cast<size_t>(bi) * 512;
+      load_raw_lane(reinterpret_cast<const uint8_t*>(base), lane, v);
+    }
+    uint16_t* st = stage[warp];
+    *reinterpret_cast<uint4*>(st + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<uint4*>(st + 16 * lane + 8) = make_uint4(v[4], v[5], v[6], v[7]);
+    __syncwarp();
+    const int tau = lane >> 1, g0 = 16 * (lane & 1);
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t lo = st[block_position(is_value, tau, g0 + 2 * j)];
+      const uint32_t hi = st[block_position(is_value, tau, g0 + 2 * j + 1)];
+      o[j] = lo | hi << 16;
+    }
+    uint16_t* dst = (is_value ? a.dst_v : a.dst_k) + (static_cast<size_t>(i) * a.hkv + h) * head_elems +
+                    natural_offset(tile, group, lane);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+    __syncwarp();
+  }
+}
+
+}  // namespace zf
+
+using namespace zf;
+
+extern "C" zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_k, const uint16_t* src_v,
+                                     const int32_t* page_ids, const int32_t* n_valid, const int32_t* raw_slots,
+                                     int32_t n, int32_t flags, void* stream) {
+  zf_status st = check_cache(cache, /*need_comp=*/true, /*need_raw=*/false, /*need_dir=*/true);
+  if (st != ZF_OK) return st;
+  if (n < 0 || (flags & ~ZF_ENCODE_FORCE_RAW)) return ZF_ERR_INVALID_ARGUMENT;
+  if (n == 0) return ZF_OK;
+  if (!src_k || !src_v || !page_ids || !n_valid || !aligned16(src_k) || !aligned16(src_v))
+    return ZF_ERR_INVALID_ARGUMENT;
+  if (cache->num_raw_slots > 0 && (!cache->k_raw || !cache->v_raw || !aligned16(cache->k_raw) || !aligned16(cache->v_raw)))
+    return ZF_ERR_INVALID_ARGUMENT;
+  if (cache->num_kv_heads > 65535) return ZF_ERR_UNSUPPORTED;
+  CodecArgs a{};
+  a.k_comp = cache->k_comp; a.v_comp = cache->v_comp; a.k_raw = cache->k_raw; a.v_raw = cache->v_raw;
+  a.dir = cache->dir; a.status = cache->status;
+  a.src_k = src_k; a.src_v = src_v;
+  a.page_ids = page_ids; a.n_valid = n_valid; a.raw_slots = raw_slots;
+  a.num_pages = cache->num_pages; a.hkv = cache->num_kv_heads; a.page_size = cache->page_size;
+  a.num_raw = cache->num_raw_slots; a.flags = flags;
+  const int nblk = cache->page_size / 4;
+  const size_t smem = static_cast<size_t>(2 * nblk) * (kSlotBytes + 1024) + 16;
+  if (cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return ZF_ERR_CUDA;
+  encode_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
+}
+
+extern "C" zf_status zf_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n, uint16_t* dst_k,
+                                   uint16_t* dst_v, void* stream) {
+  zf_status st = check_cache(cache, /*need_comp=*/false, /*need_raw=*/false, /*need_dir=*/true);
+  if (st != ZF_OK) return st;
+  if (n < 0) return ZF_ERR_INVALID_ARGUMENT;
+  if (n == 0) return ZF_OK;
+  if (!page_ids || !dst_k || !dst_v || !aligned16(dst_k) || !aligned16(dst_v)) return ZF_ERR_INVALID_ARGUMENT;
+  if (cache->num_kv_heads > 65535) return ZF_ERR_UNSUPPORTED;
+  CodecArgs a{};
+  a.k_comp = cache->k_comp; a.v_comp = cache->v_comp; a.k_raw = cache->k_raw; a.v_raw = cache->v_raw;
+  a.dir = cache->dir; a.status = cache->status;
+  a.dst_k = dst_k; a.dst_v = dst_v; a.page_ids = page_ids;
+  a.num_pages = cache->num_pages; a.hkv = cache->num_kv_heads; a.page_size = cache->page_size;
+  a.num_raw = cache->num_raw_slots;
+  decompress_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
+}

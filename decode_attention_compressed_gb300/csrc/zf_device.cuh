@@ -1,0 +1,190 @@
+// Device-side building blocks shared by the libzf kernels (sm_103a): PTX wrappers for mbarriers,
+// 1-D bulk (TMA) copies, the warp MMA and matrix transpose, the block storage order, and the
+// in-register rebuild of BF16 values from a compressed block.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/zf.h"
+
+namespace zf {
+
+constexpr int kSlotBytes = ZF_SLOT_BYTES;        // 784
+constexpr int kRawBlockBytes = ZF_RAW_BLOCK_BYTES;
+constexpr int kHeaderAt = 768;
+constexpr int kEscapesAt = 772;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // a pipeline wait gives up after 2 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Bounded: returns false after
+// kWaitTimeoutNs (or 2^30 polls), so a broken pipeline never hangs the GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+  return false;
+}
+
+// ------------------------------------------------------------------------------- bulk copies
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+// 1-D bulk copy global -> shared, completion signalled on `bar` as transaction bytes.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------- warp MMA
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col).
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 16-bit matrix held one row pair per lane (lane l: row l/4, cols 2(l%4)..+1).
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Round two floats to BF16 (nearest even) and pack: `lo` in bits 0-15, `hi` in bits 16-31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+// ------------------------------------------------------------------------- block storage order
+// Storage position of natural (token tau, channel gamma) of a 16x32 block.  The block is stored
+// in the register order of the m16n8k16 A operand: lane = 4*groupID + threadID_in_group holds
+// rows groupID (+8) and columns 2*threadID_in_group (+1, +8, +9) of each 16x16 half.
+__host__ __device__ __forceinline__ int block_position(bool is_value, int tau, int gamma) {
+  const int half = gamma >> 4;
+  const int row = is_value ? (gamma & 15) : tau;
+  const int col = is_value ? tau : (gamma & 15);
+  const int lane = 4 * (row & 7) + ((col & 7) >> 1);
+  const int r = 4 * (col >> 3) + 2 * (row >> 3) + (col & 1);
+  return 16 * lane + 8 * half + r;
+}
+
+// ------------------------------------------------------------------------- in-register rebuild
+// Eight values from 8 low bytes (lo0: values 0-3, lo1: values 4-7) and one code word
+// (byte k = code k | code k+4 << 4).  A code is sign << 3 | exponent offset; the high byte of a
+// value is sign << 7 | (base/2 + offset).  `base4` holds base/2 in every byte: base/2 + offset
+// is the 7-bit exponent>>1 field, so one 32-bit add fills four high bytes without any carry
+// crossing a byte.  Output: four BF16 pairs, value 2i in the low half of out[i].
+__device__ __forceinline__ void rebuild8(uint32_t lo0, uint32_t lo1, uint32_t code, uint32_t base4,
+                                         uint32_t* out) {
+  const uint32_t n0 = code & 0x0F0F0F0Fu;            // codes of values 0..3, one per byte
+  const uint32_t n1 = (code >> 4) & 0x0F0F0F0Fu;     // codes of values 4..7
+  // n * 0x11 copies each nibble into both halves of its byte; keep bit 7 (sign) and bits 0-2.
+  const uint32_t h0 = ((n0 * 0x11u) & 0x87878787u) + base4;
+  const uint32_t h1 = ((n1 * 0x11u) & 0x87878787u) + base4;
+  out[0] = __byte_perm(lo0, h0, 0x5140);
+  out[1] = __byte_perm(lo0, h0, 0x7362);
+  out[2] = __byte_perm(lo1, h1, 0x5140);
+  out[3] = __byte_perm(lo1, h1, 0x7362);
+}
+
+// Replace the exponent>>1 field of escaped values owned by this lane (positions 16*lane..+15).
+__device__ __forceinline__ void patch_escapes(const uint8_t* slot, uint32_t n_esc, int lane, uint32_t (&a)[8]) {
+  for (uint32_t e = 0; e < n_esc; ++e) {
+    const uint32_t entry = *reinterpret_cast<const uint16_t*>(slot + kEscapesAt + 2 * e);
+    const uint32_t p = entry >> 7;
+    if ((p >> 4) == static_cast<uint32_t>(lane)) {
+      const uint32_t idx = p & 15u;
+      const uint32_t shift = (idx & 1u) ? 24u : 8u;
+      const uint32_t mask = 0x7Fu << shift;
+      const uint32_t val = (entry & 0x7Fu) << shift;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((idx >> 1) == static_cast<uint32_t>(i)) a[i] = (a[i] & ~mask) | val;
+    }
+  }
+}
+
+// This lane's 16 values (storage positions 16*lane..16*lane+15) of a compressed block in
+// shared or global memory.
+__device__ __forceinline__ void rebuild_lane(const uint8_t* slot, int lane, uint32_t (&a)[8]) {
+  const uint32_t header = *reinterpret_cast<const uint32_t*>(slot + kHeaderAt);
+  const uint4 lo = *reinterpret_cast<const uint4*>(slot + 16 * lane);
+  const uint2 code = *reinterpret_cast<const uint2*>(slot + 512 + 8 * lane);
+  const uint32_t base4 = (header & 0x7Fu) * 0x01010101u;
+  rebuild8(lo.x, lo.y, code.x, base4, &a[0]);
+  rebuild8(lo.z, lo.w, code.y, base4, &a[4]);
+  const uint32_t n_esc = (header >> 8) & 7u;
+  if (n_esc) patch_escapes(slot, n_esc, lane, a);
+}
+
+__device__ __forceinline__ void load_raw_lane(const uint8_t* block, int lane, uint32_t (&a)[8]) {
+  const uint4 x = *reinterpret_cast<const uint4*>(block + 32 * lane);
+  const uint4 y = *reinterpret_cast<const uint4*>(block + 32 * lane + 16);
+  a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+  a[4] = y.x; a[5] = y.y; a[6] = y.z; a[7] = y.w;
+}
+
+__device__ __forceinline__ void report(int32_t* status, int32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace zf

@@ -124,15 +124,14 @@ def make_layer(w: Workload, layer: int = 0, device="cpu", seq_lens=None) -> Laye
         perm = torch.randperm(total, generator=gen, device=dev).cpu()
     else:
         perm = torch.arange(total)
+    counts = torch.tensor(npages, dtype=torch.int64)
+    req = torch.repeat_interleave(torch.arange(B), counts)                 # request of each pool slot
+    first = torch.cumsum(counts, 0) - counts
+    idx_in_req = torch.arange(total) - torch.repeat_interleave(first, counts)
     table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    table[req, idx_in_req] = perm.to(torch.int32)
     n_valid = torch.zeros(total, dtype=torch.int32)
-    at = 0
-    for b in range(B):
-        ids = perm[at:at + npages[b]]
-        table[b, : npages[b]] = ids.to(torch.int32)
-        for i in range(npages[b]):
-            n_valid[ids[i]] = min(P, int(lens_cpu[b]) - i * P)
-        at += npages[b]
+    n_valid[perm] = torch.clamp(lens_cpu[req] - idx_in_req * P, max=P).to(torch.int32)
 
     K = torch.randn(total, Hkv, P, D, generator=gen, device=dev) * s
     if w.spike_prob > 0:

@@ -1,0 +1,191 @@
+"""Thin Python binding over libzf.so (C ABI in include/zf.h).
+
+Argument marshalling only: torch tensors provide device memory and the current CUDA stream; every
+step of encoding, decompression and attention runs in the library's CUDA kernels.  The library is
+loaded on first use and a missing library raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libzf.so")
+
+HEAD_DIM = 128
+SLOT_BYTES = 784
+RAW_BLOCK_BYTES = 1024
+DIR_COMPRESSED = -1
+DIR_INVALID = -2
+ENCODE_FORCE_RAW = 1
+DEV_BAD_PAGE_ID, DEV_BAD_RAW_SLOT, DEV_BAD_N_VALID = 0x1, 0x2, 0x4
+DEV_BAD_SEQ_LEN, DEV_BAD_DIR, DEV_TIMEOUT = 0x8, 0x10, 0x20
+
+_c_int32, _c_void_p, _c_size_t, _c_float = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+
+
+class ZfCacheDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_pages", _c_int32), ("num_kv_heads", _c_int32), ("head_dim", _c_int32),
+        ("page_size", _c_int32), ("num_raw_slots", _c_int32), ("reserved", _c_int32),
+        ("k_comp", _c_void_p), ("v_comp", _c_void_p), ("k_raw", _c_void_p), ("v_raw", _c_void_p),
+        ("dir", _c_void_p), ("status", _c_void_p),
+    ]
+
+
+# name -> (restype, argtypes), mirroring include/zf.h
+SIGNATURES = {
+    "zf_status_string": (ctypes.c_char_p, [_c_int32]),
+    "zf_page_head_bytes": (_c_size_t, [_c_int32, _c_int32]),
+    "zf_encode_pages": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                   _c_void_p, _c_int32, _c_int32, _c_void_p]),
+    "zf_decompress": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p, _c_void_p]),
+    "zf_decode_attn_workspace_size": (_c_size_t, [_c_int32, _c_int32, _c_int32, _c_int32, _c_int32]),
+    "zf_decode_attn": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_void_p, _c_int32,
+                                  _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
+    "zf_dense_decode_attn": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_void_p,
+                                        _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p, _c_size_t,
+                                        _c_void_p]),
+}
+
+_LIB = None
+
+
+class ZfError(RuntimeError):
+    pass
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libzf.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ZfError(f"{LIB_PATH} is missing: build it with `python -m decode_attention_compressed_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = handle
+    return _LIB
+
+
+def status_string(code: int) -> str:
+    return lib().zf_status_string(code).decode()
+
+
+def _check(name: str, code: int):
+    if code != 0:
+        raise ZfError(f"{name}: {status_string(code)} ({code})")
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev_i32(x, device):
+    return torch.as_tensor(x, dtype=torch.int32, device=device).contiguous()
+
+
+class Cache:
+    """One layer's paged cache in device memory, laid out as include/zf.h describes.
+
+    k_comp/v_comp: [num_pages][Hkv][P/4 * 784] uint8; k_raw/v_raw: [num_raw][Hkv][P/4 * 512] int16
+    (BF16 bits); dir: [num_pages][Hkv] int32; status: one int32 device word.
+    """
+
+    def __init__(self, num_pages, num_kv_heads, page_size, num_raw_slots, device="cuda", compressed=True):
+        nblk = page_size // 4
+        self.num_pages, self.num_kv_heads, self.page_size = num_pages, num_kv_heads, page_size
+        self.num_raw_slots = num_raw_slots
+        dev = torch.device(device)
+        if compressed:
+            self.k_comp = torch.empty((num_pages, num_kv_heads, nblk * SLOT_BYTES), dtype=torch.uint8, device=dev)
+            self.v_comp = torch.empty_like(self.k_comp)
+            self.dir = torch.full((num_pages, num_kv_heads), DIR_INVALID, dtype=torch.int32, device=dev)
+        else:
+            self.k_comp = self.v_comp = self.dir = None
+        self.k_raw = torch.empty((num_raw_slots, num_kv_heads, nblk * 512), dtype=torch.int16, device=dev)
+        self.v_raw = torch.empty_like(self.k_raw)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    @property
+    def device(self):
+        return self.status.device
+
+    def desc(self) -> ZfCacheDesc:
+        return ZfCacheDesc(self.num_pages, self.num_kv_heads, HEAD_DIM, self.page_size, self.num_raw_slots, 0,
+                           _ptr(self.k_comp), _ptr(self.v_comp), _ptr(self.k_raw), _ptr(self.v_raw),
+                           _ptr(self.dir), _ptr(self.status))
+
+    def status_word(self) -> int:
+        return int(self.status.item())
+
+    def compressed_bytes(self) -> int:
+        """Bytes the cache's pools occupy."""
+        return sum(t.numel() * t.element_size() for t in (self.k_comp, self.v_comp, self.k_raw, self.v_raw, self.dir)
+                   if t is not None)
+
+
+def encode_pages(cache: Cache, src_k, src_v, page_ids, n_valid, raw_slots=None, force_raw=False, stream=None):
+    """Compress (or store raw) pages: src_k/src_v [n][Hkv][P][128] int16 BF16 bits on the device."""
+    dev = cache.device
+    src_k, src_v = src_k.contiguous(), src_v.contiguous()
+    n = int(src_k.shape[0])
+    ids = _dev_i32(page_ids, dev)
+    nv = _dev_i32(n_valid, dev)
+    rs = _dev_i32(raw_slots, dev) if raw_slots is not None else _dev_i32([-1] * n, dev)
+    d = cache.desc()
+    code = lib().zf_encode_pages(ctypes.byref(d), _ptr(src_k), _ptr(src_v), _ptr(ids), _ptr(nv), _ptr(rs), n,
+                                 ENCODE_FORCE_RAW if force_raw else 0, _stream(stream))
+    _check("zf_encode_pages", code)
+    return ids, nv, rs          # keep them alive until the stream has consumed them
+
+
+def decompress(cache: Cache, page_ids, stream=None):
+    dev = cache.device
+    ids = _dev_i32(page_ids, dev)
+    n = int(ids.numel())
+    k = torch.empty((n, cache.num_kv_heads, cache.page_size, HEAD_DIM), dtype=torch.int16, device=dev)
+    v = torch.empty_like(k)
+    d = cache.desc()
+    _check("zf_decompress", lib().zf_decompress(ctypes.byref(d), _ptr(ids), n, _ptr(k), _ptr(v), _stream(stream)))
+    return k, v
+
+
+def workspace_size(batch, num_q_heads, num_kv_heads, page_size, max_pages) -> int:
+    return int(lib().zf_decode_attn_workspace_size(batch, num_q_heads, num_kv_heads, page_size, max_pages))
+
+
+def decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse=None, workspace=None,
+                stream=None, dense=False):
+    """Decode attention over the cache.  q [B][Hq][128] int16 (BF16 bits), page_table [B][max_pages]
+    int32, seq_lens [B] int32, all on the device.  Returns (out [B][Hq][128] f32, lse [B][Hq] f32).
+    dense=True runs zf_dense_decode_attn on the raw pool (page id = raw slot)."""
+    B, Hq, _ = q.shape
+    max_pages = int(page_table.shape[1])
+    scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else scale
+    dev = cache.device
+    if out is None:
+        out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    need = workspace_size(B, Hq, cache.num_kv_heads, cache.page_size, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    d = cache.desc()
+    fn = lib().zf_dense_decode_attn if dense else lib().zf_decode_attn
+    code = fn(ctypes.byref(d), _ptr(q), B, Hq, _ptr(page_table), max_pages, _ptr(seq_lens), scale, _ptr(out),
+              _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("zf_dense_decode_attn" if dense else "zf_decode_attn", code)
+    return out, lse
+
+
+def dense_decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, **kw):
+    return decode_attn(cache, q, page_table, seq_lens, scale, dense=True, **kw)

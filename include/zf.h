@@ -1,0 +1,185 @@
+/*
+ * zf.h — C ABI of libzf: decode attention over a losslessly compressed BF16 paged KV cache,
+ * hand-written CUDA for GB300 (sm_103a).
+ *
+ * The method follows "ZipFusion: Fusing Lossless KV Decompression with Attention for Efficient
+ * LLM Decoding": full pages are compressed into fixed-layout blocks (§III.B, Fig. 2), the
+ * attention kernel copies compressed blocks from HBM to shared memory and rebuilds the exact
+ * BF16 bit patterns in registers with integer operations right before the tensor-core
+ * instructions (§III.C), partially filled pages stay uncompressed (§III.D), and split-KV partial
+ * results are combined by a split-result merge (§IV.B).
+ *
+ * General rules for every call below
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library never allocates,
+ *    frees or keeps them.  All arrays are dense, row-major, and 16-byte aligned.
+ *  - BF16 values are passed as their 16-bit patterns (uint16_t).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call only enqueues
+ *    work on `stream` and returns; results are ready when the stream reaches that point.
+ *  - Host-side argument errors are detected before anything is launched and returned as a
+ *    negative zf_status.  Data-dependent errors found on the device (an out-of-range page id,
+ *    a page that needed raw storage but got none, a pipeline wait that gave up) never fault:
+ *    the offending page is skipped and a bit is OR-ed into the optional device status word
+ *    zf_cache.status (ZF_DEV_* below), which the caller may read after synchronising.
+ *  - The library keeps no global state; concurrent calls on different streams are safe as long
+ *    as they do not write the same memory.
+ *
+ * Data layout of one layer's cache (head_dim is fixed at 128, page_size P is a multiple of 16):
+ *  - A BLOCK is 16 consecutive tokens x 32 consecutive channels of one (page, kv head, K|V):
+ *    512 values.  A page head holds P/16 tiles x 4 channel groups = P/4 blocks, tile-major.
+ *  - Storage order inside a block (ZipFusion §III.C: keys and values are arranged for their
+ *    operand roles): position p = 16*lane + 8*half + r is element r of `lane` in the A operand of
+ *    the warp MMA m16n8k16 (PTX ISA, "Matrix Fragments for mma.m16n8k16"): for K the A operand
+ *    is the 16x16 tile (rows tokens, columns channels 16*half..+15); for V it is the transposed
+ *    tile (rows channels 16*half..+15, columns tokens).
+ *  - Compressed block, 784 bytes: [0,512) the values' low bytes in storage order;
+ *    [512,768) 4-bit codes (bit 3 sign, bits 0-2 exponent offset), byte 4m+k = code[8m+k] |
+ *    code[8m+k+4] << 4; [768,772) header u32 = base/2 | n_escapes << 8 | 1 << 24 (format 1,
+ *    other bits 0); [772,784) up to six u16 escapes (position << 7 | exponent >> 1), ascending.
+ *    base is the block's minimum exponent rounded down to even when every exponent fits
+ *    [base, base+15] (ZipFusion's rule); otherwise the smallest even base whose window reaches
+ *    the maximum exponent, with the (at most 6) lower values listed as escapes.
+ *  - Raw block, 1024 bytes: the 512 BF16 values in storage order.
+ *  - k_comp/v_comp: [num_pages][num_kv_heads][P/4 blocks][784 bytes]  (slot of each page id)
+ *    k_raw/v_raw:   [num_raw_slots][num_kv_heads][P/4 blocks][512 BF16]
+ *    dir:           [num_pages][num_kv_heads] int32: ZF_DIR_COMPRESSED, a raw slot index >= 0,
+ *                   or ZF_DIR_INVALID.
+ */
+#ifndef ZF_H
+#define ZF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t zf_status;
+#define ZF_OK 0
+#define ZF_ERR_INVALID_ARGUMENT (-1)   /* null pointer, bad size, misaligned pointer, bad shape */
+#define ZF_ERR_UNSUPPORTED (-2)        /* valid but outside what this build handles */
+#define ZF_ERR_WORKSPACE_TOO_SMALL (-3)
+#define ZF_ERR_CUDA (-4)               /* a CUDA runtime call failed (launch or attribute) */
+
+/* Bits of the device status word (zf_cache.status). */
+#define ZF_DEV_BAD_PAGE_ID 0x1         /* page id outside [0, num_pages) */
+#define ZF_DEV_BAD_RAW_SLOT 0x2        /* a page head needed raw storage and its raw slot was missing or out of range */
+#define ZF_DEV_BAD_N_VALID 0x4         /* n_valid outside [0, page_size] */
+#define ZF_DEV_BAD_SEQ_LEN 0x8         /* seq_len outside [0, max_pages_per_req * page_size] */
+#define ZF_DEV_BAD_DIR 0x10            /* directory entry neither compressed nor a valid raw slot */
+#define ZF_DEV_TIMEOUT 0x20            /* a shared-memory pipeline wait gave up */
+
+#define ZF_HEAD_DIM 128
+#define ZF_BLOCK_TOKENS 16
+#define ZF_BLOCK_CHANNELS 32
+#define ZF_SLOT_BYTES 784
+#define ZF_RAW_BLOCK_BYTES 1024
+#define ZF_MAX_ESCAPES 6
+#define ZF_FORMAT_VERSION 1
+#define ZF_DIR_COMPRESSED (-1)
+#define ZF_DIR_INVALID (-2)
+#define ZF_MAX_BATCH 4096              /* requests per zf_decode_attn call */
+#define ZF_MAX_PAGE_SIZE 128
+
+#define ZF_ENCODE_FORCE_RAW 1          /* zf_encode_pages flag: store every page raw */
+
+/* One layer's cache.  Only the pointers a call uses must be valid for that call. */
+typedef struct zf_cache {
+  int32_t num_pages;      /* page ids are in [0, num_pages) */
+  int32_t num_kv_heads;
+  int32_t head_dim;       /* must be 128 */
+  int32_t page_size;      /* tokens per page, multiple of 16, <= ZF_MAX_PAGE_SIZE */
+  int32_t num_raw_slots;  /* raw page slots in k_raw / v_raw (may be 0) */
+  int32_t reserved;       /* must be 0 */
+  uint8_t* k_comp;        /* [num_pages][num_kv_heads][page_size/4][784] */
+  uint8_t* v_comp;
+  uint16_t* k_raw;        /* [num_raw_slots][num_kv_heads][page_size/4][512] */
+  uint16_t* v_raw;
+  int32_t* dir;           /* [num_pages][num_kv_heads] */
+  int32_t* status;        /* optional device word; ZF_DEV_* bits are OR-ed in; NULL = not reported */
+} zf_cache;
+
+/* Human-readable name of a status code.  Never returns NULL. */
+const char* zf_status_string(zf_status status);
+
+/* Bytes of one (page, kv head) record of K (or of V): compressed = page_size/4 * 784,
+ * raw = page_size/4 * 1024.  Returns 0 for an unsupported page size. */
+size_t zf_page_head_bytes(int32_t page_size, int32_t compressed);
+
+/*
+ * zf_encode_pages — compress (or store raw) n full or partial pages.
+ * ZipFusion §III.B (format) and §III.D (page lifecycle: a partially filled page stays
+ * uncompressed so decoding can keep appending to it; a full page is compressed later and keeps
+ * its page id).
+ *   src_k, src_v: [n][num_kv_heads][page_size][128] BF16, natural (token, channel) layout; page i
+ *                 of the call is written under id page_ids[i].
+ *   page_ids:     [n] distinct ids in [0, num_pages).
+ *   n_valid:      [n] tokens filled in each page, 0..page_size.  Pages with n_valid < page_size,
+ *                 pages with a block that needs more than 6 escapes, and every page when
+ *                 flags & ZF_ENCODE_FORCE_RAW are stored raw in slot raw_slots[i] (values past
+ *                 n_valid are stored as given).  Otherwise the page goes to its compressed slot.
+ *   raw_slots:    [n] raw slot per page, or -1 when none is available (a page that then needs
+ *                 raw storage gets ZF_DIR_INVALID and ZF_DEV_BAD_RAW_SLOT).
+ *   Writes k_comp/v_comp or k_raw/v_raw and dir[page_ids[i]][*].  All pointers are device
+ *   pointers; n == 0 is a no-op.  The source must not alias the cache.
+ */
+zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_k, const uint16_t* src_v,
+                          const int32_t* page_ids, const int32_t* n_valid,
+                          const int32_t* raw_slots, int32_t n, int32_t flags, void* stream);
+
+/*
+ * zf_decompress — bit-exact inverse of zf_encode_pages, used for verification.
+ *   page_ids: [n] ids; dst_k, dst_v: [n][num_kv_heads][page_size][128] BF16 in natural layout.
+ *   A page head whose directory entry is invalid is written as zeros (and ZF_DEV_BAD_DIR set).
+ */
+zf_status zf_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n,
+                        uint16_t* dst_k, uint16_t* dst_v, void* stream);
+
+/* Workspace bytes zf_decode_attn / zf_dense_decode_attn need for these sizes on the current
+ * device (split-KV partial outputs and log-sum-exps).  0 on invalid sizes. */
+size_t zf_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t page_size, int32_t max_pages_per_req);
+
+/*
+ * zf_decode_attn — batched single-token decode attention over the compressed paged cache.
+ * ZipFusion §III.C (attention consumes compressed blocks copied HBM->shared memory and rebuilt in
+ * registers, raw blocks need no rebuild; page metadata for later pages is fetched while earlier
+ * pages are attended) and §IV.B (split-KV with a split-result merge).
+ *   q:          [batch][num_q_heads][128] BF16.  Query head h reads kv head h / (num_q_heads /
+ *               num_kv_heads); num_q_heads must be a multiple of num_kv_heads.
+ *   page_table: [batch][max_pages_per_req] page ids; token t of request b is slot t % page_size
+ *               of page page_table[b][t / page_size].  Entries past a request's pages are unread.
+ *   seq_lens:   [batch] device int32 context lengths, 0..max_pages_per_req * page_size.
+ *   softmax_scale: multiplies q.k before the softmax.
+ *   out:        [batch][num_q_heads][128] float32 = sum_t softmax(scale * q.k)_t v_t.
+ *   lse:        [batch][num_q_heads] float32, natural-log log-sum-exp of scale * q.k.
+ *               A request with seq_len 0 gets out = 0 and lse = -inf.
+ *   workspace:  device buffer of at least zf_decode_attn_workspace_size(...) bytes, any contents;
+ *               it must not be shared with a concurrent call.
+ *   batch <= ZF_MAX_BATCH.  Two kernels are enqueued (attention, then merge); results are
+ *   deterministic (no atomics).
+ */
+zf_status zf_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch,
+                         int32_t num_q_heads, const int32_t* page_table, int32_t max_pages_per_req,
+                         const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * zf_dense_decode_attn — the same decode attention over an uncompressed BF16 paged cache: page
+ * id p of the page table is read from raw slot p of cache->k_raw / cache->v_raw (raw block
+ * layout above; zf_encode_pages with ZF_ENCODE_FORCE_RAW and raw_slots = page_ids builds it).
+ * cache->num_raw_slots bounds the page ids; dir and the compressed pools are not used.
+ * Same grid, pipeline and merge as zf_decode_attn; it reads 1024-byte blocks instead of
+ * 784-byte ones and skips the reconstruction.  Arguments as for zf_decode_attn.
+ */
+zf_status zf_dense_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch,
+                               int32_t num_q_heads, const int32_t* page_table,
+                               int32_t max_pages_per_req, const int32_t* seq_lens,
+                               float softmax_scale, float* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZF_H */

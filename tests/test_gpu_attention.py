@@ -1,0 +1,191 @@
+"""GPU parity of zf_decode_attn and zf_dense_decode_attn against the float64 oracle.
+
+Bars (float32 kernel vs float64 oracle on the same BF16 inputs): max-abs 4e-3 and mean-abs 5e-4
+on `out`, 1e-3 on `lse`; empty contexts give out = 0 and lse = -inf exactly.
+Small cases compare every output; the full-size workloads, run in the benchmark's launch
+configuration, compare sampled (request, head) outputs that the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_compressed_gb300 import inputs as I
+from oracle import zf_oracle as O
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def zf():
+    return H.zf_module()
+
+
+def W(B, hq, hkv, P, ctx, **kw):
+    return I.Workload("case", B, hq, hkv, P, ctx, **kw)
+
+
+CASES = {
+    "one_token": (W(1, 8, 2, 16, 1), [1]),
+    "ragged_gqa4": (W(2, 8, 2, 16, 67, pool="random", seed=3), [17, 67]),
+    "mha": (W(3, 4, 4, 16, 33, seed=4), [33, 16, 5]),
+    "gqa7_spikes": (W(3, 14, 2, 16, 300, pool="random", k_sigma=0.7, n_outlier=0, spike_prob=0.02,
+                      v_std=0.5, seed=5), [300, 48, 1]),
+    "gqa8": (W(2, 16, 2, 16, 200, seed=6), [200, 129]),
+    "gqa12_two_slices": (W(2, 24, 2, 16, 150, pool="random", seed=7), [150, 31]),
+    "gqa1_page64": (W(3, 2, 2, 64, 260, pool="random", seed=8), [260, 65, 7]),
+    "page64_gqa4": (W(2, 16, 4, 64, 700, pool="random", seed=9), [700, 129]),
+    "empty_requests": (W(4, 8, 2, 16, 40, seed=10), [0, 40, 0, 3]),
+    "long_chunked": (W(1, 8, 1, 16, 3000, seed=11), [3000]),
+}
+
+
+def _run(zf, layer, cache, dense=False):
+    dev = torch.device("cuda")
+    q = layer.q.to(dev)
+    table = layer.page_table.to(dev)
+    lens = layer.seq_lens.to(dev)
+    out, lse = (zf.dense_decode_attn if dense else zf.decode_attn)(cache, q, table, lens, layer.scale)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _oracle(layer):
+    oc = H.oracle_cache_from(layer, O)
+    return O.decode_attention(H.np_bits(layer.q), oc, layer.page_table.numpy(), layer.seq_lens.numpy(), layer.scale)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_small_cases(zf, name):
+    w, lens = CASES[name]
+    layer = I.make_layer(w, seq_lens=lens)
+    ref_out, ref_lse = _oracle(layer)
+    gc = H.gpu_cache_from(layer, zf)
+    out, lse = _run(zf, layer, gc)
+    H.compare_attention(out, lse, ref_out, ref_lse)
+    assert gc.status_word() == 0
+    dc = H.gpu_cache_from(layer, zf, force_raw=True)
+    dout, dlse = _run(zf, layer, dc, dense=True)
+    H.compare_attention(dout, dlse, ref_out, ref_lse)
+    assert dc.status_word() == 0
+
+
+def test_mixed_raw_and_compressed_pages(zf):
+    """Full pages forced raw next to compressed ones and raw partial tails, in one request."""
+    w = W(2, 12, 3, 16, 250, pool="random", seed=12)
+    layer = I.make_layer(w, seq_lens=[250, 181])
+    gc = H.gpu_cache_from(layer, zf)
+    some = list(range(0, layer.num_pages, 3))
+    zf.encode_pages(gc, layer.k_pages[some].cuda(), layer.v_pages[some].cuda(), some, [16] * len(some), some,
+                    force_raw=True)
+    torch.cuda.synchronize()
+    d = gc.dir.cpu().numpy()
+    assert (d == -1).any() and (d >= 0).any()
+    ref_out, ref_lse = _oracle(layer)
+    out, lse = _run(zf, layer, gc)
+    H.compare_attention(out, lse, ref_out, ref_lse)
+
+
+def test_deterministic(zf):
+    w, lens = CASES["gqa7_spikes"]
+    layer = I.make_layer(w, seq_lens=lens)
+    gc = H.gpu_cache_from(layer, zf)
+    a = _run(zf, layer, gc)
+    b = _run(zf, layer, gc)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_bad_page_ids_are_reported_not_faulted(zf):
+    w = W(2, 8, 2, 16, 64, seed=13)
+    layer = I.make_layer(w, seq_lens=[64, 40])
+    gc = H.gpu_cache_from(layer, zf)
+    table = layer.page_table.clone()
+    table[0, 1] = 10 ** 6
+    table[1, 0] = -5
+    out, lse = zf.decode_attn(gc, layer.q.cuda(), table.cuda(), layer.seq_lens.cuda(), layer.scale)
+    torch.cuda.synchronize()
+    assert gc.status_word() & zf.DEV_BAD_PAGE_ID
+    assert torch.isfinite(out).all()
+    lens = torch.tensor([64, 10 ** 6], dtype=torch.int32)
+    gc.status.zero_()
+    zf.decode_attn(gc, layer.q.cuda(), layer.page_table.cuda(), lens.cuda(), layer.scale)
+    torch.cuda.synchronize()
+    assert gc.status_word() & zf.DEV_BAD_SEQ_LEN
+
+
+SMALL_WORKLOADS = {
+    "tiny": (I.WORKLOADS["tiny"], None),
+    "llama7b_mha": (I.scaled(I.WORKLOADS["llama7b_mha_512"], ctx=256), None),
+    "llama3_8b_batched": (I.scaled(I.WORKLOADS["llama3_8b_batched"], batch=5, ctx=700, ctx_min=100), None),
+    "qwen2_7b_maxbatch": (I.scaled(I.WORKLOADS["qwen2_7b_maxbatch"], batch=3, ctx=800), None),
+    "long_ctx": (I.scaled(I.WORKLOADS["long_ctx"], batch=2, ctx=1500), [1500, 1473]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_WORKLOADS))
+def test_workload_shapes_small(zf, name):
+    w, lens = SMALL_WORKLOADS[name]
+    layer = I.make_layer(w, seq_lens=lens)
+    ref_out, ref_lse = _oracle(layer)
+    gc = H.gpu_cache_from(layer, zf)
+    out, lse = _run(zf, layer, gc)
+    H.compare_attention(out, lse, ref_out, ref_lse)
+    dc = H.gpu_cache_from(layer, zf, force_raw=True)
+    H.compare_attention(*_run(zf, layer, dc, dense=True), ref_out, ref_lse)
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+FULL = ["tiny", "llama7b_mha_512", "llama7b_mha_2048", "llama7b_mha_8192", "llama3_8b_batched",
+        "qwen2_7b_maxbatch", "long_ctx"]
+
+
+def sampled_reference(layer, pairs):
+    """Oracle outputs for the sampled (request, query head) pairs, one by one, from the BF16
+    source pages of that request and kv head."""
+    w = layer.workload
+    P, group = w.page_size, w.group
+    table = layer.page_table.cpu().numpy()
+    lens = layer.seq_lens.cpu().numpy()
+    q = H.np_bits(layer.q)
+    out = np.zeros((w.batch, w.num_q_heads, 128))
+    lse = np.full((w.batch, w.num_q_heads), -math.inf)
+    for b, h in pairs:
+        L = int(lens[b])
+        pages = torch.as_tensor(table[b, : -(-L // P)], dtype=torch.long, device=layer.k_pages.device)
+        g = h // group
+        K = H.np_bits(layer.k_pages[pages, g].reshape(-1, 128))[:L]
+        V = H.np_bits(layer.v_pages[pages, g].reshape(-1, 128))[:L]
+        out[b, h], lse[b, h], _ = O.attention_one(O.bf16_to_f64(q[b, h]), O.bf16_to_f64(K), O.bf16_to_f64(V),
+                                                  layer.scale)
+    return out, lse
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(zf, name):
+    w = I.WORKLOADS[name]
+    layer = I.make_layer(w, layer=0, device="cuda")
+    npg = layer.num_pages
+    # encode exactly as the benchmark does: page i keeps id i, raw slot i offered for partial tails
+    tails = torch.nonzero(layer.n_valid < w.page_size).flatten().cpu().tolist()
+    raw_slots = [-1] * npg
+    for j, p in enumerate(tails):
+        raw_slots[p] = j
+    gc = zf.Cache(npg, w.num_kv_heads, w.page_size, max(len(tails), 1) + 64)
+    zf.encode_pages(gc, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, raw_slots)
+    out, lse = zf.decode_attn(gc, layer.q, layer.page_table, layer.seq_lens, layer.scale)
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    rng = np.random.default_rng(0)
+    pairs = sorted({(int(rng.integers(w.batch)), int(rng.integers(w.num_q_heads))) for _ in range(6)}
+                   | {(0, 0), (w.batch - 1, w.num_q_heads - 1)})
+    ref_out, ref_lse = sampled_reference(layer, pairs)
+    H.compare_attention(out, lse, ref_out, ref_lse, pairs=pairs)
+    # properties at any size: finite, |out| bounded by max |v| of the request's head
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    # the sampled pages decompress to their source bits
+    sample_pages = sorted({int(x) for x in rng.integers(0, npg, 16)})
+    k, v = zf.decompress(gc, sample_pages)
+    idx = torch.as_tensor(sample_pages, device="cuda")
+    assert torch.equal(k, layer.k_pages[idx]) and torch.equal(v, layer.v_pages[idx])

@@ -1,0 +1,142 @@
+"""GPU parity of zf_encode_pages / zf_decompress against the oracle: bit-exact bytes, directory and
+status on the workloads' distributions and on adversarial blocks; decompress returns every
+source bit."""
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_compressed_gb300 import inputs as I
+from oracle import zf_oracle as O
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def zf():
+    return H.zf_module()
+
+
+SMALL = {
+    "tiny": I.WORKLOADS["tiny"],
+    "llama7b_mha": I.scaled(I.WORKLOADS["llama7b_mha_512"], ctx=128),
+    "llama3_8b_batched": I.scaled(I.WORKLOADS["llama3_8b_batched"], batch=4, ctx=300, ctx_min=40),
+    "qwen2_7b_maxbatch": I.scaled(I.WORKLOADS["qwen2_7b_maxbatch"], batch=3, ctx=600),
+    "long_ctx": I.scaled(I.WORKLOADS["long_ctx"], batch=2, ctx=400),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_encode_matches_oracle_bit_exactly(zf, name):
+    layer = I.make_layer(SMALL[name])
+    gc = H.gpu_cache_from(layer, zf)
+    oc = H.oracle_cache_from(layer, O)
+    H.assert_caches_equal(gc, oc)
+    # the distributions exercise both kinds of storage and the escape list
+    assert (oc.dir == -1).any()
+    if name in ("llama3_8b_batched", "long_ctx"):
+        assert (oc.dir >= 0).any()          # partial tail pages stay raw
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_decompress_returns_every_bit(zf, name):
+    layer = I.make_layer(SMALL[name])
+    gc = H.gpu_cache_from(layer, zf)
+    k, v = zf.decompress(gc, list(range(layer.num_pages)))
+    torch.cuda.synchronize()
+    assert torch.equal(k.cpu(), layer.k_pages) and torch.equal(v.cpu(), layer.v_pages)
+    assert gc.status_word() == 0
+
+
+def _pattern(s, e, f):
+    return (s << 15) | (e << 7) | f
+
+
+def adversarial_pages(seed=0, hkv=2, P=16):
+    """Pages whose blocks cover: all 65,536 BF16 patterns inside a window, escapes of every
+    pattern class, exactly 6 and 7 escapes, window boundaries, NaN/Inf/zero/subnormal blocks."""
+    rng = np.random.default_rng(seed)
+    blocks = []
+    for E in range(0, 256, 2):                              # every pattern, compressed
+        vals = np.array([_pattern(s, e, f) for s in (0, 1) for e in (E, E + 1) for f in range(128)])
+        blocks.append(rng.permutation(vals))
+    filler = np.array([_pattern(s, e, f) for s in (0, 1) for e in range(240, 256) for f in range(128)])
+    low = rng.permutation(np.array([_pattern(s, e, f) for e in range(240) for s in (0, 1) for f in range(128)]))
+    for i in range(0, 6 * 40, 6):                           # 6 escapes (base/2 = 120)
+        v = np.concatenate([low[i:i + 6], rng.choice(filler, 506, replace=False)])
+        v[-1] = _pattern(1, 255, 3)
+        blocks.append(rng.permutation(v))
+    seven = np.full(512, _pattern(0, 127, 0))
+    seven[:7] = _pattern(0, 20, 1)                           # 7 escapes: the page must stay raw
+    blocks.append(rng.permutation(seven))
+    b = np.full(512, _pattern(0, 110, 5))
+    b[:3] = _pattern(0, 101, 1)
+    b[3] = _pattern(1, 116, 9)                               # odd minimum, range 15 -> 3 escapes
+    blocks.append(rng.permutation(b))
+    b = np.full(512, _pattern(0, 100, 5))
+    b[0] = _pattern(1, 115, 0)                               # range 15 from an even minimum
+    blocks.append(rng.permutation(b))
+    for sp in (0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0, 0xFFFF, 0x0001, 0x807F):
+        blocks.append(np.full(512, sp))
+    zero_base = rng.integers(0, 128, 512) | (rng.integers(0, 2, 512) << 15)   # exponents 0 (subnormals)
+    blocks.append(zero_base)
+    per_page = hkv * 2 * (P // 4)
+    while len(blocks) % per_page:
+        blocks.append(rng.integers(0, 65536, 512))        # random patterns (mostly raw-bound)
+    blocks = np.stack(blocks).astype(np.uint16).reshape(-1, hkv, 2, P // 16, 4, 16, 32)
+    # -> [n][hkv][K|V][tile][group][16][32] -> natural pages [n][hkv][P][128]
+    pages = blocks.transpose(0, 1, 2, 3, 5, 4, 6).reshape(-1, hkv, 2, P, 128)
+    return pages[:, :, 0], pages[:, :, 1]
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_adversarial_blocks(zf, P):
+    k, v = adversarial_pages(hkv=2, P=P)
+    n = k.shape[0]
+    kt = torch.from_numpy(k.view(np.int16).copy()).cuda()
+    vt = torch.from_numpy(v.view(np.int16).copy()).cuda()
+    gc = zf.Cache(n, 2, P, n)
+    zf.encode_pages(gc, kt, vt, list(range(n)), [P] * n, list(range(n)))
+    oc = O.Cache(num_pages=n, num_kv_heads=2, page_size=P, num_raw=n)
+    O.encode_pages(oc, k, v, list(range(n)), [P] * n, list(range(n)))
+    torch.cuda.synchronize()
+    H.assert_caches_equal(gc, oc)
+    assert (oc.dir == -1).sum() > 0 and (oc.dir >= 0).sum() > 0
+    dk, dv = zf.decompress(gc, list(range(n)))
+    torch.cuda.synchronize()
+    assert torch.equal(dk, kt) and torch.equal(dv, vt)
+
+
+def test_page_lifecycle_and_status(zf):
+    """ZipFusion §III.D on the GPU: partial pages raw, full pages compressed under their id,
+    missing raw slots and bad ids reported in the status word, forced raw storage."""
+    w = I.scaled(I.WORKLOADS["llama3_8b_batched"], batch=2, ctx=90, ctx_min=20)
+    layer = I.make_layer(w)
+    n = layer.num_pages
+    ids = list(reversed(range(n)))                       # page i of the call gets id n-1-i
+    perm = np.random.default_rng(0).permutation(n + 2)
+    raw = [(-1 if i % 3 == 0 else int(perm[i])) for i in range(n)]   # distinct slots
+    gc = H.gpu_cache_from(layer, zf, raw_slots=raw, page_ids=ids, extra_raw=2)
+    oc = H.oracle_cache_from(layer, O, raw_slots=raw, page_ids=ids, extra_raw=2)
+    H.assert_caches_equal(gc, oc)
+    # bad page id and bad n_valid
+    gc2 = zf.Cache(4, w.num_kv_heads, w.page_size, 4)
+    src = layer.k_pages[:3].cuda()
+    zf.encode_pages(gc2, src, src, [0, 9, 2], [16, 16, 17], [0, 1, 2])
+    torch.cuda.synchronize()
+    assert gc2.status_word() == (zf.DEV_BAD_PAGE_ID | zf.DEV_BAD_N_VALID)
+    d = gc2.dir.cpu().numpy()
+    assert (d[0] == -1).all() and (d[2] == -2).all() and (d[1] == -2).all()
+    # forced raw
+    gc3 = H.gpu_cache_from(layer, zf, force_raw=True)
+    oc3 = H.oracle_cache_from(layer, O, force_raw=True)
+    H.assert_caches_equal(gc3, oc3)
+    assert (oc3.dir >= 0).all()
+
+
+def test_decompress_of_invalid_entries(zf):
+    gc = zf.Cache(3, 2, 16, 1)
+    k, v = zf.decompress(gc, [0, 2, 7])
+    torch.cuda.synchronize()
+    assert (k == 0).all() and (v == 0).all()
+    assert gc.status_word() == (zf.DEV_BAD_DIR | zf.DEV_BAD_PAGE_ID)

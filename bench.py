@@ -159,15 +159,12 @@ def setup_layers(zf, I, w, device):
     for l in range(w.layers):
         layer = I.make_layer(w, layer=l, device=device)
         npg = layer.num_pages
-        tails = torch.nonzero(layer.n_valid < w.page_size).flatten().cpu().tolist()
         extra = 0
         if w.name == "long_ctx":
             extra = 8 * w.batch       # spare page ids for the appended tokens
-        raw_slots = [-1] * npg
-        for j, p in enumerate(tails):
-            raw_slots[p] = j
-        cache = zf.Cache(npg + extra, w.num_kv_heads, w.page_size, len(tails) + 4 * w.batch + 8, device=device)
-        zf.encode_pages(cache, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, raw_slots)
+        # page i keeps id i; raw slot i is its fallback (partial tails, blocks with > 6 escapes)
+        cache = zf.Cache(npg + extra, w.num_kv_heads, w.page_size, npg + extra, device=device)
+        zf.encode_pages(cache, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, list(range(npg)))
         dense = zf.Cache(npg + extra, w.num_kv_heads, w.page_size, npg + extra, device=device, compressed=False)
         zf.encode_pages(dense, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, list(range(npg)),
                         force_raw=True)
@@ -206,6 +203,33 @@ def prefill_encode_ms(zf, I, device):
     return ms, src_bytes / (ms * 1e-3) / 1e9
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks of the default process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_requests(batch: int, rank: int, world: int):
+    """Requests a replica owns when a batch is sharded over ranks (contiguous, balanced)."""
+    per, extra = divmod(batch, world)
+    start = rank * per + min(rank, extra)
+    return list(range(start, start + per + (1 if rank < extra else 0)))
+
+
+def workload_of(args):
+    from decode_attention_compressed_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload]
+    kw = {}
+    if args.layers is not None:
+        kw["layers"] = min(args.layers, w.layers)
+    if args.batch is not None:
+        kw["batch"] = min(args.batch, w.batch)
+    return I.scaled(w, **kw) if kw else w
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -218,7 +242,7 @@ def run_gpu(args, rank, world, local_rank):
 
     device = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(device)
-    w = I.WORKLOADS[args.workload]
+    w = workload_of(args)
     layers = setup_layers(zf, I, w, device)
     stream = torch.cuda.current_stream()
     outs = [(torch.empty(w.batch, w.num_q_heads, 128, device=device),
@@ -268,9 +292,7 @@ def run_gpu(args, rank, world, local_rank):
         ms = s.elapsed_time(e)
         calls = [a.elapsed_time(b) for row in per_call for (a, b) in row]
         if world > 1:
-            t = torch.tensor([ms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+            ms = max_over_ranks(ms, device)
         return ms / steps, statistics.mean(calls), clk.summary()
 
     if append is not None:
@@ -316,8 +338,8 @@ def run_gpu(args, rank, world, local_rank):
     comp_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], True) for ent in layers)
     dense_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], False) for ent in layers)
     uncompressed = sum(dense_equiv_bytes(ent["layer"]) for ent in layers)
-    stored = sum(ent["cache"].compressed_bytes() for ent in layers)
-    dense_stored = sum(ent["dense"].compressed_bytes() for ent in layers)
+    stored = sum(ent["cache"].stored_bytes(ent["num_pages"]) for ent in layers)
+    dense_stored = sum(ent["num_pages"] * w.num_kv_heads * 2 * w.page_size * 128 * 2 for ent in layers)
     per_launch = comp_bytes / len(layers)
     peak, peak_kind = read_peaks()
     achieved = per_launch / (call_ms * 1e-3) / 1e9
@@ -342,6 +364,8 @@ def run_gpu(args, rank, world, local_rank):
         pct_of_hbm_peak=round(100 * comp_bytes / (ms_step * 1e-3) / 1e9 / peak, 1),
         pct_of_8tbs_spec=round(100 * comp_bytes / (ms_step * 1e-3) / 1e9 / SPEC_HBM_GBS, 1),
         compression_ratio=round(dense_stored / stored, 4),
+        raw_page_heads=round(sum(float((ent["dirs"][: ent["num_pages"]] >= 0).float().mean()) for ent in layers)
+                             / len(layers), 6),
         bytes_read_ratio=round(dense_bytes / comp_bytes, 4),
         dense={"us_per_step": round(dense_ms_step * 1e3, 3), "kv_gbs": round(dense_bytes / (dense_ms_step * 1e-3) / 1e9, 1),
                "pct_of_hbm_peak": round(100 * dense_bytes / (dense_ms_step * 1e-3) / 1e9 / peak, 1),
@@ -470,7 +494,7 @@ def run_reference(args, rank):
     from oracle import zf_oracle as O
     if rank != 0:
         return None
-    w = I.WORKLOADS[args.workload]
+    w = workload_of(args)
     run = oracle_sample(I, O, w, 1)
     scale = w.batch * w.num_kv_heads * w.layers
     for _ in range(args.warmup):
@@ -500,6 +524,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="use only the first N layers of a multi-layer workload (profiling captures)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="use only the first B requests (profiling captures on a smaller device footprint)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -522,7 +550,7 @@ def main():
     if rank == 0:
         from decode_attention_compressed_gb300 import inputs as I
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(I.WORKLOADS[args.workload])
+            res["cpu_baseline"] = cpu_baseline(workload_of(args))
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

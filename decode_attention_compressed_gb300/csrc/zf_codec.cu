@@ -261,9 +261,11 @@ using namespace zf;
 extern "C" zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_k, const uint16_t* src_v,
                                      const int32_t* page_ids, const int32_t* n_valid, const int32_t* raw_slots,
                                      int32_t n, int32_t flags, void* stream) {
-  zf_status st = check_cache(cache, /*need_comp=*/true, /*need_raw=*/false, /*need_dir=*/true);
+  if (flags & ~ZF_ENCODE_FORCE_RAW) return ZF_ERR_INVALID_ARGUMENT;
+  // a forced-raw encode never writes the compressed pools, so they may be absent
+  zf_status st = check_cache(cache, /*need_comp=*/!(flags & ZF_ENCODE_FORCE_RAW), /*need_raw=*/false, /*need_dir=*/true);
   if (st != ZF_OK) return st;
-  if (n < 0 || (flags & ~ZF_ENCODE_FORCE_RAW)) return ZF_ERR_INVALID_ARGUMENT;
+  if (n < 0) return ZF_ERR_INVALID_ARGUMENT;
   if (n == 0) return ZF_OK;
   if (!src_k || !src_v || !page_ids || !n_valid || !aligned16(src_k) || !aligned16(src_v))
     return ZF_ERR_INVALID_ARGUMENT;

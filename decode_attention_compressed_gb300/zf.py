@@ -108,9 +108,9 @@ class Cache:
         if compressed:
             self.k_comp = torch.empty((num_pages, num_kv_heads, nblk * SLOT_BYTES), dtype=torch.uint8, device=dev)
             self.v_comp = torch.empty_like(self.k_comp)
-            self.dir = torch.full((num_pages, num_kv_heads), DIR_INVALID, dtype=torch.int32, device=dev)
         else:
-            self.k_comp = self.v_comp = self.dir = None
+            self.k_comp = self.v_comp = None       # dense cache: raw slots only (zf_dense_decode_attn)
+        self.dir = torch.full((num_pages, num_kv_heads), DIR_INVALID, dtype=torch.int32, device=dev)
         self.k_raw = torch.empty((num_raw_slots, num_kv_heads, nblk * 512), dtype=torch.int16, device=dev)
         self.v_raw = torch.empty_like(self.k_raw)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -127,10 +127,17 @@ class Cache:
     def status_word(self) -> int:
         return int(self.status.item())
 
-    def compressed_bytes(self) -> int:
-        """Bytes the cache's pools occupy."""
-        return sum(t.numel() * t.element_size() for t in (self.k_comp, self.v_comp, self.k_raw, self.v_raw, self.dir)
-                   if t is not None)
+    def stored_bytes(self, num_pages=None) -> int:
+        """Bytes the first `num_pages` pages actually occupy (synchronises): every page head costs
+        its compressed record or its raw record, plus its directory entry."""
+        n = self.num_pages if num_pages is None else num_pages
+        nblk = self.page_size // 4
+        if self.k_comp is None:
+            return n * self.num_kv_heads * 2 * nblk * RAW_BLOCK_BYTES
+        d = self.dir[:n].cpu()
+        comp = int((d == DIR_COMPRESSED).sum())
+        raw = int((d >= 0).sum())
+        return 2 * nblk * (comp * SLOT_BYTES + raw * RAW_BLOCK_BYTES) + d.numel() * 4
 
 
 def encode_pages(cache: Cache, src_k, src_v, page_ids, n_valid, raw_slots=None, force_raw=False, stream=None):

@@ -73,6 +73,8 @@ def test_encode_rejects_bad_arguments_before_launch(zf):
     assert _encode(zf, _desc(zf), n=-1) == -1
     assert _encode(zf, _desc(zf), flags=4) == -1
     assert _encode(zf, _desc(zf), n=0) == 0                      # nothing to do, nothing launched
+    assert _encode(zf, _desc(zf, k_comp=None), n=0) == -1
+    assert _encode(zf, _desc(zf, k_comp=None), n=0, flags=1) == 0  # forced raw needs no compressed pools
 
 
 def test_decompress_rejects_bad_arguments(zf):

@@ -167,13 +167,9 @@ def test_full_size_sampled(zf, name):
     w = I.WORKLOADS[name]
     layer = I.make_layer(w, layer=0, device="cuda")
     npg = layer.num_pages
-    # encode exactly as the benchmark does: page i keeps id i, raw slot i offered for partial tails
-    tails = torch.nonzero(layer.n_valid < w.page_size).flatten().cpu().tolist()
-    raw_slots = [-1] * npg
-    for j, p in enumerate(tails):
-        raw_slots[p] = j
-    gc = zf.Cache(npg, w.num_kv_heads, w.page_size, max(len(tails), 1) + 64)
-    zf.encode_pages(gc, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, raw_slots)
+    # encode exactly as the benchmark does: page i keeps id i and may fall back to raw slot i
+    gc = zf.Cache(npg, w.num_kv_heads, w.page_size, npg)
+    zf.encode_pages(gc, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, list(range(npg)))
     out, lse = zf.decode_attn(gc, layer.q, layer.page_table, layer.seq_lens, layer.scale)
     torch.cuda.synchronize()
     assert gc.status_word() == 0
@@ -184,6 +180,15 @@ def test_full_size_sampled(zf, name):
     H.compare_attention(out, lse, ref_out, ref_lse, pairs=pairs)
     # properties at any size: finite, |out| bounded by max |v| of the request's head
     assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    # the dense comparator on the same inputs, same launch configuration
+    dc = zf.Cache(npg, w.num_kv_heads, w.page_size, npg, compressed=False)
+    zf.encode_pages(dc, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, list(range(npg)),
+                    force_raw=True)
+    dout, dlse = zf.dense_decode_attn(dc, layer.q, layer.page_table, layer.seq_lens, layer.scale)
+    torch.cuda.synchronize()
+    assert dc.status_word() == 0
+    H.compare_attention(dout, dlse, ref_out, ref_lse, pairs=pairs)
+    del dc, dout, dlse
     # the sampled pages decompress to their source bits
     sample_pages = sorted({int(x) for x in rng.integers(0, npg, 16)})
     k, v = zf.decompress(gc, sample_pages)

@@ -26,6 +26,7 @@
 #include <stdint.h>
 
 #include <climits>
+#include <mutex>
 
 #include "zf_device.cuh"
 #include "zf_host.h"
@@ -646,4 +647,51 @@ extern "C" zf_status zf_dense_decode_attn(const zf_cache* cache, const uint16_t*
                                           void* workspace, size_t workspace_bytes, void* stream) {
   return launch_attention<false>(cache, q, batch, num_q_heads, page_table, max_pages_per_req, seq_lens,
                                  softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------------------------
+// zf_decode_attn_static: the same attention for callers that cannot allocate device memory.
+// Its split-KV scratch is this file-scope device array (held by every GPU that loads the library
+// until exit).  Host code must not pass `g_static_workspace` itself to a kernel: on the host the
+// name is only a stand-in, so the device address is looked up once per device below.
+static __device__ __align__(256) unsigned char g_static_workspace[ZF_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kStaticMaxDevices = 64;
+std::mutex g_static_mutex;
+void* g_static_address[kStaticMaxDevices] = {};
+
+// Address of g_static_workspace on the current device (looked up on the first call per device).
+zf_status static_workspace_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZF_ERR_CUDA;
+  if (dev < 0 || dev >= kStaticMaxDevices) return ZF_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_address[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return ZF_ERR_CUDA;
+    g_static_address[dev] = p;
+  }
+  *out = g_static_address[dev];
+  return ZF_OK;
+}
+}  // namespace
+
+extern "C" zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t* q, int32_t batch,
+                                           int32_t num_q_heads, const int32_t* page_table,
+                                           int32_t max_pages_per_req, const int32_t* seq_lens,
+                                           float softmax_scale, float* out, float* lse, void* stream) {
+  if (!cache) return ZF_ERR_INVALID_ARGUMENT;
+  if (!attn_shape_ok(batch, num_q_heads, cache->num_kv_heads, max_pages_per_req)) return ZF_ERR_INVALID_ARGUMENT;
+  const int P = cache->page_size;
+  if (P < ZF_BLOCK_TOKENS || P % ZF_BLOCK_TOKENS || P > ZF_MAX_PAGE_SIZE) return ZF_ERR_INVALID_ARGUMENT;
+  int sms = 0;
+  zf_status st = current_sm_count(&sms);
+  if (st != ZF_OK) return st;
+  const Plan p = make_plan(batch, num_q_heads, cache->num_kv_heads, P, max_pages_per_req, sms);
+  if (p.ws_bytes > ZF_STATIC_WORKSPACE_BYTES) return ZF_ERR_STATIC_WORKSPACE_EXCEEDED;
+  void* ws = nullptr;
+  if ((st = static_workspace_address(&ws)) != ZF_OK) return st;
+  return launch_attention<true>(cache, q, batch, num_q_heads, page_table, max_pages_per_req, seq_lens,
+                                softmax_scale, out, lse, ws, ZF_STATIC_WORKSPACE_BYTES, stream);
 }

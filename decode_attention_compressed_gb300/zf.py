@@ -48,6 +48,8 @@ SIGNATURES = {
     "zf_dense_decode_attn": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_void_p,
                                         _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p, _c_size_t,
                                         _c_void_p]),
+    "zf_decode_attn_static": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_void_p,
+                                         _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p]),
 }
 
 _LIB = None
@@ -196,3 +198,25 @@ def decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse
 
 def dense_decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, **kw):
     return decode_attn(cache, q, page_table, seq_lens, scale, dense=True, **kw)
+
+
+STATIC_WORKSPACE_BYTES = 32 << 20
+ERR_STATIC_WORKSPACE_EXCEEDED = -5
+
+
+def decode_attn_static(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse=None, stream=None):
+    """zf_decode_attn_static: the same attention without a caller-provided workspace, for callers
+    that cannot allocate device memory (the library's 32 MiB static scratch array is used).
+    Calls must not overlap on the GPU; the first call on a device must precede any stream capture."""
+    B, Hq, _ = q.shape
+    scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else scale
+    dev = cache.device
+    if out is None:
+        out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    d = cache.desc()
+    code = lib().zf_decode_attn_static(ctypes.byref(d), _ptr(q), B, Hq, _ptr(page_table), int(page_table.shape[1]),
+                                       _ptr(seq_lens), scale, _ptr(out), _ptr(lse), _stream(stream))
+    _check("zf_decode_attn_static", code)
+    return out, lse

@@ -60,6 +60,7 @@ typedef int32_t zf_status;
 #define ZF_ERR_UNSUPPORTED (-2)        /* valid but outside what this build handles */
 #define ZF_ERR_WORKSPACE_TOO_SMALL (-3)
 #define ZF_ERR_CUDA (-4)               /* a CUDA runtime call failed (launch or attribute) */
+#define ZF_ERR_STATIC_WORKSPACE_EXCEEDED (-5) /* zf_decode_attn_static: sizes need more than ZF_STATIC_WORKSPACE_BYTES */
 
 /* Bits of the device status word (zf_cache.status). */
 #define ZF_DEV_BAD_PAGE_ID 0x1         /* page id outside [0, num_pages) */
@@ -177,6 +178,32 @@ zf_status zf_dense_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t
                                int32_t max_pages_per_req, const int32_t* seq_lens,
                                float softmax_scale, float* out, float* lse, void* workspace,
                                size_t workspace_bytes, void* stream);
+
+/*
+ * zf_decode_attn_static — zf_decode_attn for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for integration only.
+ *   Some callers have no way to hand the library a workspace: for example a kernel plugin inside
+ *   a host engine that owns every byte of device memory through its own pool and exposes no
+ *   scratch hook, or a latency-critical path where cudaMalloc (which can synchronise the device)
+ *   is not allowed.  This call takes the same arguments as zf_decode_attn minus the workspace and
+ *   uses a scratch array compiled into the library instead: ZF_STATIC_WORKSPACE_BYTES (32 MiB) of
+ *   device memory that every GPU which loads libzf holds until the process exits.  It calls no
+ *   cudaMalloc, cudaFree or allocating library routine.
+ *   - Sizes whose split-KV partials need more than ZF_STATIC_WORKSPACE_BYTES (see
+ *     zf_decode_attn_workspace_size) are rejected with ZF_ERR_STATIC_WORKSPACE_EXCEEDED before
+ *     anything is launched.
+ *   - The first call on a device looks up that device's address of the array (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the previous call's contents (nothing in it has
+ *     to start at zero).  Calls that overlap on the GPU (other streams, other threads) race on it:
+ *     serialise them.
+ *   Results are identical to zf_decode_attn's for the same inputs.
+ */
+#define ZF_STATIC_WORKSPACE_BYTES (32u << 20)
+zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t* q, int32_t batch,
+                                int32_t num_q_heads, const int32_t* page_table,
+                                int32_t max_pages_per_req, const int32_t* seq_lens,
+                                float softmax_scale, float* out, float* lse, void* stream);
 
 #ifdef __cplusplus
 }

@@ -271,36 +271,65 @@ def run_gpu(args, rank, world, local_rank):
             if events is not None:
                 events[i][1].record()
 
-    def timed(dense=False, steps=args.steps, warmup=args.warmup):
+    def capture(fn):
+        """fn() captured once into a CUDA graph (after one eager warm-up on a side stream)."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(run, steps=args.steps, warmup=args.warmup, per_call=False, dense=False):
+        """Device time per step of `run` (CUDA events on the launching stream; max over ranks),
+        the mean per-call duration when per_call is set (eager only), and the clocks seen."""
         for _ in range(warmup):
-            step(dense)
+            run()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        per_call = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                     for _ in layers] for _ in range(steps)]
+        events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in layers] for _ in range(steps)] if per_call else None
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(local_rank) as clk:
             s.record()
             for k in range(steps):
-                step(dense, per_call[k])
+                if per_call:
+                    step(dense, events[k])
+                else:
+                    run()
             e.record()
             torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         ms = s.elapsed_time(e)
-        calls = [a.elapsed_time(b) for row in per_call for (a, b) in row]
+        calls = [x.elapsed_time(y) for row in events for (x, y) in row] if per_call else None
         if world > 1:
             ms = max_over_ranks(ms, device)
-        return ms / steps, statistics.mean(calls), clk.summary()
+        return ms / steps, (statistics.mean(calls) if calls else None), clk.summary()
 
-    if append is not None:
+    use_graph = append is None           # the append step changes pointers every step: eager
+    if use_graph:
+        g_comp = capture(lambda: step(False))
+        g_dense = capture(lambda: step(True))
+        ms_step, _, clocks = timed(g_comp.replay)
+        call_ms = ms_step / len(layers)
+        dense_ms_step, _, dense_clocks = timed(g_dense.replay)
+        dense_call_ms = dense_ms_step / len(layers)
+        eager_ms, _, _ = timed(lambda: step(False))
+        eager_dense_ms, _, _ = timed(lambda: step(True))
+    else:
         append.reset()
-    ms_step, call_ms, clocks = timed(False)
-    if append is not None:
+        ms_step, call_ms, clocks = timed(lambda: step(False), per_call=True)
         append.reset()
-    dense_ms_step, dense_call_ms, dense_clocks = timed(True)
+        dense_ms_step, dense_call_ms, dense_clocks = timed(lambda: step(True), per_call=True, dense=True)
+        eager_ms, eager_dense_ms = ms_step, dense_ms_step
 
     # end to end through the public API: q (and seq_lens) from pinned host memory, out + lse back
     q_host = [ent["layer"].q.cpu().pin_memory() for ent in layers]
@@ -320,20 +349,14 @@ def run_gpu(args, rank, world, local_rank):
             out_host[i][1].copy_(outs[i][1], non_blocking=True)
 
     if append is None:
-        for _ in range(args.warmup):
-            e2e_step()
-        torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
-        for _ in range(args.steps):
-            e2e_step()
-        e.record()
-        torch.cuda.synchronize()
-        e2e_ms = s.elapsed_time(e) / args.steps
+        g_e2e = capture(e2e_step)
+        e2e_ms, _, _ = timed(g_e2e.replay)
+        e2e_eager_ms, _, _ = timed(e2e_step)
         h2d = sum(q.numel() * 2 + l.numel() * 4 for q, l in zip(q_host, lens_host))
         d2h = sum(o.numel() * 4 + l.numel() * 4 for o, l in out_host)
     else:
-        e2e_ms, h2d, d2h = None, 0, 0
+        e2e_ms = e2e_eager_ms = None
+        h2d = d2h = 0
 
     comp_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], True) for ent in layers)
     dense_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], False) for ent in layers)
@@ -371,13 +394,19 @@ def run_gpu(args, rank, world, local_rank):
                "pct_of_hbm_peak": round(100 * dense_bytes / (dense_ms_step * 1e-3) / 1e9 / peak, 1),
                "call_us": round(dense_call_ms * 1e3, 3), "clocks": dense_clocks},
         speedup_vs_dense=round(dense_ms_step / ms_step, 4),
-        roofline={"kernel": "attn_kernel<compressed> + merge_kernel (one zf_decode_attn call)", "bound": "hbm",
+        launch_mode="cuda_graph (one graph per decode step)" if use_graph else "eager",
+        eager={"us_per_step": round(eager_ms * 1e3, 3), "dense_us_per_step": round(eager_dense_ms * 1e3, 3),
+               "e2e_us_per_step": round(e2e_eager_ms * 1e3, 3) if e2e_eager_ms else None},
+        roofline={"kernel": "attn_kernel<compressed> + merge_kernel (one zf_decode_attn call; "
+                            + ("step time / layers" if use_graph else "events around each call") + ")",
+                  "bound": "hbm",
                   "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                   "peak_source": peak_kind, "bytes_per_launch": int(per_launch), "call_us": round(call_ms * 1e3, 3),
                   "traffic": read_traffic(w.name)},
         e2e={"value": round(e2e_ms * 1e3, 3) if e2e_ms else None, "unit": "us/step", "h2d_bytes_per_step": h2d,
              "d2h_bytes_per_step": d2h},
         gpu_launches=args.steps * len(layers) * 2 + (args.steps if append is not None else 0),
+        gpu_launches_note="per timed region of the compressed path: attention + merge per layer (+1 encode per step when appending)",
         clocks=clocks, **extra,
     )
     return result

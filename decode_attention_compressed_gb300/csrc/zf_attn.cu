@@ -10,16 +10,21 @@
 // Design for sm_103a (one CTA per SM, persistent over a static list of work items):
 //  * work item = (request b, kv head g, head slice, chunk of pages); the chunk size is picked on
 //    the host so that items fill the SMs in whole rounds;
-//  * warp 8 is the producer: it resolves page ids through the page table and the directory and
-//    streams every 16-token tile (K 4 blocks + V 4 blocks) into a 16-stage shared-memory ring
-//    with 1-D bulk copies (cp.async.bulk, mbarrier transaction counts, L2 evict-first);
-//  * warps 0-7 consume tiles round-robin.  A warp rebuilds K blocks straight into m16n8k16
-//    A fragments (the storage order is the fragment order), computes S^T = K Q^T for up to 8
-//    query heads of the GQA group (one MMA n-tile), runs the online softmax in the log2 domain,
-//    transposes P^T into B fragments with movmatrix, and accumulates O^T = V^T P^T with P split
-//    into a BF16 high part and a BF16 remainder (two MMAs) so P keeps ~16 significant bits;
-//  * at the end of an item the 8 warps' (m, l, O) are merged through shared memory and written
-//    as the item's partial (or as the final output when the request has a single chunk);
+//  * warp 10 is the metadata warp: it runs one item ahead, resolving the item's page ids through
+//    the page table and the directory into shared memory and bulk-copying the item's q rows;
+//  * warps 0-9 each stream their own 16-token tiles (tile u of an item goes to warp u % 10) into
+//    two private 8 KB shared-memory stages with 16-byte cp.async, prefetching the next tile while
+//    computing the current one.  (Measured on GB300: 1-D bulk copies of 3-6 KB issued by one
+//    thread per SM complete about one per 0.55 us, far below HBM bandwidth, while per-warp
+//    16-byte async copies of the same scattered tiles reach 6.6-6.8 TB/s.)
+//  * per tile, a warp rebuilds K blocks straight into m16n8k16 A fragments (the storage order is
+//    the fragment order), computes S^T = K Q^T for up to 8 query heads of the GQA group (one MMA
+//    n-tile), runs the online softmax in the log2 domain (the running max is only raised, after a
+//    warp vote, when a score exceeds it by more than 8), transposes P^T into B fragments with
+//    movmatrix, and accumulates O^T = V^T P^T with P split into a BF16 high part and a BF16
+//    remainder (two MMAs) so P keeps ~16 significant bits; V blocks are rebuilt right before use;
+//  * at the end of an item the warps' (m, l, O) are merged through shared memory and written as
+//    the item's partial (or as the final output when the request has a single chunk);
 //  * a second kernel merges each (request, head)'s chunk partials by log-sum-exp.
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -33,18 +38,26 @@
 
 namespace zf {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 16;
-constexpr int kStageBytes = 8192;                   // K tile + V tile, raw size
-constexpr int kHalfStage = 4096;
+// Per-variant shape: the compressed kernel runs 15 consumer warps with 6272-byte stages (one
+// compressed K+V tile; raw tiles load K, then V, into the same stage); the dense kernel runs 10
+// consumer warps with 8192-byte stages (one raw K+V tile).  Plus one metadata warp.
+template <bool kCompressed>
+struct Cfg {
+  static constexpr int kWarps = kCompressed ? 15 : 10;
+  static constexpr int kStageBytes = kCompressed ? 6272 : 8192;
+  static constexpr int kVOffset = kCompressed ? 3136 : 4096;   // V tile within a stage
+  static constexpr int kThreads = (kWarps + 1) * 32;
+};
+constexpr int kWarpStages = 2;
 constexpr int kTileCompBytes = 4 * kSlotBytes;      // 3136: one 16-token tile of K (or V), compressed
 constexpr int kTileRawBytes = 4 * kRawBlockBytes;   // 4096
 constexpr int kHeadsPerSlice = 8;                   // MMA n
+constexpr int kMaxChunkPages = 256;                 // pages per work item (metadata buffer size)
 constexpr int kOStride = 132;                       // padded combine row (conflict-free writes)
 constexpr int kCombineWarpFloats = kHeadsPerSlice * kOStride + 16;
 constexpr int kItemOverheadTiles = 4;               // planner: fixed cost of an item, in tiles
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;           // log2 units: p <= 2^8 between max updates
 
 enum : int { kKindComp = 0, kKindRaw = 1, kKindInvalid = 2 };
 
@@ -73,86 +86,196 @@ struct Plan {
   size_t part_o_bytes = 0, ws_bytes = 0, smem = 0;
 };
 
-struct SmemLayout {
-  size_t stages, full, empty, kinds, flag, combine, lens, prefix, total;
+// What the metadata warp publishes for an item.
+struct ItemDesc {
+  int b, c, g, t0, t1, units, h0, nh, single;
 };
 
+struct SmemLayout {
+  size_t stages, item_full, item_empty, misc, desc, meta, qbuf, prefix, total;
+};
+
+template <bool kCompressed>
 __host__ __device__ inline SmemLayout smem_layout(int batch) {
+  using C = Cfg<kCompressed>;
   SmemLayout s;
   size_t at = 0;
-  s.stages = at; at += static_cast<size_t>(kStages) * kStageBytes;
-  s.full = at; at += kStages * 8;
-  s.empty = at; at += kStages * 8;
-  s.kinds = at; at += kStages * 4;
-  s.flag = at; at += 16;
-  s.combine = at; at += static_cast<size_t>(kConsumerWarps) * kCombineWarpFloats * 4;
-  s.lens = at; at += static_cast<size_t>(batch) * 4;
+  s.stages = at; at += static_cast<size_t>(C::kWarps) * kWarpStages * C::kStageBytes;
+  s.item_full = at; at += 2 * 8;
+  s.item_empty = at; at += 2 * 8;
+  s.misc = at; at += 16 + 16 * 4;                         // [0] abort flag, [16..] combine stage per warp
+  s.desc = at; at += 2 * 64;
+  s.meta = at; at += 2 * kMaxChunkPages * 4;
+  s.qbuf = at; at += 2 * kHeadsPerSlice * ZF_HEAD_DIM * 2;
   s.prefix = at; at += static_cast<size_t>(batch + 1) * 4;
   s.total = (at + 127) & ~static_cast<size_t>(127);
   return s;
 }
 
-struct Item {
-  int b, g, s, c, p0, p1, t0, t1, units;
-};
+template <int kWarps>
+__device__ __forceinline__ void consumer_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+}
 
-__device__ __forceinline__ Item decode_item(const AttnArgs& a, const int* lens, const int* prefix, int item) {
-  Item it;
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Item `item` of the flat list: its request, chunk, kv head, head slice, token range and tiles.
+__device__ __forceinline__ ItemDesc describe_item(const AttnArgs& a, const int* prefix, int item) {
+  ItemDesc d;
   const int per = a.hkv * a.slices;
   const int j = item / per;
   const int r = item - j * per;
-  it.g = r / a.slices;
-  it.s = r - it.g * a.slices;
+  d.g = r / a.slices;
+  const int s = r - d.g * a.slices;
   int lo = 0, hi = a.batch;                 // prefix[lo] <= j < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (prefix[mid] <= j) lo = mid; else hi = mid;
   }
-  it.b = lo;
-  it.c = j - prefix[lo];
-  const int L = lens[lo];
+  d.b = lo;
+  d.c = j - prefix[lo];
+  d.single = (prefix[lo + 1] - prefix[lo]) == 1;
+  const int L = min(max(a.seq_lens[lo], 0), a.max_pages * a.page_size);
   const int pages = (L + a.page_size - 1) / a.page_size;
-  it.p0 = it.c * a.chunk_pages;
-  it.p1 = min(it.p0 + a.chunk_pages, pages);
-  it.t0 = it.p0 * a.page_size;
-  it.t1 = min(it.p1 * a.page_size, L);
-  it.units = (it.t1 - it.t0 + 15) >> 4;
-  return it;
+  const int p0 = d.c * a.chunk_pages;
+  const int p1 = min(p0 + a.chunk_pages, pages);
+  d.t0 = p0 * a.page_size;
+  d.t1 = min(p1 * a.page_size, L);
+  d.units = (d.t1 - d.t0 + 15) >> 4;
+  d.h0 = d.g * a.group + s * kHeadsPerSlice;
+  d.nh = min(kHeadsPerSlice, a.group - s * kHeadsPerSlice);
+  return d;
 }
 
-__device__ __forceinline__ void consumer_barrier() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+// Resolve the item's pages into meta[i] = slot << 2 | kind (all 32 lanes).  All page-table loads
+// are issued before the directory loads that depend on them.
+template <bool kCompressed>
+__device__ __forceinline__ void resolve_pages(const AttnArgs& a, const ItemDesc& d, int* meta, int lane) {
+  constexpr int kPer = kMaxChunkPages / 32;
+  const int p0 = d.t0 / a.page_size;
+  const int npg = (d.t1 - d.t0 + a.page_size - 1) / a.page_size;
+  const int32_t* row = a.page_table + static_cast<size_t>(d.b) * a.max_pages + p0;
+  int pid[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = lane + 32 * k;
+    pid[k] = i < npg ? row[i] : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = lane + 32 * k;
+    if (i >= npg) break;
+    int kind = kKindInvalid, slot = 0;
+    if (kCompressed) {
+      if (pid[k] >= 0 && pid[k] < a.num_pages) {
+        const int dd = a.dir[static_cast<size_t>(pid[k]) * a.hkv + d.g];
+        if (dd == ZF_DIR_COMPRESSED) {
+          kind = kKindComp;
+          slot = pid[k];
+        } else if (dd >= 0 && dd < a.num_raw) {
+          kind = kKindRaw;
+          slot = dd;
+        } else {
+          report(a.status, ZF_DEV_BAD_DIR);
+        }
+      } else {
+        report(a.status, ZF_DEV_BAD_PAGE_ID);
+      }
+    } else if (pid[k] >= 0 && pid[k] < a.num_raw) {
+      kind = kKindRaw;
+      slot = pid[k];
+    } else {
+      report(a.status, ZF_DEV_BAD_PAGE_ID);
+    }
+    meta[i] = (slot << 2) | kind;
+  }
+}
+
+// Start the 16-byte async copies of tile u of an item into `stage`: K at 0 and V at kVOffset.  In
+// the compressed kernel a raw tile does not fit one stage: only its K half is started here and
+// the V half is fetched after QK^T (see load_raw_v).
+template <bool kCompressed>
+__device__ __forceinline__ void issue_tile(const AttnArgs& a, const ItemDesc& d, const int* meta, int u,
+                                           uint8_t* stage, int lane, uint64_t policy) {
+  using C = Cfg<kCompressed>;
+  const int tiles_per_page = a.page_size / ZF_BLOCK_TOKENS;
+  const int m = meta[u / tiles_per_page];
+  const int kind = m & 3;
+  const size_t head = static_cast<size_t>(m >> 2) * a.hkv + d.g;
+  const int t = u % tiles_per_page;
+  if (kCompressed && kind == kKindComp) {
+    const size_t off = head * a.comp_head_bytes + static_cast<size_t>(t) * kTileCompBytes;
+    const uint8_t* ks = a.k_comp + off;
+    const uint8_t* vs = a.v_comp + off;
+#pragma unroll
+    for (int v = lane; v < kTileCompBytes / 16; v += 32) {
+      cp_async16(stage + 16 * v, ks + 16 * v, policy);
+      cp_async16(stage + C::kVOffset + 16 * v, vs + 16 * v, policy);
+    }
+  } else if (kind == kKindRaw) {
+    const size_t off = head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes;
+    const uint8_t* ks = a.k_raw + off;
+#pragma unroll
+    for (int v = lane; v < kTileRawBytes / 16; v += 32) {
+      cp_async16(stage + 16 * v, ks + 16 * v, policy);
+      if (!kCompressed) cp_async16(stage + C::kVOffset + 16 * v, a.v_raw + off + 16 * v, policy);
+    }
+  }
+}
+
+// Compressed kernel, raw tile: after QK^T, fetch the V half into the same stage and wait for it.
+__device__ __forceinline__ void load_raw_v(const AttnArgs& a, const ItemDesc& d, const int* meta, int u,
+                                           uint8_t* stage, int lane, uint64_t policy) {
+  const int tiles_per_page = a.page_size / ZF_BLOCK_TOKENS;
+  const int m = meta[u / tiles_per_page];
+  const size_t head = static_cast<size_t>(m >> 2) * a.hkv + d.g;
+  const size_t off = head * a.raw_head_bytes + static_cast<size_t>(u % tiles_per_page) * kTileRawBytes;
+  __syncwarp();                                   // every lane is done reading the K half
+#pragma unroll
+  for (int v = lane; v < kTileRawBytes / 16; v += 32) cp_async16(stage + 16 * v, a.v_raw + off + 16 * v, policy);
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncwarp();
 }
 
 template <bool kCompressed>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(const AttnArgs a) {
+  using C = Cfg<kCompressed>;
+  constexpr int kWarps = C::kWarps;
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemLayout L = smem_layout(a.batch);
-  uint8_t* stages = smem + L.stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
-  int* kinds = reinterpret_cast<int*>(smem + L.kinds);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
-  float* combine = reinterpret_cast<float*>(smem + L.combine);
-  int* lens = reinterpret_cast<int*>(smem + L.lens);
+  const SmemLayout L = smem_layout<kCompressed>(a.batch);
+  uint64_t* item_full = reinterpret_cast<uint64_t*>(smem + L.item_full);
+  uint64_t* item_empty = reinterpret_cast<uint64_t*>(smem + L.item_empty);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+  int* combine_stage = reinterpret_cast<int*>(smem + L.misc + 16);
+  ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + L.desc);
+  int* meta = reinterpret_cast<int*>(smem + L.meta);
+  uint16_t* qbuf = reinterpret_cast<uint16_t*>(smem + L.qbuf);
   int* prefix = reinterpret_cast<int*>(smem + L.prefix);
+  uint8_t* stages = smem + L.stages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- prologue: barriers, clamped lengths, chunk counts and their prefix sums
-  if (tid < kStages) {
-    mbar_init(&full[tid], 1);
-    mbar_init(&empty[tid], 1);
+  // ---- prologue: barriers, chunk counts per request and their prefix sums
+  if (tid < 2) {
+    mbar_init(&item_full[tid], 1);
+    mbar_init(&item_empty[tid], kWarps);
   }
   if (tid == 0) *abort_flag = 0;
   const int max_len = a.max_pages * a.page_size;
-  for (int b = tid; b < a.batch; b += kAttnThreads) {
+  for (int b = tid; b < a.batch; b += C::kThreads) {
     int len = a.seq_lens[b];
     if (len < 0 || len > max_len) {
       if (blockIdx.x == 0) report(a.status, ZF_DEV_BAD_SEQ_LEN);
       len = min(max(len, 0), max_len);
     }
-    lens[b] = len;
     const int pages = (len + a.page_size - 1) / a.page_size;
     prefix[b + 1] = (pages + a.chunk_pages - 1) / a.chunk_pages;
   }
@@ -175,227 +298,198 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   }
   __syncthreads();
   const int total_items = prefix[a.batch] * a.hkv * a.slices;
+  const uint64_t policy = l2_evict_first_policy();
 
-  if (warp == kConsumerWarps) {
-    // ================================================================ producer warp
-    const uint64_t policy = l2_evict_first_policy();
-    uint32_t seq = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
-      const Item it = decode_item(a, lens, prefix, item);
-      const int32_t* row = a.page_table + static_cast<size_t>(it.b) * a.max_pages;
-      for (int pb = it.p0; pb < it.p1 && ok; pb += 32) {
-        // page metadata for the next 32 pages, one lane each
-        const int pi = pb + lane;
-        int kind = kKindInvalid, slot = 0;
-        if (pi < it.p1) {
-          const int pid = row[pi];
-          if (kCompressed) {
-            if (pid >= 0 && pid < a.num_pages) {
-              const int d = a.dir[static_cast<size_t>(pid) * a.hkv + it.g];
-              if (d == ZF_DIR_COMPRESSED) {
-                kind = kKindComp;
-                slot = pid;
-              } else if (d >= 0 && d < a.num_raw) {
-                kind = kKindRaw;
-                slot = d;
-              } else {
-                report(a.status, ZF_DEV_BAD_DIR);
-              }
-            } else {
-              report(a.status, ZF_DEV_BAD_PAGE_ID);
-            }
-          } else if (pid >= 0 && pid < a.num_raw) {
-            kind = kKindRaw;
-            slot = pid;
-          } else {
-            report(a.status, ZF_DEV_BAD_PAGE_ID);
-          }
+  if (warp == kWarps) {
+    // ============================================================== metadata warp
+    int k = 0;
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++k) {
+      const int buf = k & 1;
+      bool ok = true;
+      if (lane == 0) ok = !*abort_flag && mbar_wait(&item_empty[buf], ((k >> 1) & 1u) ^ 1u);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          report(a.status, ZF_DEV_TIMEOUT);
+          *abort_flag = 1;
         }
-        const int npg = min(32, it.p1 - pb);
-        for (int j = 0; j < npg; ++j) {
-          const int kind_j = __shfl_sync(0xFFFFFFFFu, kind, j);
-          const int slot_j = __shfl_sync(0xFFFFFFFFu, slot, j);
-          const int ntok = min(a.page_size, it.t1 - (pb + j) * a.page_size);
-          const int ntiles = (ntok + 15) >> 4;
-          if (lane == 0) {
-            const size_t head = static_cast<size_t>(slot_j) * a.hkv + it.g;
-            for (int t = 0; t < ntiles; ++t) {
-              const int stage = static_cast<int>(seq % kStages);
-              const uint32_t phase = (seq / kStages) & 1u;
-              if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1u)) {
-                report(a.status, ZF_DEV_TIMEOUT);
-                *abort_flag = 1;
-                ok = false;
-                break;
-              }
-              kinds[stage] = kind_j;
-              uint8_t* dst = stages + static_cast<size_t>(stage) * kStageBytes;
-              if (kind_j == kKindComp) {
-                const size_t off = head * a.comp_head_bytes + static_cast<size_t>(t) * kTileCompBytes;
-                mbar_arrive_expect_tx(&full[stage], 2 * kTileCompBytes);
-                bulk_copy_g2s(dst, a.k_comp + off, kTileCompBytes, &full[stage], policy);
-                bulk_copy_g2s(dst + kHalfStage, a.v_comp + off, kTileCompBytes, &full[stage], policy);
-              } else if (kind_j == kKindRaw) {
-                const size_t off = head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes;
-                mbar_arrive_expect_tx(&full[stage], 2 * kTileRawBytes);
-                bulk_copy_g2s(dst, a.k_raw + off, kTileRawBytes, &full[stage], policy);
-                bulk_copy_g2s(dst + kHalfStage, a.v_raw + off, kTileRawBytes, &full[stage], policy);
-              } else {
-                mbar_arrive(&full[stage]);
-              }
-              ++seq;
-            }
-          }
-          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-          if (!ok) break;
-        }
+        break;
+      }
+      const ItemDesc d = describe_item(a, prefix, item);
+      resolve_pages<kCompressed>(a, d, meta + buf * kMaxChunkPages, lane);
+      __syncwarp();
+      if (lane == 0) {
+        desc[buf] = d;
+        const uint32_t qbytes = d.nh * ZF_HEAD_DIM * 2;
+        mbar_arrive_expect_tx(&item_full[buf], qbytes);
+        bulk_copy_g2s(qbuf + buf * kHeadsPerSlice * ZF_HEAD_DIM,
+                      a.q + (static_cast<size_t>(d.b) * a.hq + d.h0) * ZF_HEAD_DIM, qbytes, &item_full[buf], policy);
       }
     }
-    if (lane == 0 && !ok) {
-      // give copies already in flight a bounded chance to land before the CTA exits
-      for (int s = 0; s < kStages; ++s) {
-        if (seq > static_cast<uint32_t>(s)) {
-          const uint32_t last = seq - 1 - ((seq - 1 - s) % kStages);
-          mbar_wait(&full[s], (last / kStages) & 1u);
-        }
-      }
+    // its own q copies must have landed before the CTA can exit (consumers that gave up waiting
+    // would not have waited for them)
+    if (lane == 0) {
+      for (int j = k - 2; j < k; ++j)
+        if (j >= 0) mbar_wait(&item_full[j & 1], (j >> 1) & 1u);
     }
     return;
   }
 
   // ================================================================== consumer warps
   const int gi = lane >> 2, ti = lane & 3;
-  uint32_t seq_base = 0;
+  uint8_t* my_stages = stages + static_cast<size_t>(warp) * kWarpStages * C::kStageBytes;
   bool aborted = false;
-  float* my_combine = combine + warp * kCombineWarpFloats;
-  for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-    const Item it = decode_item(a, lens, prefix, item);
-    const int h0 = it.g * a.group + it.s * kHeadsPerSlice;
-    const int nh = min(kHeadsPerSlice, a.group - it.s * kHeadsPerSlice);
-
-    // Q^T as the B operand (k = channel, n = head): lane holds head gi, channels 2ti(+1), +8(+9)
-    uint32_t qb[8][2];
-    {
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          a.q + (static_cast<size_t>(it.b) * a.hq + h0 + min(gi, nh - 1)) * ZF_HEAD_DIM);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        qb[ks][0] = gi < nh ? qrow[8 * ks + ti] : 0u;
-        qb[ks][1] = gi < nh ? qrow[8 * ks + ti + 4] : 0u;
-      }
+  int sidx = 0;                 // stage of the next tile to consume
+  int pending_item = -1;        // item whose first tile for this warp is already in flight
+  int k = 0;
+  for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++k) {
+    const int buf = k & 1;
+    if (!aborted && (*abort_flag || !mbar_wait(&item_full[buf], (k >> 1) & 1u))) {
+      aborted = true;
+      *abort_flag = 1;
+      report(a.status, ZF_DEV_TIMEOUT);
     }
+    const ItemDesc d = desc[buf];
+    const int* m = meta + buf * kMaxChunkPages;
+    // Q^T as the B operand (k = channel, n = head): lane holds head gi, channels 2ti(+1), +8(+9);
+    // read from shared memory at each use
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qbuf + (buf * kHeadsPerSlice + min(gi, d.nh - 1)) * ZF_HEAD_DIM);
+    const uint32_t qmask = gi < d.nh ? 0xFFFFFFFFu : 0u;
+
     float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
     float o[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    for (int k = warp; k < it.units; k += kConsumerWarps) {
-      const uint32_t s = seq_base + k;
-      const int stage = static_cast<int>(s % kStages);
-      if (!aborted && (*abort_flag || !mbar_wait(&full[stage], (s / kStages) & 1u))) {
-        aborted = true;
-        *abort_flag = 1;
-        report(a.status, ZF_DEV_TIMEOUT);
-      }
-      if (aborted) continue;
-      const int kind = kinds[stage];
-      const int ntok = min(16, it.t1 - (it.t0 + 16 * k));
-      const uint8_t* kp = stages + static_cast<size_t>(stage) * kStageBytes;
-      const uint8_t* vp = kp + kHalfStage;
+    // this warp's first tile of the item, unless it was prefetched during the previous item
+    if (!aborted && pending_item != item && warp < d.units) {
+      issue_tile<kCompressed>(a, d, m, warp, my_stages + sidx * C::kStageBytes, lane, policy);
+      cp_async_commit();
+    }
+    pending_item = -1;
 
-      // ---- S^T (16 tokens x 8 heads) = K (16 x 128) . Q^T (128 x 8)
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t va[4][8];
-      if (kCompressed && kind == kKindComp) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t ka[8];
-          rebuild_lane(kp + j * kSlotBytes, lane, ka);
-          mma_bf16(sacc, ka[0], ka[1], ka[2], ka[3], qb[2 * j][0], qb[2 * j][1]);
-          mma_bf16(sacc, ka[4], ka[5], ka[6], ka[7], qb[2 * j + 1][0], qb[2 * j + 1][1]);
+    for (int u = warp; u < d.units && !aborted; u += kWarps) {
+      // prefetch the warp's next tile: the next one of this item, or its first one of the next item
+      const int un = u + kWarps;
+      uint8_t* next_stage = my_stages + (sidx ^ 1) * C::kStageBytes;
+      if (un < d.units) {
+        issue_tile<kCompressed>(a, d, m, un, next_stage, lane, policy);
+      } else if (item + static_cast<int>(gridDim.x) < total_items) {
+        const int nb = buf ^ 1;
+        if (*abort_flag || !mbar_wait(&item_full[nb], ((k + 1) >> 1) & 1u)) {
+          aborted = true;
+          *abort_flag = 1;
+          report(a.status, ZF_DEV_TIMEOUT);
+        } else if (warp < desc[nb].units) {
+          issue_tile<kCompressed>(a, desc[nb], meta + nb * kMaxChunkPages, warp, next_stage, lane, policy);
+          pending_item = item + gridDim.x;
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) rebuild_lane(vp + j * kSlotBytes, lane, va[j]);
-      } else if (kind == kKindRaw) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t ka[8];
-          load_raw_lane(kp + j * kRawBlockBytes, lane, ka);
-          mma_bf16(sacc, ka[0], ka[1], ka[2], ka[3], qb[2 * j][0], qb[2 * j][1]);
-          mma_bf16(sacc, ka[4], ka[5], ka[6], ka[7], qb[2 * j + 1][0], qb[2 * j + 1][1]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) load_raw_lane(vp + j * kRawBlockBytes, lane, va[j]);
       }
+      cp_async_commit();
+      cp_async_wait_1();          // everything but the group just committed has landed
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);   // the stage is free once its bytes are in registers
-      if (kind == kKindInvalid) continue;
-      if (ntok < 16) {
-        // tokens past the context may hold anything (even NaN): zero their values so that
-        // p = 0 times them stays 0.  V^T fragment columns of this lane: tokens 2ti, 2ti+1 (regs
-        // 0,1,4,5) and 2ti+8, 2ti+9 (regs 2,3,6,7).
-        const uint32_t keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
-        const uint32_t keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
+      if (aborted) break;
+
+      const int kind = m[u / (a.page_size / ZF_BLOCK_TOKENS)] & 3;
+      if (kind != kKindInvalid) {
+        uint8_t* kp = my_stages + sidx * C::kStageBytes;
+        const bool comp = kCompressed && kind == kKindComp;
+        const int ntok = min(16, d.t1 - (d.t0 + 16 * u));
+
+        // ---- S^T (16 tokens x 8 heads) = K (16 x 128) . Q^T (128 x 8); two accumulation chains
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          va[j][0] &= keep_a; va[j][1] &= keep_a; va[j][4] &= keep_a; va[j][5] &= keep_a;
-          va[j][2] &= keep_b; va[j][3] &= keep_b; va[j][6] &= keep_b; va[j][7] &= keep_b;
+          uint32_t ka[8];
+          if (comp) rebuild_lane(kp + j * kSlotBytes, lane, ka);
+          else load_raw_lane(kp + j * kRawBlockBytes, lane, ka);
+          const uint32_t q0 = qrow[16 * j + ti] & qmask, q1 = qrow[16 * j + ti + 4] & qmask;
+          const uint32_t q2 = qrow[16 * j + 8 + ti] & qmask, q3 = qrow[16 * j + 12 + ti] & qmask;
+          float(&acc)[4] = (j & 1) ? sb : sa;
+          mma_bf16(acc, ka[0], ka[1], ka[2], ka[3], q0, q1);
+          mma_bf16(acc, ka[4], ka[5], ka[6], ka[7], q2, q3);
+        }
+        const uint8_t* vp = kp + C::kVOffset;
+        if (kCompressed && !comp) {      // raw tile in the compressed kernel: V goes where K was
+          load_raw_v(a, d, m, u, kp, lane, policy);
+          vp = kp;
+        }
+
+        // ---- online softmax, log2 domain.  lane: tokens gi, gi+8 x heads 2ti, 2ti+1
+        float x0 = (sa[0] + sb[0]) * a.scale_log2, x1 = (sa[1] + sb[1]) * a.scale_log2;
+        float x2 = (sa[2] + sb[2]) * a.scale_log2, x3 = (sa[3] + sb[3]) * a.scale_log2;
+        uint32_t keep_a = 0xFFFFFFFFu, keep_b = 0xFFFFFFFFu;
+        if (ntok < 16) {
+          if (gi >= ntok) x0 = x1 = -CUDART_INF_F;
+          if (gi + 8 >= ntok) x2 = x3 = -CUDART_INF_F;
+          // tokens past the context may hold anything (even NaN): their values are zeroed so that
+          // p = 0 times them stays 0.  V^T columns of this lane: tokens 2ti, 2ti+1 (regs 0,1,4,5)
+          // and 2ti+8, 2ti+9 (regs 2,3,6,7).
+          keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
+          keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
+        }
+        const bool grow = fmaxf(x0, x2) > m0 + kRescaleThreshold || fmaxf(x1, x3) > m1 + kRescaleThreshold;
+        if (__any_sync(0xFFFFFFFFu, grow)) {
+          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+          for (int dd = 4; dd < 32; dd <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, dd));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, dd));
+          }
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: token 0 is valid
+          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+          m0 = mn0;
+          m1 = mn1;
+          l0 *= al0;
+          l1 *= al1;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+          }
+        }
+        const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
+        const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // P^T as the B operand (k = token, n = head): high BF16 part and BF16 remainder
+        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        const uint32_t r01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
+        const uint32_t r23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
+        const uint32_t bh0 = transpose8x8(h01), bh1 = transpose8x8(h23);
+        const uint32_t bl0 = transpose8x8(r01), bl1 = transpose8x8(r23);
+
+        // ---- O^T (128 channels x 8 heads) += V^T (128 x 16 tokens) . P^T (16 x 8)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t va[8];
+          if (comp) rebuild_lane(vp + j * kSlotBytes, lane, va);
+          else load_raw_lane(vp + j * kRawBlockBytes, lane, va);
+          va[0] &= keep_a; va[1] &= keep_a; va[4] &= keep_a; va[5] &= keep_a;
+          va[2] &= keep_b; va[3] &= keep_b; va[6] &= keep_b; va[7] &= keep_b;
+          mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bh0, bh1);
+          mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bh0, bh1);
+          mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bl0, bl1);
+          mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bl0, bl1);
         }
       }
-
-      // ---- online softmax (log2 domain).  sacc: (token gi | gi+8) x (head 2ti | 2ti+1)
-      float x0 = sacc[0] * a.scale_log2, x1 = sacc[1] * a.scale_log2;
-      float x2 = sacc[2] * a.scale_log2, x3 = sacc[3] * a.scale_log2;
-      if (gi >= ntok) x0 = x1 = -CUDART_INF_F;
-      if (gi + 8 >= ntok) x2 = x3 = -CUDART_INF_F;
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-      for (int d = 4; d < 32; d <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, d));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, d));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: token 0 of a tile is valid
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
-      }
-      // P^T as the B operand (k = token, n = head): high BF16 part and BF16 remainder
-      const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-      const uint32_t r01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
-      const uint32_t r23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
-      const uint32_t bh0 = transpose8x8(h01), bh1 = transpose8x8(h23);
-      const uint32_t bl0 = transpose8x8(r01), bl1 = transpose8x8(r23);
-
-      // ---- O^T (128 channels x 8 heads) += V^T (128 x 16 tokens) . P^T (16 x 8)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mma_bf16(o[2 * j], va[j][0], va[j][1], va[j][2], va[j][3], bh0, bh1);
-        mma_bf16(o[2 * j], va[j][0], va[j][1], va[j][2], va[j][3], bl0, bl1);
-        mma_bf16(o[2 * j + 1], va[j][4], va[j][5], va[j][6], va[j][7], bh0, bh1);
-        mma_bf16(o[2 * j + 1], va[j][4], va[j][5], va[j][6], va[j][7], bl0, bl1);
-      }
+      __syncwarp();                // the stage may now be refilled
+      sidx ^= 1;
     }
-    seq_base += static_cast<uint32_t>(it.units);
 
-    // ---- merge the 8 warps' states of this item through shared memory
+    // ---- merge the warps' states of this item through shared memory.  Each warp writes its state
+    // into its stage that holds no tile in flight (the one it consumed last).
 #pragma unroll
-    for (int d = 4; d < 32; d <<= 1) {
-      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, d);
-      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, d);
+    for (int dd = 4; dd < 32; dd <<= 1) {
+      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, dd);
+      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, dd);
     }
+    float* my_combine = reinterpret_cast<float*>(my_stages + (sidx ^ 1) * C::kStageBytes);
     float* cm = my_combine + kHeadsPerSlice * kOStride;
     float* cl = cm + kHeadsPerSlice;
+    if (lane == 0) combine_stage[warp] = sidx ^ 1;
     if (gi == 0) {
       cm[2 * ti] = m0;
       cm[2 * ti + 1] = m1;
@@ -409,23 +503,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       my_combine[(2 * ti) * kOStride + 16 * mt + gi + 8] = o[mt][2];
       my_combine[(2 * ti + 1) * kOStride + 16 * mt + gi + 8] = o[mt][3];
     }
-    consumer_barrier();
-    {
-      const int hh = warp;                 // this thread finishes head hh, channels 4*lane..+3
-      if (hh < nh) {
-        float mw[kConsumerWarps];
+    consumer_barrier<kWarps>();
+    if (!aborted) {
+      const int hh = warp;                     // warps 0..7 finish head hh, channels 4*lane..+3
+      if (hh < d.nh) {
+        float mw[kWarps];
         float M = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          mw[w] = combine[w * kCombineWarpFloats + kHeadsPerSlice * kOStride + hh];
+        for (int w = 0; w < kWarps; ++w) {
+          const float* cwp = reinterpret_cast<const float*>(
+              stages + (static_cast<size_t>(w) * kWarpStages + combine_stage[w]) * C::kStageBytes);
+          mw[w] = cwp[kHeadsPerSlice * kOStride + hh];
           M = fmaxf(M, mw[w]);
         }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float lsum = 0.f;
         if (M != -CUDART_INF_F) {
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float* cwp = combine + w * kCombineWarpFloats;
+          for (int w = 0; w < kWarps; ++w) {
+            const float* cwp = reinterpret_cast<const float*>(
+                stages + (static_cast<size_t>(w) * kWarpStages + combine_stage[w]) * C::kStageBytes);
             const float f = exp2f(mw[w] - M);
             lsum += f * cwp[kHeadsPerSlice * kOStride + kHeadsPerSlice + hh];
             const float4 v = *reinterpret_cast<const float4*>(cwp + hh * kOStride + 4 * lane);
@@ -441,19 +538,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         acc.z *= inv;
         acc.w *= inv;
         const float lse2 = lsum > 0.f ? M + log2f(lsum) : -CUDART_INF_F;
-        const size_t bh = static_cast<size_t>(it.b) * a.hq + h0 + hh;
-        if (prefix[it.b + 1] - prefix[it.b] == 1) {
+        const size_t bh = static_cast<size_t>(d.b) * a.hq + d.h0 + hh;
+        if (d.single) {
           *reinterpret_cast<float4*>(a.out + bh * ZF_HEAD_DIM + 4 * lane) = acc;
           if (lane == 0) a.lse[bh] = lse2 * kLn2;
         } else {
-          const size_t pidx = bh * a.max_chunks + it.c;
+          const size_t pidx = bh * a.max_chunks + d.c;
           *reinterpret_cast<float4*>(a.part_o + pidx * ZF_HEAD_DIM + 4 * lane) = acc;
           if (lane == 0) a.part_lse[pidx] = lse2;
         }
       }
     }
-    consumer_barrier();
+    consumer_barrier<kWarps>();
+    if (lane == 0) mbar_arrive(&item_empty[buf]);     // this item's metadata and q are free
   }
+  cp_async_wait_all();
 }
 
 struct MergeArgs {
@@ -512,8 +611,9 @@ static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, 
   const long long pairs = static_cast<long long>(batch) * hkv * p.slices;
   const int tiles = page_size / ZF_BLOCK_TOKENS;
   long long best = LLONG_MAX;
-  int best_cp = max_pages;
-  for (int cp = 1; cp <= max_pages; ++cp) {
+  int best_cp = 1;
+  const int cp_max = max_pages < kMaxChunkPages ? max_pages : kMaxChunkPages;
+  for (int cp = 1; cp <= cp_max; ++cp) {
     const long long chunks = (max_pages + cp - 1) / cp;
     const long long items = pairs * chunks;
     const long long grid = items < num_sms ? items : num_sms;
@@ -531,8 +631,23 @@ static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, 
   const size_t n = static_cast<size_t>(batch) * hq * p.max_chunks;
   p.part_o_bytes = n * ZF_HEAD_DIM * 4;
   p.ws_bytes = p.part_o_bytes + ((n * 4 + 255) & ~static_cast<size_t>(255));
-  p.smem = smem_layout(batch).total;
   return p;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel); the limit only grows.
+static zf_status ensure_smem_limit(const void* kernel, int which, size_t bytes) {
+  static std::mutex mu;
+  static size_t done[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZF_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return ZF_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev][which] >= bytes) return ZF_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+      cudaSuccess)
+    return ZF_ERR_CUDA;
+  done[dev][which] = bytes;
+  return ZF_OK;
 }
 
 static zf_status current_sm_count(int* sms) {
@@ -596,10 +711,11 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaFuncSetAttribute(attn_kernel<kCompressed>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(p.smem)) != cudaSuccess)
-    return ZF_ERR_CUDA;
-  attn_kernel<kCompressed><<<p.grid, kAttnThreads, p.smem, s>>>(a);
+  const size_t smem = smem_layout<kCompressed>(batch).total;
+  if ((st = ensure_smem_limit(reinterpret_cast<const void*>(attn_kernel<kCompressed>), kCompressed ? 1 : 0,
+                             smem)) != ZF_OK)
+    return st;
+  attn_kernel<kCompressed><<<p.grid, Cfg<kCompressed>::kThreads, smem, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return ZF_ERR_CUDA;
 
   MergeArgs m{};

@@ -190,7 +190,10 @@ __global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
   uint16_t* dv = a.v_raw + (static_cast<size_t>(rs) * a.hkv + h) * rec;
   const int n16 = static_cast<int>(rec / 8);
   for (int t = threadIdx.x; t < 2 * n16; t += kCodecThreads) {
-    const uint4 val = reinterpret_cast<const uint4*>(raw)[t];
+    // shared memory holds blocks in storage order (16-byte group 2*lane + half); raw blocks are
+    // half-major (group 32*half + lane)
+    const int blk = t >> 6, within = t & 63;
+    const uint4 val = reinterpret_cast<const uint4*>(raw)[blk * 64 + 2 * (within & 31) + (within >> 5)];
     if (t < n16) reinterpret_cast<uint4*>(dk)[t] = val;
     else reinterpret_cast<uint4*>(dv)[t - n16] = val;
   }

@@ -105,6 +105,13 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
   return y;
 }
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); ex2(-inf) = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Round two floats to BF16 (nearest even) and pack: `lo` in bits 0-15, `hi` in bits 16-31.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -176,9 +183,11 @@ __device__ __forceinline__ void rebuild_lane(const uint8_t* slot, int lane, uint
   if (n_esc) patch_escapes(slot, n_esc, lane, a);
 }
 
+// This lane's 16 values of a raw block.  Raw blocks are half-major (position 256*half + 8*lane + r
+// holds storage position 16*lane + 8*half + r), so each 16-byte read of a warp is conflict-free.
 __device__ __forceinline__ void load_raw_lane(const uint8_t* block, int lane, uint32_t (&a)[8]) {
-  const uint4 x = *reinterpret_cast<const uint4*>(block + 32 * lane);
-  const uint4 y = *reinterpret_cast<const uint4*>(block + 32 * lane + 16);
+  const uint4 x = *reinterpret_cast<const uint4*>(block + 16 * lane);
+  const uint4 y = *reinterpret_cast<const uint4*>(block + 512 + 16 * lane);
   a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
   a[4] = y.x; a[5] = y.y; a[6] = y.z; a[7] = y.w;
 }

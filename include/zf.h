@@ -38,7 +38,8 @@
  *    base is the block's minimum exponent rounded down to even when every exponent fits
  *    [base, base+15] (ZipFusion's rule); otherwise the smallest even base whose window reaches
  *    the maximum exponent, with the (at most 6) lower values listed as escapes.
- *  - Raw block, 1024 bytes: the 512 BF16 values in storage order.
+ *  - Raw block, 1024 bytes: the 512 BF16 values, half-major: position 256*half + 8*lane + r
+ *    holds storage position 16*lane + 8*half + r (conflict-free 16-byte reads per half).
  *  - k_comp/v_comp: [num_pages][num_kv_heads][P/4 blocks][784 bytes]  (slot of each page id)
  *    k_raw/v_raw:   [num_raw_slots][num_kv_heads][P/4 blocks][512 BF16]
  *    dir:           [num_pages][num_kv_heads] int32: ZF_DIR_COMPRESSED, a raw slot index >= 0,

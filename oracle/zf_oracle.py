@@ -126,6 +126,17 @@ def from_storage(x: np.ndarray, role: str) -> np.ndarray:
     return x[_ORDER[role]]
 
 
+def to_raw_order(x: np.ndarray) -> np.ndarray:
+    """Storage order (p = 16*lane + 8*half + r) -> raw-block order (256*half + 8*lane + r): a raw
+    block keeps each lane's eight values of one half together, half 0 of all lanes first."""
+    return np.asarray(x, dtype=np.uint16).reshape(32, 2, 8).transpose(1, 0, 2).ravel()
+
+
+def from_raw_order(x: np.ndarray) -> np.ndarray:
+    """Inverse of to_raw_order."""
+    return np.asarray(x, dtype=np.uint16).reshape(2, 32, 8).transpose(1, 0, 2).ravel()
+
+
 # ----------------------------------------------------------------------------------------------
 # Block codec (ZipFusion §III.B, extended by an escape list)
 # ----------------------------------------------------------------------------------------------
@@ -226,7 +237,7 @@ def page_blocks(page: np.ndarray):
 
 def encode_page_head(k_page: np.ndarray, v_page: np.ndarray, n_valid: int, force_raw: bool = False):
     """Encode one page head.  Returns ("comp", k_record, v_record) with 784-byte slots, or
-    ("raw", k_record, v_record) with 512 BF16 values per block in storage order.
+    ("raw", k_record, v_record) with 512 BF16 values per block in raw-block order.
 
     The page stays raw when it is partially filled (ZipFusion §III.D), when any of its K or V
     blocks cannot be encoded, or when the caller asks for raw storage.
@@ -237,8 +248,8 @@ def encode_page_head(k_page: np.ndarray, v_page: np.ndarray, n_valid: int, force
         slots_v = [encode_block(b, "v") for b in page_blocks(v_page)]
         if all(s is not None for s in slots_k + slots_v):
             return "comp", np.concatenate(slots_k), np.concatenate(slots_v)
-    raw_k = np.concatenate([to_storage(b, "k") for b in page_blocks(k_page)])
-    raw_v = np.concatenate([to_storage(b, "v") for b in page_blocks(v_page)])
+    raw_k = np.concatenate([to_raw_order(to_storage(b, "k")) for b in page_blocks(k_page)])
+    raw_v = np.concatenate([to_raw_order(to_storage(b, "v")) for b in page_blocks(v_page)])
     return "raw", raw_k, raw_v
 
 
@@ -255,8 +266,8 @@ def decode_page_head(kind: str, k_record: np.ndarray, v_record: np.ndarray, P: i
                 k[rows, cols] = decode_block(k_record[SLOT_BYTES * i:SLOT_BYTES * (i + 1)], "k")
                 v[rows, cols] = decode_block(v_record[SLOT_BYTES * i:SLOT_BYTES * (i + 1)], "v")
             else:
-                k[rows, cols] = from_storage(k_record[BLOCK_VALUES * i:BLOCK_VALUES * (i + 1)], "k")
-                v[rows, cols] = from_storage(v_record[BLOCK_VALUES * i:BLOCK_VALUES * (i + 1)], "v")
+                k[rows, cols] = from_storage(from_raw_order(k_record[BLOCK_VALUES * i:BLOCK_VALUES * (i + 1)]), "k")
+                v[rows, cols] = from_storage(from_raw_order(v_record[BLOCK_VALUES * i:BLOCK_VALUES * (i + 1)]), "v")
             i += 1
     return k, v
 
@@ -266,7 +277,7 @@ class Cache:
     """Host model of one layer's compressed paged cache, byte-for-byte the library's layout.
 
     k_comp/v_comp: [num_pages][Hkv][P/16 * 4 * 784] uint8 (slot of each page id)
-    k_raw/v_raw:   [num_raw][Hkv][P/16 * 4 * 512] uint16 (raw slots, storage order)
+    k_raw/v_raw:   [num_raw][Hkv][P/16 * 4 * 512] uint16 (raw slots, raw-block order)
     dir:           [num_pages][Hkv] int32: -1 compressed, r >= 0 raw slot r, -2 invalid
     """
     num_pages: int

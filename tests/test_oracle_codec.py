@@ -37,6 +37,15 @@ def test_fragment_cells_match_hand_listed_ptx_table():
         assert O.fragment_cell(lane, r) == (row, col)
 
 
+def test_raw_order_is_the_half_major_storage_order():
+    x = np.arange(512, dtype=np.uint16)
+    r = O.to_raw_order(x)
+    for lane in (0, 5, 31):
+        for half in (0, 1):
+            assert (r[256 * half + 8 * lane:256 * half + 8 * lane + 8] == x[16 * lane + 8 * half:16 * lane + 8 * half + 8]).all()
+    assert (O.from_raw_order(r) == x).all()
+
+
 def test_key_and_value_orders_differ_and_transpose():
     k, v = O.storage_order("k"), O.storage_order("v")
     assert (k != v).any()

@@ -10,13 +10,14 @@
 // Design for sm_103a (one CTA per SM, persistent over a static list of work items):
 //  * work item = (request b, kv head g, head slice, chunk of pages); the chunk size is picked on
 //    the host so that items fill the SMs in whole rounds;
-//  * warp 10 is the metadata warp: it runs one item ahead, resolving the item's page ids through
-//    the page table and the directory into shared memory and bulk-copying the item's q rows;
-//  * warps 0-9 each stream their own 16-token tiles (tile u of an item goes to warp u % 10) into
-//    two private 8 KB shared-memory stages with 16-byte cp.async, prefetching the next tile while
-//    computing the current one.  (Measured on GB300: 1-D bulk copies of 3-6 KB issued by one
-//    thread per SM complete about one per 0.55 us, far below HBM bandwidth, while per-warp
-//    16-byte async copies of the same scattered tiles reach 6.6-6.8 TB/s.)
+//  * the last warp is the metadata warp: it runs one item ahead, resolving the item's page ids
+//    through the page table and the directory into shared memory and staging the item's q rows;
+//  * the consumer warps each stream their own 16-token tiles (tile u of an item goes to warp
+//    u % warps) into two private shared-memory stages, prefetching the next tile while computing
+//    the current one: one lane of the warp issues 1-D bulk copies (cp.async.bulk, L2 evict-first)
+//    on the warp's own mbarrier.  (Measured on GB300: bulk copies of 3-8 KB complete at about one
+//    per 0.55 us per issuing warp, so one producer warp per SM tops out at 0.9-2.3 TB/s on this
+//    traffic, while 8+ issuing warps reach 5.3-6.4 TB/s.)
 //  * per tile, a warp rebuilds K blocks straight into m16n8k16 A fragments (the storage order is
 //    the fragment order), computes S^T = K Q^T for up to 8 query heads of the GQA group (one MMA
 //    n-tile), runs the online softmax in the log2 domain (the running max is only raised, after a
@@ -52,10 +53,14 @@ constexpr int kWarpStages = 2;
 constexpr int kTileCompBytes = 4 * kSlotBytes;      // 3136: one 16-token tile of K (or V), compressed
 constexpr int kTileRawBytes = 4 * kRawBlockBytes;   // 4096
 constexpr int kHeadsPerSlice = 8;                   // MMA n
-constexpr int kMaxChunkPages = 256;                 // pages per work item (metadata buffer size)
+constexpr int kMaxItemTiles = 256;                  // 16-token tiles per work item (metadata buffer size)
+// q rows in shared memory: channel words permuted so that lane (gi, ti) finds the four B-fragment
+// words of k-steps 2j and 2j+1 (words 16j + ti + {0, 4, 8, 12}) in one 16-byte read at word
+// 16j + 4ti; rows padded to 320 bytes so the eight rows of a warp's reads hit distinct banks.
+constexpr int kQRowBytes = 320;
 constexpr int kOStride = 132;                       // padded combine row (conflict-free writes)
 constexpr int kCombineWarpFloats = kHeadsPerSlice * kOStride + 16;
-constexpr int kItemOverheadTiles = 4;               // planner: fixed cost of an item, in tiles
+constexpr int kItemOverheadTiles = 12;              // planner: fixed cost of an item, in tiles
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p <= 2^8 between max updates
 
@@ -92,7 +97,7 @@ struct ItemDesc {
 };
 
 struct SmemLayout {
-  size_t stages, item_full, item_empty, misc, desc, meta, qbuf, prefix, total;
+  size_t stages, item_full, item_empty, misc, desc, meta, qbuf, bars, prefix, total;
 };
 
 template <bool kCompressed>
@@ -101,12 +106,13 @@ __host__ __device__ inline SmemLayout smem_layout(int batch) {
   SmemLayout s;
   size_t at = 0;
   s.stages = at; at += static_cast<size_t>(C::kWarps) * kWarpStages * C::kStageBytes;
-  s.item_full = at; at += 2 * 8;
+  s.item_full = at; at += 2 * 8;                          // count 1: the metadata warp
   s.item_empty = at; at += 2 * 8;
   s.misc = at; at += 16 + 16 * 4;                         // [0] abort flag, [16..] combine stage per warp
   s.desc = at; at += 2 * 64;
-  s.meta = at; at += 2 * kMaxChunkPages * 4;
-  s.qbuf = at; at += 2 * kHeadsPerSlice * ZF_HEAD_DIM * 2;
+  s.meta = at; at += 2 * kMaxItemTiles * 4;
+  s.qbuf = at; at += 2 * kHeadsPerSlice * kQRowBytes;
+  s.bars = at; at += static_cast<size_t>(C::kWarps) * kWarpStages * 8;
   s.prefix = at; at += static_cast<size_t>(batch + 1) * 4;
   s.total = (at + 127) & ~static_cast<size_t>(127);
   return s;
@@ -117,14 +123,6 @@ __device__ __forceinline__ void consumer_barrier() {
   asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Item `item` of the flat list: its request, chunk, kv head, head slice, token range and tiles.
 __device__ __forceinline__ ItemDesc describe_item(const AttnArgs& a, const int* prefix, int item) {
@@ -154,11 +152,12 @@ __device__ __forceinline__ ItemDesc describe_item(const AttnArgs& a, const int* 
   return d;
 }
 
-// Resolve the item's pages into meta[i] = slot << 2 | kind (all 32 lanes).  All page-table loads
-// are issued before the directory loads that depend on them.
+// Resolve the item's pages into one entry per tile: meta[u] = slot << 5 | tile_in_page << 2 | kind
+// (all 32 lanes).  All page-table loads are issued before the directory loads that depend on them.
 template <bool kCompressed>
-__device__ __forceinline__ void resolve_pages(const AttnArgs& a, const ItemDesc& d, int* meta, int lane) {
-  constexpr int kPer = kMaxChunkPages / 32;
+__device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc& d, int* meta, int lane) {
+  constexpr int kPer = kMaxItemTiles / 32;
+  const int tpp = a.page_size / ZF_BLOCK_TOKENS;
   const int p0 = d.t0 / a.page_size;
   const int npg = (d.t1 - d.t0 + a.page_size - 1) / a.page_size;
   const int32_t* row = a.page_table + static_cast<size_t>(d.b) * a.max_pages + p0;
@@ -194,55 +193,72 @@ __device__ __forceinline__ void resolve_pages(const AttnArgs& a, const ItemDesc&
     } else {
       report(a.status, ZF_DEV_BAD_PAGE_ID);
     }
-    meta[i] = (slot << 2) | kind;
+    for (int t = 0; t < tpp; ++t) {
+      const int u = i * tpp + t;
+      if (u < d.units) meta[u] = (slot << 5) | (t << 2) | kind;
+    }
   }
 }
 
-// Start the 16-byte async copies of tile u of an item into `stage`: K at 0 and V at kVOffset.  In
-// the compressed kernel a raw tile does not fit one stage: only its K half is started here and
-// the V half is fetched after QK^T (see load_raw_v).
+// Start the copies of tile u of an item into `stage` (K at 0, V at kVOffset), signalled on the
+// warp's own barrier `bar`: one lane issues 1-D bulk copies (each consumer warp issues its own, so
+// an SM has 10-15 copy streams in flight).  In the compressed kernel a raw tile does not fit one
+// stage: only its K half is started here and the V half is fetched after QK^T (issue_raw_v).
+// Returns whether anything was armed on `bar`.
 template <bool kCompressed>
-__device__ __forceinline__ void issue_tile(const AttnArgs& a, const ItemDesc& d, const int* meta, int u,
-                                           uint8_t* stage, int lane, uint64_t policy) {
+__device__ __forceinline__ bool issue_tile(const AttnArgs& a, const ItemDesc& d, const int* meta, int u,
+                                           uint8_t* stage, uint64_t* bar, int lane, uint64_t policy) {
   using C = Cfg<kCompressed>;
-  const int tiles_per_page = a.page_size / ZF_BLOCK_TOKENS;
-  const int m = meta[u / tiles_per_page];
+  const int m = meta[u];
   const int kind = m & 3;
-  const size_t head = static_cast<size_t>(m >> 2) * a.hkv + d.g;
-  const int t = u % tiles_per_page;
+  const size_t head = static_cast<size_t>(m >> 5) * a.hkv + d.g;
+  const int t = (m >> 2) & 7;
   if (kCompressed && kind == kKindComp) {
-    const size_t off = head * a.comp_head_bytes + static_cast<size_t>(t) * kTileCompBytes;
-    const uint8_t* ks = a.k_comp + off;
-    const uint8_t* vs = a.v_comp + off;
-#pragma unroll
-    for (int v = lane; v < kTileCompBytes / 16; v += 32) {
-      cp_async16(stage + 16 * v, ks + 16 * v, policy);
-      cp_async16(stage + C::kVOffset + 16 * v, vs + 16 * v, policy);
+    if (lane == 0) {
+      const size_t off = head * a.comp_head_bytes + static_cast<size_t>(t) * kTileCompBytes;
+      mbar_arrive_expect_tx(bar, 2 * kTileCompBytes);
+      bulk_copy_g2s(stage, a.k_comp + off, kTileCompBytes, bar, policy);
+      bulk_copy_g2s(stage + C::kVOffset, a.v_comp + off, kTileCompBytes, bar, policy);
     }
-  } else if (kind == kKindRaw) {
-    const size_t off = head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes;
-    const uint8_t* ks = a.k_raw + off;
-#pragma unroll
-    for (int v = lane; v < kTileRawBytes / 16; v += 32) {
-      cp_async16(stage + 16 * v, ks + 16 * v, policy);
-      if (!kCompressed) cp_async16(stage + C::kVOffset + 16 * v, a.v_raw + off + 16 * v, policy);
+    return true;
+  }
+  if (kind == kKindRaw) {
+    if (lane == 0) {
+      const size_t off = head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes;
+      mbar_arrive_expect_tx(bar, (kCompressed ? 1 : 2) * kTileRawBytes);
+      bulk_copy_g2s(stage, a.k_raw + off, kTileRawBytes, bar, policy);
+      if (!kCompressed) bulk_copy_g2s(stage + C::kVOffset, a.v_raw + off, kTileRawBytes, bar, policy);
     }
+    return true;
+  }
+  return false;
+}
+
+// Compressed kernel, raw tile: after QK^T, fetch the V half into the same stage.
+__device__ __forceinline__ void issue_raw_v(const AttnArgs& a, const ItemDesc& d, const int* meta, int u,
+                                            uint8_t* stage, uint64_t* bar, int lane, uint64_t policy) {
+  const int m = meta[u];
+  const size_t head = static_cast<size_t>(m >> 5) * a.hkv + d.g;
+  const size_t off = head * a.raw_head_bytes + static_cast<size_t>((m >> 2) & 7) * kTileRawBytes;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, kTileRawBytes);
+    bulk_copy_g2s(stage, a.v_raw + off, kTileRawBytes, bar, policy);
   }
 }
 
-// Compressed kernel, raw tile: after QK^T, fetch the V half into the same stage and wait for it.
-__device__ __forceinline__ void load_raw_v(const AttnArgs& a, const ItemDesc& d, const int* meta, int u,
-                                           uint8_t* stage, int lane, uint64_t policy) {
-  const int tiles_per_page = a.page_size / ZF_BLOCK_TOKENS;
-  const int m = meta[u / tiles_per_page];
-  const size_t head = static_cast<size_t>(m >> 2) * a.hkv + d.g;
-  const size_t off = head * a.raw_head_bytes + static_cast<size_t>(u % tiles_per_page) * kTileRawBytes;
-  __syncwarp();                                   // every lane is done reading the K half
+// Stage q rows of an item into qbuf (permuted, padded layout; rows past nh are zero).
+__device__ __forceinline__ void stage_q(const AttnArgs& a, const ItemDesc& d, uint8_t* qb, int lane) {
+  // 8 rows x 64 words; lane handles word w = lane and lane + 32 of every row
+  for (int r = 0; r < kHeadsPerSlice; ++r) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(d.b) * a.hq + d.h0 + min(r, d.nh - 1)) * ZF_HEAD_DIM);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(qb + r * kQRowBytes);
 #pragma unroll
-  for (int v = lane; v < kTileRawBytes / 16; v += 32) cp_async16(stage + 16 * v, a.v_raw + off + 16 * v, policy);
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncwarp();
+    for (int h = 0; h < 2; ++h) {
+      const int w = lane + 32 * h;              // channel word w = 16j + 4r' + t  (t < 4, r' < 4)
+      const int j = w >> 4, rr = (w >> 2) & 3, t = w & 3;
+      dst[16 * j + 4 * t + rr] = r < d.nh ? src[w] : 0u;
+    }
+  }
 }
 
 template <bool kCompressed>
@@ -257,7 +273,8 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
   int* combine_stage = reinterpret_cast<int*>(smem + L.misc + 16);
   ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + L.desc);
   int* meta = reinterpret_cast<int*>(smem + L.meta);
-  uint16_t* qbuf = reinterpret_cast<uint16_t*>(smem + L.qbuf);
+  uint8_t* qbuf = smem + L.qbuf;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* prefix = reinterpret_cast<int*>(smem + L.prefix);
   uint8_t* stages = smem + L.stages;
 
@@ -268,7 +285,11 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
     mbar_init(&item_full[tid], 1);
     mbar_init(&item_empty[tid], kWarps);
   }
+  if (tid < kWarps * kWarpStages) mbar_init(&bars[tid], 1);
   if (tid == 0) *abort_flag = 0;
+  // everything above touched only shared memory; inputs may come from the preceding grid
+  wait_prior_grid();
+  allow_next_grid();
   const int max_len = a.max_pages * a.page_size;
   for (int b = tid; b < a.batch; b += C::kThreads) {
     int len = a.seq_lens[b];
@@ -316,21 +337,13 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
         break;
       }
       const ItemDesc d = describe_item(a, prefix, item);
-      resolve_pages<kCompressed>(a, d, meta + buf * kMaxChunkPages, lane);
+      resolve_tiles<kCompressed>(a, d, meta + buf * kMaxItemTiles, lane);
+      stage_q(a, d, qbuf + buf * kHeadsPerSlice * kQRowBytes, lane);
       __syncwarp();
       if (lane == 0) {
         desc[buf] = d;
-        const uint32_t qbytes = d.nh * ZF_HEAD_DIM * 2;
-        mbar_arrive_expect_tx(&item_full[buf], qbytes);
-        bulk_copy_g2s(qbuf + buf * kHeadsPerSlice * ZF_HEAD_DIM,
-                      a.q + (static_cast<size_t>(d.b) * a.hq + d.h0) * ZF_HEAD_DIM, qbytes, &item_full[buf], policy);
+        mbar_arrive(&item_full[buf]);        // release: the warp's page metadata and q rows
       }
-    }
-    // its own q copies must have landed before the CTA can exit (consumers that gave up waiting
-    // would not have waited for them)
-    if (lane == 0) {
-      for (int j = k - 2; j < k; ++j)
-        if (j >= 0) mbar_wait(&item_full[j & 1], (j >> 1) & 1u);
     }
     return;
   }
@@ -338,8 +351,11 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
   // ================================================================== consumer warps
   const int gi = lane >> 2, ti = lane & 3;
   uint8_t* my_stages = stages + static_cast<size_t>(warp) * kWarpStages * C::kStageBytes;
+  uint64_t* my_bars = bars + warp * kWarpStages;
   bool aborted = false;
   int sidx = 0;                 // stage of the next tile to consume
+  uint32_t phase = 0;           // bit s: parity of the next wait on stage s
+  uint32_t inflight = 0;        // bit s: stage s has copies armed and not yet waited for
   int pending_item = -1;        // item whose first tile for this warp is already in flight
   int k = 0;
   for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++k) {
@@ -350,11 +366,10 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
       report(a.status, ZF_DEV_TIMEOUT);
     }
     const ItemDesc d = desc[buf];
-    const int* m = meta + buf * kMaxChunkPages;
-    // Q^T as the B operand (k = channel, n = head): lane holds head gi, channels 2ti(+1), +8(+9);
-    // read from shared memory at each use
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qbuf + (buf * kHeadsPerSlice + min(gi, d.nh - 1)) * ZF_HEAD_DIM);
-    const uint32_t qmask = gi < d.nh ? 0xFFFFFFFFu : 0u;
+    const int* m = meta + buf * kMaxItemTiles;
+    // Q^T as the B operand (k = channel, n = head): one 16-byte read gives this lane's words of
+    // k-steps 2j and 2j+1 (rows past the group's heads are zero)
+    const uint8_t* qrow = qbuf + (buf * kHeadsPerSlice + gi) * kQRowBytes + 16 * ti;
 
     float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
     float o[8][4];
@@ -363,34 +378,45 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
 
     // this warp's first tile of the item, unless it was prefetched during the previous item
     if (!aborted && pending_item != item && warp < d.units) {
-      issue_tile<kCompressed>(a, d, m, warp, my_stages + sidx * C::kStageBytes, lane, policy);
-      cp_async_commit();
+      if (issue_tile<kCompressed>(a, d, m, warp, my_stages + sidx * C::kStageBytes, &my_bars[sidx], lane, policy))
+        inflight |= 1u << sidx;
     }
     pending_item = -1;
 
     for (int u = warp; u < d.units && !aborted; u += kWarps) {
       // prefetch the warp's next tile: the next one of this item, or its first one of the next item
       const int un = u + kWarps;
-      uint8_t* next_stage = my_stages + (sidx ^ 1) * C::kStageBytes;
+      const int ns = sidx ^ 1;
+      uint8_t* next_stage = my_stages + ns * C::kStageBytes;
       if (un < d.units) {
-        issue_tile<kCompressed>(a, d, m, un, next_stage, lane, policy);
+        if (issue_tile<kCompressed>(a, d, m, un, next_stage, &my_bars[ns], lane, policy)) inflight |= 1u << ns;
       } else if (item + static_cast<int>(gridDim.x) < total_items) {
         const int nb = buf ^ 1;
         if (*abort_flag || !mbar_wait(&item_full[nb], ((k + 1) >> 1) & 1u)) {
           aborted = true;
           *abort_flag = 1;
           report(a.status, ZF_DEV_TIMEOUT);
+          break;
         } else if (warp < desc[nb].units) {
-          issue_tile<kCompressed>(a, desc[nb], meta + nb * kMaxChunkPages, warp, next_stage, lane, policy);
+          if (issue_tile<kCompressed>(a, desc[nb], meta + nb * kMaxItemTiles, warp, next_stage, &my_bars[ns], lane,
+                                      policy))
+            inflight |= 1u << ns;
           pending_item = item + gridDim.x;
         }
       }
-      cp_async_commit();
-      cp_async_wait_1();          // everything but the group just committed has landed
-      __syncwarp();
-      if (aborted) break;
+      // wait for the current tile
+      if (inflight & (1u << sidx)) {
+        if (*abort_flag || !mbar_wait(&my_bars[sidx], (phase >> sidx) & 1u)) {
+          aborted = true;
+          *abort_flag = 1;
+          report(a.status, ZF_DEV_TIMEOUT);
+          break;
+        }
+        phase ^= 1u << sidx;
+        inflight &= ~(1u << sidx);
+      }
 
-      const int kind = m[u / (a.page_size / ZF_BLOCK_TOKENS)] & 3;
+      const int kind = m[u] & 3;
       if (kind != kKindInvalid) {
         uint8_t* kp = my_stages + sidx * C::kStageBytes;
         const bool comp = kCompressed && kind == kKindComp;
@@ -403,15 +429,22 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
           uint32_t ka[8];
           if (comp) rebuild_lane(kp + j * kSlotBytes, lane, ka);
           else load_raw_lane(kp + j * kRawBlockBytes, lane, ka);
-          const uint32_t q0 = qrow[16 * j + ti] & qmask, q1 = qrow[16 * j + ti + 4] & qmask;
-          const uint32_t q2 = qrow[16 * j + 8 + ti] & qmask, q3 = qrow[16 * j + 12 + ti] & qmask;
+          const uint4 q = *reinterpret_cast<const uint4*>(qrow + 64 * j);
           float(&acc)[4] = (j & 1) ? sb : sa;
-          mma_bf16(acc, ka[0], ka[1], ka[2], ka[3], q0, q1);
-          mma_bf16(acc, ka[4], ka[5], ka[6], ka[7], q2, q3);
+          mma_bf16(acc, ka[0], ka[1], ka[2], ka[3], q.x, q.y);
+          mma_bf16(acc, ka[4], ka[5], ka[6], ka[7], q.z, q.w);
         }
         const uint8_t* vp = kp + C::kVOffset;
         if (kCompressed && !comp) {      // raw tile in the compressed kernel: V goes where K was
-          load_raw_v(a, d, m, u, kp, lane, policy);
+          __syncwarp();                  // every lane is done reading the K half
+          issue_raw_v(a, d, m, u, kp, &my_bars[sidx], lane, policy);
+          if (*abort_flag || !mbar_wait(&my_bars[sidx], (phase >> sidx) & 1u)) {
+            aborted = true;
+            *abort_flag = 1;
+            report(a.status, ZF_DEV_TIMEOUT);
+            break;
+          }
+          phase ^= 1u << sidx;
           vp = kp;
         }
 
@@ -552,7 +585,9 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
     consumer_barrier<kWarps>();
     if (lane == 0) mbar_arrive(&item_empty[buf]);     // this item's metadata and q are free
   }
-  cp_async_wait_all();
+  // copies still in flight (only after a wait gave up) must land before the CTA exits
+  for (int st = 0; st < kWarpStages; ++st)
+    if (inflight & (1u << st)) mbar_wait(&my_bars[st], (phase >> st) & 1u);
 }
 
 struct MergeArgs {
@@ -568,6 +603,8 @@ struct MergeArgs {
 // Requests with one chunk were finished by the attention kernel; empty requests get 0 / -inf.
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  wait_prior_grid();                       // the attention grid's partials
+  allow_next_grid();
   const int idx = blockIdx.x * 4 + warp;
   if (idx >= a.batch * a.hq) return;
   const int b = idx / a.hq;
@@ -612,7 +649,7 @@ static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, 
   const int tiles = page_size / ZF_BLOCK_TOKENS;
   long long best = LLONG_MAX;
   int best_cp = 1;
-  const int cp_max = max_pages < kMaxChunkPages ? max_pages : kMaxChunkPages;
+  const int cp_max = max_pages < kMaxItemTiles / tiles ? max_pages : kMaxItemTiles / tiles;
   for (int cp = 1; cp <= cp_max; ++cp) {
     const long long chunks = (max_pages + cp - 1) / cp;
     const long long items = pairs * chunks;
@@ -676,6 +713,8 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
       (reinterpret_cast<uintptr_t>(page_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return ZF_ERR_INVALID_ARGUMENT;
   if (!(scale == scale)) return ZF_ERR_INVALID_ARGUMENT;
+  // tile entries pack a slot id into 26 bits
+  if (c->num_pages >= (1 << 26) || c->num_raw_slots >= (1 << 26)) return ZF_ERR_UNSUPPORTED;
   int sms = 0;
   if ((st = current_sm_count(&sms)) != ZF_OK) return st;
   const Plan p = make_plan(batch, hq, c->num_kv_heads, c->page_size, max_pages, sms);
@@ -715,8 +754,19 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   if ((st = ensure_smem_limit(reinterpret_cast<const void*>(attn_kernel<kCompressed>), kCompressed ? 1 : 0,
                              smem)) != ZF_OK)
     return st;
-  attn_kernel<kCompressed><<<p.grid, Cfg<kCompressed>::kThreads, smem, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return ZF_ERR_CUDA;
+  // programmatic dependent launch: each kernel may start while its predecessor in the stream
+  // drains, and waits for it (griddepcontrol.wait) before touching inputs or the workspace
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(Cfg<kCompressed>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_kernel<kCompressed>, a) != cudaSuccess) return ZF_ERR_CUDA;
 
   MergeArgs m{};
   m.seq_lens = seq_lens;
@@ -731,8 +781,12 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   m.chunk_pages = p.chunk_pages;
   m.max_chunks = p.max_chunks;
   const int rows = batch * hq;
-  merge_kernel<<<(rows + 3) / 4, 128, 0, s>>>(m);
-  return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
+  cudaLaunchConfig_t mcfg = cfg;
+  mcfg.gridDim = dim3((rows + 3) / 4);
+  mcfg.blockDim = dim3(128);
+  mcfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&mcfg, merge_kernel, m) != cudaSuccess) return ZF_ERR_CUDA;
+  return ZF_OK;
 }
 
 }  // namespace zf

@@ -15,6 +15,9 @@ constexpr int kRawBlockBytes = ZF_RAW_BLOCK_BYTES;
 constexpr int kHeaderAt = 768;
 constexpr int kEscapesAt = 772;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // a pipeline wait gives up after 2 s
+// try_wait may suspend the thread up to this long (it resumes as soon as the phase completes),
+// so waiting warps do not spend issue slots polling.
+constexpr uint32_t kSuspendHintNs = 200000u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -49,25 +52,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return done != 0;
 }
 
 // Wait for the phase with the given parity to complete.  Bounded: returns false after
-// kWaitTimeoutNs (or 2^30 polls), so a broken pipeline never hangs the GPU.
+// kWaitTimeoutNs (checked at every retry), so a broken pipeline never hangs the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
   }
   return false;
 }
+
+// Programmatic dependent launch: wait for the preceding grid's results / let the next grid start.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------------------------- bulk copies
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

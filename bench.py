@@ -254,7 +254,7 @@ def run_gpu(args, rank, world, local_rank):
         append = LongContextAppend(zf, I, w, layers[0], device, 2 * (args.steps + args.warmup))
         max_pages = int(append.table.shape[1])
     ws_bytes = zf.workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.page_size, max_pages)
-    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    workspace = zf.new_workspace(ws_bytes, device)
 
     def step(dense=False, events=None):
         if append is not None and not dense:

@@ -97,7 +97,7 @@ struct ItemDesc {
 };
 
 struct SmemLayout {
-  size_t stages, item_full, item_empty, misc, desc, meta, qbuf, bars, prefix, total;
+  size_t stages, item_full, q_full, item_empty, misc, desc, meta, qbuf, bars, prefix, total;
 };
 
 template <bool kCompressed>
@@ -106,7 +106,8 @@ __host__ __device__ inline SmemLayout smem_layout(int batch) {
   SmemLayout s;
   size_t at = 0;
   s.stages = at; at += static_cast<size_t>(C::kWarps) * kWarpStages * C::kStageBytes;
-  s.item_full = at; at += 2 * 8;                          // count 1: the metadata warp
+  s.item_full = at; at += 2 * 8;                          // count 1: tiles of the item resolved
+  s.q_full = at; at += 2 * 8;                             // count 1: q rows of the item staged
   s.item_empty = at; at += 2 * 8;
   s.misc = at; at += 16 + 16 * 4;                         // [0] abort flag, [16..] combine stage per warp
   s.desc = at; at += 2 * 64;
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
   const SmemLayout L = smem_layout<kCompressed>(a.batch);
   uint64_t* item_full = reinterpret_cast<uint64_t*>(smem + L.item_full);
   uint64_t* item_empty = reinterpret_cast<uint64_t*>(smem + L.item_empty);
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + L.q_full);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
   int* combine_stage = reinterpret_cast<int*>(smem + L.misc + 16);
   ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + L.desc);
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
   // ---- prologue: barriers, chunk counts per request and their prefix sums
   if (tid < 2) {
     mbar_init(&item_full[tid], 1);
+    mbar_init(&q_full[tid], 1);
     mbar_init(&item_empty[tid], kWarps);
   }
   if (tid < kWarps * kWarpStages) mbar_init(&bars[tid], 1);
@@ -338,12 +341,14 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
       }
       const ItemDesc d = describe_item(a, prefix, item);
       resolve_tiles<kCompressed>(a, d, meta + buf * kMaxItemTiles, lane);
-      stage_q(a, d, qbuf + buf * kHeadsPerSlice * kQRowBytes, lane);
       __syncwarp();
       if (lane == 0) {
         desc[buf] = d;
-        mbar_arrive(&item_full[buf]);        // release: the warp's page metadata and q rows
+        mbar_arrive(&item_full[buf]);        // release: the tiles can be fetched
       }
+      stage_q(a, d, qbuf + buf * kHeadsPerSlice * kQRowBytes, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[buf]);   // release: the q rows
     }
     return;
   }
@@ -382,6 +387,11 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
         inflight |= 1u << sidx;
     }
     pending_item = -1;
+    if (!aborted && (*abort_flag || !mbar_wait(&q_full[buf], (k >> 1) & 1u))) {
+      aborted = true;
+      *abort_flag = 1;
+      report(a.status, ZF_DEV_TIMEOUT);
+    }
 
     for (int u = warp; u < d.units && !aborted; u += kWarps) {
       // prefetch the warp's next tile: the next one of this item, or its first one of the next item
@@ -614,6 +624,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   float4* outp = reinterpret_cast<float4*>(a.out + static_cast<size_t>(idx) * ZF_HEAD_DIM) + lane;
   if (nch == 1) return;
   const float* pl = a.part_lse + static_cast<size_t>(idx) * a.max_chunks;
+  // chunk log-sum-exps, one per lane: max and sum of 2^(lse_i - max) by warp reductions
   float M = -CUDART_INF_F;
   for (int i = lane; i < nch; i += 32) M = fmaxf(M, pl[i]);
 #pragma unroll
@@ -623,17 +634,25 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
     if (lane == 0) a.lse[idx] = -CUDART_INF_F;
     return;
   }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.f;
+  for (int i = lane; i < nch; i += 32) lsum += exp2f(pl[i] - M);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, d);
+  // weighted sum of the chunk outputs: lane owns 4 channels; weights come from the owning lane
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* po = reinterpret_cast<const float4*>(a.part_o + static_cast<size_t>(idx) * a.max_chunks * ZF_HEAD_DIM) + lane;
-  for (int i = 0; i < nch; ++i) {
-    const float f = exp2f(pl[i] - M);
-    const float4 v = po[static_cast<size_t>(i) * (ZF_HEAD_DIM / 4)];
-    lsum += f;
-    acc.x += f * v.x;
-    acc.y += f * v.y;
-    acc.z += f * v.z;
-    acc.w += f * v.w;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const float w = c0 + lane < nch ? exp2f(pl[c0 + lane] - M) : 0.f;
+    const int n = min(32, nch - c0);
+#pragma unroll 8
+    for (int j = 0; j < n; ++j) {
+      const float f = __shfl_sync(0xFFFFFFFFu, w, j);
+      const float4 v = po[static_cast<size_t>(c0 + j) * (ZF_HEAD_DIM / 4)];
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
   }
   const float inv = 1.f / lsum;
   *outp = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);

@@ -172,6 +172,11 @@ def workspace_size(batch, num_q_heads, num_kv_heads, page_size, max_pages) -> in
     return int(lib().zf_decode_attn_workspace_size(batch, num_q_heads, num_kv_heads, page_size, max_pages))
 
 
+def new_workspace(nbytes, device="cuda"):
+    """A workspace buffer for zf_decode_attn (any contents are fine)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
 def decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse=None, workspace=None,
                 stream=None, dense=False):
     """Decode attention over the cache.  q [B][Hq][128] int16 (BF16 bits), page_table [B][max_pages]
@@ -187,7 +192,7 @@ def decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse
         lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     need = workspace_size(B, Hq, cache.num_kv_heads, cache.page_size, max_pages)
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        workspace = new_workspace(need, dev)
     d = cache.desc()
     fn = lib().zf_dense_decode_attn if dense else lib().zf_decode_attn
     code = fn(ctypes.byref(d), _ptr(q), B, Hq, _ptr(page_table), max_pages, _ptr(seq_lens), scale, _ptr(out),

@@ -97,6 +97,26 @@ def test_deterministic(zf):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+def test_one_workspace_across_calls_of_different_shapes(zf):
+    """One workspace serves calls of different lengths and batch sizes (its contents between calls
+    do not matter) and gives the same bits as fresh ones."""
+    cases = [(W(3, 8, 2, 16, 900, pool="random", seed=21), [900, 333, 17]),
+             (W(2, 14, 2, 16, 2000, pool="random", seed=22), [2000, 1999]),
+             (W(3, 8, 2, 16, 900, pool="random", seed=21), [900, 333, 17])]
+    ws = zf.new_workspace(max(zf.workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.page_size, w.max_pages)
+                              for w, _ in cases))
+    for w, lens in cases:
+        layer = I.make_layer(w, seq_lens=lens)
+        gc = H.gpu_cache_from(layer, zf)
+        q, t, sl = layer.q.cuda(), layer.page_table.cuda(), layer.seq_lens.cuda()
+        shared = zf.decode_attn(gc, q, t, sl, layer.scale, workspace=ws)
+        fresh = zf.decode_attn(gc, q, t, sl, layer.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(shared[0], fresh[0]) and torch.equal(shared[1], fresh[1])
+        ref_out, ref_lse = _oracle(layer)
+        H.compare_attention(shared[0], shared[1], ref_out, ref_lse)
+
+
 def test_bad_page_ids_are_reported_not_faulted(zf):
     w = W(2, 8, 2, 16, 64, seed=13)
     layer = I.make_layer(w, seq_lens=[64, 40])

@@ -7,11 +7,14 @@
 // metadata for later pages is fetched while earlier pages are attended.  ZipFusion §IV.B:
 // split-KV partial results are combined by a split-result merge.
 //
-// Design for sm_103a (one CTA per SM, persistent over a static list of work items):
-//  * work item = (request b, kv head g, head slice, chunk of pages); the chunk size is picked on
-//    the host so that items fill the SMs in whole rounds;
-//  * the last warp is the metadata warp: it runs one item ahead, resolving the item's page ids
-//    through the page table and the directory into shared memory and staging the item's q rows;
+// Design for sm_103a (one CTA per SM, persistent):
+//  * work is balanced by pages, not by items: the pages of all (request b, kv head g, head slice)
+//    pairs, laid end to end, are cut into one equal contiguous range per CTA, so a ragged batch
+//    gives every SM the same number of tiles.  Where a range meets a pair it forms that pair's
+//    chunk(s), cut further into items of at most 256 tiles; each item yields one partial;
+//  * the last warp is the metadata warp: it walks the CTA's range, and runs one item ahead,
+//    resolving the item's page ids through the page table and the directory into shared memory
+//    and staging the item's q rows; an end marker closes the CTA's item stream;
 //  * the consumer warps each stream their own 16-token tiles (tile u of an item goes to warp
 //    u % warps) into two private shared-memory stages, prefetching the next tile while computing
 //    the current one: one lane of the warp issues 1-D bulk copies (cp.async.bulk, L2 evict-first)
@@ -59,8 +62,8 @@ constexpr int kMaxItemTiles = 256;                  // 16-token tiles per work i
 // 16j + 4ti; rows padded to 320 bytes so the eight rows of a warp's reads hit distinct banks.
 constexpr int kQRowBytes = 320;
 constexpr int kOStride = 132;                       // padded combine row (conflict-free writes)
-constexpr int kCombineWarpFloats = kHeadsPerSlice * kOStride + 16;
-constexpr int kItemOverheadTiles = 12;              // planner: fixed cost of an item, in tiles
+// partial chunks per pair are sized for ranges of at least (balanced range) / kMinRangeDivisor pages
+constexpr int kMinRangeDivisor = 16;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p <= 2^8 between max updates
 
@@ -80,15 +83,17 @@ struct AttnArgs {
   float* lse;
   float* part_o;
   float* part_lse;
-  int32_t batch, hq, hkv, group, slices, page_size, num_pages, num_raw, max_pages, chunk_pages, max_chunks;
+  int32_t* chunk_counts;     // [batch][hkv * slices] partials per pair, for the merge kernel
+  int32_t batch, hq, hkv, group, slices, page_size, num_pages, num_raw, max_pages, max_chunks;
+  int32_t min_range_pages;   // lower bound of the pages per CTA range
   int64_t comp_head_bytes;   // bytes of one (page, kv head) K record, compressed
   int64_t raw_head_bytes;    // bytes of one (page, kv head) K record, raw
   float scale_log2;          // softmax_scale * log2(e)
 };
 
 struct Plan {
-  int grid = 0, chunk_pages = 1, max_chunks = 0, slices = 1;
-  size_t part_o_bytes = 0, ws_bytes = 0, smem = 0;
+  int grid = 0, max_chunks = 0, slices = 1, min_range_pages = 1;
+  size_t part_o_bytes = 0, part_lse_bytes = 0, ws_bytes = 0;
 };
 
 // What the metadata warp publishes for an item.
@@ -124,29 +129,57 @@ __device__ __forceinline__ void consumer_barrier() {
   asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
 }
 
+// Barrier over the consumer warps that also ORs a predicate across them (the same answer in all).
+template <int kWarps>
+__device__ __forceinline__ bool consumer_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kWarps * 32)
+      : "memory");
+  return r != 0;
+}
 
-// Item `item` of the flat list: its request, chunk, kv head, head slice, token range and tiles.
-__device__ __forceinline__ ItemDesc describe_item(const AttnArgs& a, const int* prefix, int item) {
+
+// Geometry of the page sequence: pair p = (request b, r = kv head * slices + slice) owns pages
+// [S_p, S_p + n_b) with S_p = HS * prefix[b] + r * n_b (HS pairs per request, n_b pages each).
+// CTA k owns [k W, (k + 1) W); within one CTA range a pair's pages are cut every pmax pages from
+// where they start.  Partials of a pair are numbered in page order across CTAs.
+struct Ranges {
+  int W, pmax, ppc;   // pages per CTA range, pages per item, items of a full range
+};
+
+// Partials of the pair starting at S that lie in CTA ranges before range k.
+__device__ __forceinline__ int chunks_before(const Ranges& g, int S, int k) {
+  const int k0 = S / g.W;
+  if (k <= k0) return 0;
+  const int first = (k0 + 1) * g.W - S;
+  return (first + g.pmax - 1) / g.pmax + (k - k0 - 1) * g.ppc;
+}
+
+// Partials of the pair with pages [S, S + n), n >= 1.
+__device__ __forceinline__ int pair_chunks(const Ranges& g, int S, int n) {
+  const int kl = (S + n - 1) / g.W;
+  const int tail = S + n - max(S, kl * g.W);
+  return chunks_before(g, S, kl) + (tail + g.pmax - 1) / g.pmax;
+}
+
+// The item covering pages [pg0, pg1) of pair (b, r) as partial c.
+__device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int r, int pg0, int pg1, int c,
+                                                   bool single) {
   ItemDesc d;
-  const int per = a.hkv * a.slices;
-  const int j = item / per;
-  const int r = item - j * per;
+  d.b = b;
+  d.c = c;
   d.g = r / a.slices;
   const int s = r - d.g * a.slices;
-  int lo = 0, hi = a.batch;                 // prefix[lo] <= j < prefix[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= j) lo = mid; else hi = mid;
-  }
-  d.b = lo;
-  d.c = j - prefix[lo];
-  d.single = (prefix[lo + 1] - prefix[lo]) == 1;
-  const int L = min(max(a.seq_lens[lo], 0), a.max_pages * a.page_size);
-  const int pages = (L + a.page_size - 1) / a.page_size;
-  const int p0 = d.c * a.chunk_pages;
-  const int p1 = min(p0 + a.chunk_pages, pages);
-  d.t0 = p0 * a.page_size;
-  d.t1 = min(p1 * a.page_size, L);
+  d.single = single;
+  const int L = min(max(a.seq_lens[b], 0), a.max_pages * a.page_size);
+  d.t0 = pg0 * a.page_size;
+  d.t1 = min(pg1 * a.page_size, L);
   d.units = (d.t1 - d.t0 + 15) >> 4;
   d.h0 = d.g * a.group + s * kHeadsPerSlice;
   d.nh = min(kHeadsPerSlice, a.group - s * kHeadsPerSlice);
@@ -282,7 +315,7 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- prologue: barriers, chunk counts per request and their prefix sums
+  // ---- prologue: barriers, pages per request and their prefix sums, the CTA ranges
   if (tid < 2) {
     mbar_init(&item_full[tid], 1);
     mbar_init(&q_full[tid], 1);
@@ -300,8 +333,7 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
       if (blockIdx.x == 0) report(a.status, ZF_DEV_BAD_SEQ_LEN);
       len = min(max(len, 0), max_len);
     }
-    const int pages = (len + a.page_size - 1) / a.page_size;
-    prefix[b + 1] = (pages + a.chunk_pages - 1) / a.chunk_pages;
+    prefix[b + 1] = (len + a.page_size - 1) / a.page_size;
   }
   fence_mbar_init();
   __syncthreads();
@@ -321,34 +353,80 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
     if (lane == 0) prefix[0] = 0;
   }
   __syncthreads();
-  const int total_items = prefix[a.batch] * a.hkv * a.slices;
+  const int HS = a.hkv * a.slices;
+  const int total = HS * prefix[a.batch];       // pages of all pairs (the host bounds it below 2^30)
+  Ranges g;
+  g.W = max((total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x), a.min_range_pages);
+  g.pmax = kMaxItemTiles / (a.page_size / ZF_BLOCK_TOKENS);
+  g.ppc = (g.W + g.pmax - 1) / g.pmax;
+  // partials per pair, for the merge kernel (spread over all CTAs)
+  for (int p = blockIdx.x * C::kThreads + tid; p < a.batch * HS; p += gridDim.x * C::kThreads) {
+    const int b = p / HS, r = p - b * HS;
+    const int n = prefix[b + 1] - prefix[b];
+    a.chunk_counts[p] = n > 0 ? pair_chunks(g, HS * prefix[b] + r * n, n) : 0;
+  }
   const uint64_t policy = l2_evict_first_policy();
 
   if (warp == kWarps) {
     // ============================================================== metadata warp
+    // Walk this CTA's page range [lo, hi) pair by pair, publishing one item at a time (double
+    // buffered), then an end marker.
     int k = 0;
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++k) {
+    bool ok = true;
+    auto publish = [&](const ItemDesc& d) -> bool {
       const int buf = k & 1;
-      bool ok = true;
-      if (lane == 0) ok = !*abort_flag && mbar_wait(&item_empty[buf], ((k >> 1) & 1u) ^ 1u);
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) {
+      bool good = true;
+      if (lane == 0) good = !*abort_flag && mbar_wait(&item_empty[buf], ((k >> 1) & 1u) ^ 1u);
+      good = __shfl_sync(0xFFFFFFFFu, good, 0);
+      if (!good) {
         if (lane == 0) {
           report(a.status, ZF_DEV_TIMEOUT);
           *abort_flag = 1;
         }
-        break;
+        return false;
       }
-      const ItemDesc d = describe_item(a, prefix, item);
-      resolve_tiles<kCompressed>(a, d, meta + buf * kMaxItemTiles, lane);
+      if (d.b >= 0) resolve_tiles<kCompressed>(a, d, meta + buf * kMaxItemTiles, lane);
       __syncwarp();
       if (lane == 0) {
         desc[buf] = d;
         mbar_arrive(&item_full[buf]);        // release: the tiles can be fetched
       }
-      stage_q(a, d, qbuf + buf * kHeadsPerSlice * kQRowBytes, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[buf]);   // release: the q rows
+      if (d.b >= 0) {
+        stage_q(a, d, qbuf + buf * kHeadsPerSlice * kQRowBytes, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[buf]);   // release: the q rows
+      }
+      ++k;
+      return true;
+    };
+    const long long lo_l = static_cast<long long>(blockIdx.x) * g.W;
+    const int hi = static_cast<int>(min(lo_l + g.W, static_cast<long long>(total)));
+    int t = static_cast<int>(min(lo_l, static_cast<long long>(total)));
+    int b = 0;
+    {   // the request holding page t: largest b with HS * prefix[b] <= t
+      int l = 0, h = a.batch;
+      while (h - l > 1) {
+        const int mid = (l + h) >> 1;
+        if (HS * prefix[mid] <= t) l = mid; else h = mid;
+      }
+      b = l;
+    }
+    while (ok && t < hi) {
+      while (HS * prefix[b + 1] <= t) ++b;       // skip requests without pages
+      const int n = prefix[b + 1] - prefix[b];
+      const int r = (t - HS * prefix[b]) / n;
+      const int S = HS * prefix[b] + r * n;
+      const int seg_end = min(hi, S + n);
+      const bool single = pair_chunks(g, S, n) == 1;
+      int c = chunks_before(g, S, blockIdx.x);
+      for (int pt = t; ok && pt < seg_end; pt += g.pmax, ++c)
+        ok = publish(describe_piece(a, b, r, pt - S, min(pt + g.pmax, seg_end) - S, c, single));
+      t = seg_end;
+    }
+    if (ok) {
+      ItemDesc end_marker{};
+      end_marker.b = -1;
+      publish(end_marker);
     }
     return;
   }
@@ -361,15 +439,16 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
   int sidx = 0;                 // stage of the next tile to consume
   uint32_t phase = 0;           // bit s: parity of the next wait on stage s
   uint32_t inflight = 0;        // bit s: stage s has copies armed and not yet waited for
-  int pending_item = -1;        // item whose first tile for this warp is already in flight
-  int k = 0;
-  for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++k) {
+  bool prefetched = false;      // this warp's first tile of the current item is already in flight
+  for (int k = 0;; ++k) {
     const int buf = k & 1;
     if (!aborted && (*abort_flag || !mbar_wait(&item_full[buf], (k >> 1) & 1u))) {
       aborted = true;
       *abort_flag = 1;
       report(a.status, ZF_DEV_TIMEOUT);
     }
+    // one decision for all consumer warps: stop at the end marker, or once any wait gave up
+    if (consumer_any<kWarps>(aborted || desc[buf].b < 0)) break;
     const ItemDesc d = desc[buf];
     const int* m = meta + buf * kMaxItemTiles;
     // Q^T as the B operand (k = channel, n = head): one 16-byte read gives this lane's words of
@@ -382,11 +461,11 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     // this warp's first tile of the item, unless it was prefetched during the previous item
-    if (!aborted && pending_item != item && warp < d.units) {
+    if (!prefetched && warp < d.units) {
       if (issue_tile<kCompressed>(a, d, m, warp, my_stages + sidx * C::kStageBytes, &my_bars[sidx], lane, policy))
         inflight |= 1u << sidx;
     }
-    pending_item = -1;
+    prefetched = false;
     if (!aborted && (*abort_flag || !mbar_wait(&q_full[buf], (k >> 1) & 1u))) {
       aborted = true;
       *abort_flag = 1;
@@ -400,18 +479,18 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
       uint8_t* next_stage = my_stages + ns * C::kStageBytes;
       if (un < d.units) {
         if (issue_tile<kCompressed>(a, d, m, un, next_stage, &my_bars[ns], lane, policy)) inflight |= 1u << ns;
-      } else if (item + static_cast<int>(gridDim.x) < total_items) {
-        const int nb = buf ^ 1;
+      } else {
+        const int nb = buf ^ 1;       // the next item (or the end marker) is published after this one
         if (*abort_flag || !mbar_wait(&item_full[nb], ((k + 1) >> 1) & 1u)) {
           aborted = true;
           *abort_flag = 1;
           report(a.status, ZF_DEV_TIMEOUT);
           break;
-        } else if (warp < desc[nb].units) {
+        } else if (desc[nb].b >= 0 && warp < desc[nb].units) {
           if (issue_tile<kCompressed>(a, desc[nb], meta + nb * kMaxItemTiles, warp, next_stage, &my_bars[ns], lane,
                                       policy))
             inflight |= 1u << ns;
-          pending_item = item + gridDim.x;
+          prefetched = true;
         }
       }
       // wait for the current tile
@@ -601,12 +680,12 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
 }
 
 struct MergeArgs {
-  const int32_t* seq_lens;
   const float* part_o;
   const float* part_lse;
   float* out;
   float* lse;
-  int32_t batch, hq, page_size, max_pages, chunk_pages, max_chunks;
+  const int32_t* chunk_counts;
+  int32_t batch, hq, group, slices, max_chunks;
 };
 
 // One warp per (request, query head): lse = log2 sum_i 2^lse_i, out = sum_i 2^(lse_i - lse) o_i.
@@ -617,10 +696,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   allow_next_grid();
   const int idx = blockIdx.x * 4 + warp;
   if (idx >= a.batch * a.hq) return;
-  const int b = idx / a.hq;
-  const int len = min(max(a.seq_lens[b], 0), a.max_pages * a.page_size);
-  const int pages = (len + a.page_size - 1) / a.page_size;
-  const int nch = (pages + a.chunk_pages - 1) / a.chunk_pages;
+  const int b = idx / a.hq, h = idx - b * a.hq;
+  const int gq = h / a.group;
+  const int nch = a.chunk_counts[(b * (a.hq / a.group) + gq) * a.slices + (h - gq * a.group) / kHeadsPerSlice];
   float4* outp = reinterpret_cast<float4*>(a.out + static_cast<size_t>(idx) * ZF_HEAD_DIM) + lane;
   if (nch == 1) return;
   const float* pl = a.part_lse + static_cast<size_t>(idx) * a.max_chunks;
@@ -665,28 +743,20 @@ static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, 
   const int group = hq / hkv;
   p.slices = (group + kHeadsPerSlice - 1) / kHeadsPerSlice;
   const long long pairs = static_cast<long long>(batch) * hkv * p.slices;
-  const int tiles = page_size / ZF_BLOCK_TOKENS;
-  long long best = LLONG_MAX;
-  int best_cp = 1;
-  const int cp_max = max_pages < kMaxItemTiles / tiles ? max_pages : kMaxItemTiles / tiles;
-  for (int cp = 1; cp <= cp_max; ++cp) {
-    const long long chunks = (max_pages + cp - 1) / cp;
-    const long long items = pairs * chunks;
-    const long long grid = items < num_sms ? items : num_sms;
-    const long long rounds = (items + grid - 1) / grid;
-    const long long cost = rounds * (static_cast<long long>(cp) * tiles + kItemOverheadTiles);
-    if (cost <= best) {          // ties go to the larger chunk (fewer partials)
-      best = cost;
-      best_cp = cp;
-    }
-  }
-  p.chunk_pages = best_cp;
-  p.max_chunks = (max_pages + best_cp - 1) / best_cp;
-  const long long items = pairs * p.max_chunks;
-  p.grid = static_cast<int>(items < num_sms ? (items > 0 ? items : 1) : num_sms);
+  const long long total_max = pairs * max_pages;     // pages when every request is full length
+  p.grid = static_cast<int>(total_max < num_sms ? (total_max > 0 ? total_max : 1) : num_sms);
+  // The kernel gives each CTA max(ceil(total / grid), min_range_pages) pages; a floor keeps the
+  // number of partials per pair, and so the workspace, bounded when requests are short.
+  const long long balanced = (total_max + p.grid - 1) / p.grid;
+  p.min_range_pages = static_cast<int>(balanced / kMinRangeDivisor > 1 ? balanced / kMinRangeDivisor : 1);
+  // A pair of n pages meets at most ceil(n / W) + 1 CTA ranges and is cut every pmax pages in
+  // each, so it has at most floor(n / pmax) + ceil(n / W) + 1 partials.
+  const int pmax = kMaxItemTiles / (page_size / ZF_BLOCK_TOKENS);
+  p.max_chunks = max_pages / pmax + (max_pages + p.min_range_pages - 1) / p.min_range_pages + 1;
   const size_t n = static_cast<size_t>(batch) * hq * p.max_chunks;
   p.part_o_bytes = n * ZF_HEAD_DIM * 4;
-  p.ws_bytes = p.part_o_bytes + ((n * 4 + 255) & ~static_cast<size_t>(255));
+  p.part_lse_bytes = (n * 4 + 255) & ~static_cast<size_t>(255);
+  p.ws_bytes = p.part_o_bytes + p.part_lse_bytes + ((static_cast<size_t>(pairs) * 4 + 255) & ~static_cast<size_t>(255));
   return p;
 }
 
@@ -714,8 +784,12 @@ static zf_status current_sm_count(int* sms) {
 }
 
 static bool attn_shape_ok(int batch, int hq, int hkv, int max_pages) {
-  return batch >= 0 && batch <= ZF_MAX_BATCH && hkv >= 1 && hq >= hkv && hq % hkv == 0 && max_pages >= 1 &&
-         static_cast<long long>(max_pages) * ZF_MAX_PAGE_SIZE < INT_MAX;
+  if (!(batch >= 0 && batch <= ZF_MAX_BATCH && hkv >= 1 && hq >= hkv && hq % hkv == 0 && max_pages >= 1 &&
+        static_cast<long long>(max_pages) * ZF_MAX_PAGE_SIZE < INT_MAX))
+    return false;
+  // the kernel indexes the pages of all (request, kv head, head slice) pairs with 32-bit ints
+  const long long slices = (hq / hkv + kHeadsPerSlice - 1) / kHeadsPerSlice;
+  return static_cast<long long>(batch) * hkv * slices * max_pages < (1ll << 30);
 }
 
 template <bool kCompressed>
@@ -753,6 +827,7 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   a.lse = lse;
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.part_o_bytes);
+  a.chunk_counts = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + p.part_o_bytes + p.part_lse_bytes);
   a.batch = batch;
   a.hq = hq;
   a.hkv = c->num_kv_heads;
@@ -762,8 +837,8 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   a.num_pages = c->num_pages;
   a.num_raw = c->num_raw_slots;
   a.max_pages = max_pages;
-  a.chunk_pages = p.chunk_pages;
   a.max_chunks = p.max_chunks;
+  a.min_range_pages = p.min_range_pages;
   a.comp_head_bytes = static_cast<int64_t>(c->page_size / 4) * kSlotBytes;
   a.raw_head_bytes = static_cast<int64_t>(c->page_size / 4) * kRawBlockBytes;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -788,16 +863,15 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   if (cudaLaunchKernelEx(&cfg, attn_kernel<kCompressed>, a) != cudaSuccess) return ZF_ERR_CUDA;
 
   MergeArgs m{};
-  m.seq_lens = seq_lens;
   m.part_o = a.part_o;
   m.part_lse = a.part_lse;
   m.out = out;
   m.lse = lse;
   m.batch = batch;
   m.hq = hq;
-  m.page_size = c->page_size;
-  m.max_pages = max_pages;
-  m.chunk_pages = p.chunk_pages;
+  m.chunk_counts = a.chunk_counts;
+  m.group = a.group;
+  m.slices = a.slices;
   m.max_chunks = p.max_chunks;
   const int rows = batch * hq;
   cudaLaunchConfig_t mcfg = cfg;

@@ -51,6 +51,9 @@ struct Cfg {
   static constexpr int kStageBytes = kCompressed ? 6272 : 8192;
   static constexpr int kVOffset = kCompressed ? 3136 : 4096;   // V tile within a stage
   static constexpr int kThreads = (kWarps + 1) * 32;
+  // tiles per CTA prefetched into L2 at start-up (measured best on a 32-layer MHA step: two per
+  // warp for the compressed kernel, four per warp for the dense one)
+  static constexpr int kPrefetchTiles = kCompressed ? 2 * kWarps : 4 * kWarps;
 };
 constexpr int kWarpStages = 2;
 constexpr int kTileCompBytes = 4 * kSlotBytes;      // 3136: one 16-token tile of K (or V), compressed
@@ -64,6 +67,10 @@ constexpr int kQRowBytes = 320;
 constexpr int kOStride = 132;                       // padded combine row (conflict-free writes)
 // partial chunks per pair are sized for ranges of at least (balanced range) / kMinRangeDivisor pages
 constexpr int kMinRangeDivisor = 16;
+// start-up prefetch: used when a CTA's balanced share is between these numbers of tiles (below,
+// the preceding call's tail is too short to hide the extra planning)
+constexpr int kPrefetchMinTilesPerCta = 16;
+constexpr int kPrefetchMaxTilesPerCta = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p <= 2^8 between max updates
 
@@ -86,23 +93,26 @@ struct AttnArgs {
   int32_t* chunk_counts;     // [batch][hkv * slices] partials per pair, for the merge kernel
   int32_t batch, hq, hkv, group, slices, page_size, num_pages, num_raw, max_pages, max_chunks;
   int32_t min_range_pages;   // lower bound of the pages per CTA range
+  int32_t chunk_pages;       // > 0: fixed chunks of this many pages, items dealt round-robin
+  int32_t prefetch;          // plan and prefetch the first tiles while the preceding grid drains
   int64_t comp_head_bytes;   // bytes of one (page, kv head) K record, compressed
   int64_t raw_head_bytes;    // bytes of one (page, kv head) K record, raw
   float scale_log2;          // softmax_scale * log2(e)
 };
 
 struct Plan {
-  int grid = 0, max_chunks = 0, slices = 1, min_range_pages = 1;
+  int grid = 0, max_chunks = 0, slices = 1, min_range_pages = 1, chunk_pages = 0;
+  bool prefetch = false;
   size_t part_o_bytes = 0, part_lse_bytes = 0, ws_bytes = 0;
 };
 
 // What the metadata warp publishes for an item.
 struct ItemDesc {
-  int b, c, g, t0, t1, units, h0, nh, single;
+  int b, c, g, t0, t1, units, h0, nh, single, pg0, npg;   // pg0, npg: the item's pages in the request
 };
 
 struct SmemLayout {
-  size_t stages, item_full, q_full, item_empty, misc, desc, meta, qbuf, bars, prefix, total;
+  size_t stages, item_full, q_full, item_empty, misc, desc, meta, qbuf, bars, prefix, tails, total;
 };
 
 template <bool kCompressed>
@@ -120,6 +130,7 @@ __host__ __device__ inline SmemLayout smem_layout(int batch) {
   s.qbuf = at; at += 2 * kHeadsPerSlice * kQRowBytes;
   s.bars = at; at += static_cast<size_t>(C::kWarps) * kWarpStages * 8;
   s.prefix = at; at += static_cast<size_t>(batch + 1) * 4;
+  s.tails = at; at += static_cast<size_t>(batch);        // tokens in each request's last page, minus 1
   s.total = (at + 127) & ~static_cast<size_t>(127);
   return s;
 }
@@ -169,15 +180,18 @@ __device__ __forceinline__ int pair_chunks(const Ranges& g, int S, int n) {
 }
 
 // The item covering pages [pg0, pg1) of pair (b, r) as partial c.
+// n: pages of request b; tail: tokens in its last page.
 __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int r, int pg0, int pg1, int c,
-                                                   bool single) {
+                                                   bool single, int n, int tail) {
   ItemDesc d;
   d.b = b;
   d.c = c;
-  d.g = r / a.slices;
+  d.g = a.slices == 1 ? r : r / a.slices;
   const int s = r - d.g * a.slices;
   d.single = single;
-  const int L = min(max(a.seq_lens[b], 0), a.max_pages * a.page_size);
+  d.pg0 = pg0;
+  d.npg = pg1 - pg0;
+  const int L = (n - 1) * a.page_size + tail;
   d.t0 = pg0 * a.page_size;
   d.t1 = min(pg1 * a.page_size, L);
   d.units = (d.t1 - d.t0 + 15) >> 4;
@@ -188,18 +202,18 @@ __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int
 
 // Resolve the item's pages into one entry per tile: meta[u] = slot << 5 | tile_in_page << 2 | kind
 // (all 32 lanes).  All page-table loads are issued before the directory loads that depend on them.
-template <bool kCompressed>
+// kSpec: relaxed loads of values that may still change, and no error reports (prefetch planning).
+template <bool kCompressed, bool kSpec = false>
 __device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc& d, int* meta, int lane) {
   constexpr int kPer = kMaxItemTiles / 32;
-  const int tpp = a.page_size / ZF_BLOCK_TOKENS;
-  const int p0 = d.t0 / a.page_size;
-  const int npg = (d.t1 - d.t0 + a.page_size - 1) / a.page_size;
-  const int32_t* row = a.page_table + static_cast<size_t>(d.b) * a.max_pages + p0;
+  const int tpp = a.page_size >> 4;
+  const int npg = d.npg;
+  const int32_t* row = a.page_table + static_cast<size_t>(d.b) * a.max_pages + d.pg0;
   int pid[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int i = lane + 32 * k;
-    pid[k] = i < npg ? row[i] : -1;
+    pid[k] = i < npg ? (kSpec ? ld_relaxed(row + i) : row[i]) : -1;
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
@@ -208,23 +222,24 @@ __device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc&
     int kind = kKindInvalid, slot = 0;
     if (kCompressed) {
       if (pid[k] >= 0 && pid[k] < a.num_pages) {
-        const int dd = a.dir[static_cast<size_t>(pid[k]) * a.hkv + d.g];
+        const int32_t* dp = a.dir + static_cast<size_t>(pid[k]) * a.hkv + d.g;
+        const int dd = kSpec ? ld_relaxed(dp) : *dp;
         if (dd == ZF_DIR_COMPRESSED) {
           kind = kKindComp;
           slot = pid[k];
         } else if (dd >= 0 && dd < a.num_raw) {
           kind = kKindRaw;
           slot = dd;
-        } else {
+        } else if (!kSpec) {
           report(a.status, ZF_DEV_BAD_DIR);
         }
-      } else {
+      } else if (!kSpec) {
         report(a.status, ZF_DEV_BAD_PAGE_ID);
       }
     } else if (pid[k] >= 0 && pid[k] < a.num_raw) {
       kind = kKindRaw;
       slot = pid[k];
-    } else {
+    } else if (!kSpec) {
       report(a.status, ZF_DEV_BAD_PAGE_ID);
     }
     for (int t = 0; t < tpp; ++t) {
@@ -280,62 +295,45 @@ __device__ __forceinline__ void issue_raw_v(const AttnArgs& a, const ItemDesc& d
   }
 }
 
-// Stage q rows of an item into qbuf (permuted, padded layout; rows past nh are zero).
-__device__ __forceinline__ void stage_q(const AttnArgs& a, const ItemDesc& d, uint8_t* qb, int lane) {
-  // 8 rows x 64 words; lane handles word w = lane and lane + 32 of every row
-  for (int r = 0; r < kHeadsPerSlice; ++r) {
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(d.b) * a.hq + d.h0 + min(r, d.nh - 1)) * ZF_HEAD_DIM);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(qb + r * kQRowBytes);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int w = lane + 32 * h;              // channel word w = 16j + 4r' + t  (t < 4, r' < 4)
-      const int j = w >> 4, rr = (w >> 2) & 3, t = w & 3;
-      dst[16 * j + 4 * t + rr] = r < d.nh ? src[w] : 0u;
+// L2 prefetch of the K and V records of tiles [0, n) of an item (lanes split the tiles).
+template <bool kCompressed>
+__device__ __forceinline__ void prefetch_item_tiles(const AttnArgs& a, const ItemDesc& d, const int* meta, int n,
+                                                    int lane) {
+  for (int u = lane; u < n; u += 32) {
+    const int m = meta[u];
+    const int kind = m & 3;
+    const size_t head = static_cast<size_t>(m >> 5) * a.hkv + d.g;
+    const int t = (m >> 2) & 7;
+    if (kCompressed && kind == kKindComp) {
+      const size_t off = head * a.comp_head_bytes + static_cast<size_t>(t) * kTileCompBytes;
+      bulk_prefetch_l2(a.k_comp + off, kTileCompBytes);
+      bulk_prefetch_l2(a.v_comp + off, kTileCompBytes);
+    } else if (kind == kKindRaw) {
+      const size_t off = head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes;
+      bulk_prefetch_l2(a.k_raw + off, kTileRawBytes);
+      bulk_prefetch_l2(a.v_raw + off, kTileRawBytes);
     }
   }
 }
 
-template <bool kCompressed>
-__global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(const AttnArgs a) {
-  using C = Cfg<kCompressed>;
-  constexpr int kWarps = C::kWarps;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const SmemLayout L = smem_layout<kCompressed>(a.batch);
-  uint64_t* item_full = reinterpret_cast<uint64_t*>(smem + L.item_full);
-  uint64_t* item_empty = reinterpret_cast<uint64_t*>(smem + L.item_empty);
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + L.q_full);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
-  int* combine_stage = reinterpret_cast<int*>(smem + L.misc + 16);
-  ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + L.desc);
-  int* meta = reinterpret_cast<int*>(smem + L.meta);
-  uint8_t* qbuf = smem + L.qbuf;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  int* prefix = reinterpret_cast<int*>(smem + L.prefix);
-  uint8_t* stages = smem + L.stages;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- prologue: barriers, pages per request and their prefix sums, the CTA ranges
-  if (tid < 2) {
-    mbar_init(&item_full[tid], 1);
-    mbar_init(&q_full[tid], 1);
-    mbar_init(&item_empty[tid], kWarps);
-  }
-  if (tid < kWarps * kWarpStages) mbar_init(&bars[tid], 1);
-  if (tid == 0) *abort_flag = 0;
-  // everything above touched only shared memory; inputs may come from the preceding grid
-  wait_prior_grid();
-  allow_next_grid();
+// Pages of every request (chunks, when chunk_pages > 0) into prefix[b + 1], then prefix sums
+// (prefix[0] = 0); tokens of each request's last page, minus 1, into tails[b].  All threads; ends
+// with a barrier.
+// kSpec: relaxed loads, no error reports.
+template <bool kSpec, int kThreads>
+__device__ __forceinline__ void load_lengths(const AttnArgs& a, int* prefix, uint8_t* tails, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
   const int max_len = a.max_pages * a.page_size;
-  for (int b = tid; b < a.batch; b += C::kThreads) {
-    int len = a.seq_lens[b];
+  for (int b = tid; b < a.batch; b += kThreads) {
+    int len = kSpec ? ld_relaxed(a.seq_lens + b) : a.seq_lens[b];
     if (len < 0 || len > max_len) {
-      if (blockIdx.x == 0) report(a.status, ZF_DEV_BAD_SEQ_LEN);
+      if (!kSpec && blockIdx.x == 0) report(a.status, ZF_DEV_BAD_SEQ_LEN);
       len = min(max(len, 0), max_len);
     }
-    prefix[b + 1] = (len + a.page_size - 1) / a.page_size;
+    const int pages = (len + a.page_size - 1) / a.page_size;
+    prefix[b + 1] = a.chunk_pages > 0 ? (pages + a.chunk_pages - 1) / a.chunk_pages : pages;
+    tails[b] = static_cast<uint8_t>(len - (pages - 1) * a.page_size - 1);   // unused when pages == 0
   }
-  fence_mbar_init();
   __syncthreads();
   if (warp == 0) {
     int carry = 0;
@@ -353,26 +351,179 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
     if (lane == 0) prefix[0] = 0;
   }
   __syncthreads();
-  const int HS = a.hkv * a.slices;
-  const int total = HS * prefix[a.batch];       // pages of all pairs (the host bounds it below 2^30)
+}
+
+__device__ __forceinline__ Ranges make_ranges(const AttnArgs& a, int total) {
   Ranges g;
   g.W = max((total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x), a.min_range_pages);
   g.pmax = kMaxItemTiles / (a.page_size / ZF_BLOCK_TOKENS);
   g.ppc = (g.W + g.pmax - 1) / g.pmax;
-  // partials per pair, for the merge kernel (spread over all CTAs)
-  for (int p = blockIdx.x * C::kThreads + tid; p < a.batch * HS; p += gridDim.x * C::kThreads) {
-    const int b = p / HS, r = p - b * HS;
-    const int n = prefix[b + 1] - prefix[b];
-    a.chunk_counts[p] = n > 0 ? pair_chunks(g, HS * prefix[b] + r * n, n) : 0;
+  return g;
+}
+
+// Walk this CTA's items and hand each to emit(desc) (uniform across the warp); stops early when emit
+// returns false.  Returns whether the walk ran to its end.
+//  * balanced mode (chunk_pages == 0): this CTA's page range, pair by pair;
+//  * chunked mode: items (request, chunk, kv head / slice) of chunk_pages pages, dealt round-robin
+//    (item i to CTA i % grid); prefix holds chunk counts.
+template <bool kSpec, typename Emit>
+__device__ __forceinline__ bool walk_range(const AttnArgs& a, const int* prefix, const uint8_t* tails, const Ranges& g,
+                                           int HS, Emit&& emit) {
+  if (a.chunk_pages > 0) {
+    const int cp = a.chunk_pages;
+    const int items = HS * prefix[a.batch];
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+      const int j = item / HS, r = item - j * HS;
+      int l = 0, h = a.batch;                 // prefix[l] <= j < prefix[l + 1]
+      while (h - l > 1) {
+        const int mid = (l + h) >> 1;
+        if (prefix[mid] <= j) l = mid; else h = mid;
+      }
+      const int c = j - prefix[l];
+      const int len = min(max(kSpec ? ld_relaxed(a.seq_lens + l) : a.seq_lens[l], 0), a.max_pages * a.page_size);
+      const int n = (len + a.page_size - 1) / a.page_size;
+      if (!emit(describe_piece(a, l, r, c * cp, min(c * cp + cp, n), c, prefix[l + 1] - prefix[l] == 1, n,
+                               tails[l] + 1)))
+        return false;
+    }
+    return true;
   }
+  const int total = HS * prefix[a.batch];
+  const long long lo_l = static_cast<long long>(blockIdx.x) * g.W;
+  const int hi = static_cast<int>(min(lo_l + g.W, static_cast<long long>(total)));
+  int t = static_cast<int>(min(lo_l, static_cast<long long>(total)));
+  if (t >= hi) return true;
+  int b = 0;
+  {   // the request holding page t: largest b with HS * prefix[b] <= t
+    int l = 0, h = a.batch;
+    while (h - l > 1) {
+      const int mid = (l + h) >> 1;
+      if (HS * prefix[mid] <= t) l = mid; else h = mid;
+    }
+    b = l;
+  }
+  // the first pair may have started in an earlier range; every later one starts in this range,
+  // so only the first needs the division-based geometry
+  while (HS * prefix[b + 1] <= t) ++b;
+  int n = prefix[b + 1] - prefix[b];
+  int r = (t - HS * prefix[b]) / n;
+  int S = HS * prefix[b] + r * n;
+  int c = chunks_before(g, S, blockIdx.x);
+  bool single = pair_chunks(g, S, n) == 1;
+  const long long range_end = lo_l + g.W;
+  while (true) {
+    const int seg_end = min(hi, S + n);
+    for (int pt = t; pt < seg_end; pt += g.pmax, ++c)
+      if (!emit(describe_piece(a, b, r, pt - S, min(pt + g.pmax, seg_end) - S, c, single, n, tails[b] + 1)))
+        return false;
+    t = seg_end;
+    if (t >= hi) return true;
+    if (++r == HS) {                           // next request with pages
+      r = 0;
+      do { ++b; } while (prefix[b + 1] == prefix[b]);
+      n = prefix[b + 1] - prefix[b];
+    }
+    S = t;
+    c = 0;
+    single = n <= g.pmax && S + n <= range_end;
+  }
+}
+
+// Stage q rows of an item into qbuf (permuted, padded layout; rows past nh are zero).
+__device__ __forceinline__ void stage_q(const AttnArgs& a, const ItemDesc& d, uint8_t* qb, int lane) {
+  // 8 rows x 64 words; lane handles word w = lane and lane + 32 of every row
+  for (int r = 0; r < kHeadsPerSlice; ++r) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(d.b) * a.hq + d.h0 + min(r, d.nh - 1)) * ZF_HEAD_DIM);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(qb + r * kQRowBytes);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int w = lane + 32 * h;              // channel word w = 16j + 4r' + t  (t < 4, r' < 4)
+      const int j = w >> 4, rr = (w >> 2) & 3, t = w & 3;
+      dst[16 * j + 4 * t + rr] = r < d.nh ? src[w] : 0u;
+    }
+  }
+}
+
+template <bool kCompressed>
+// At most 112 registers per thread (the compiler needs 104 for the compressed variant, without
+// spills): 16 warps then leave room on every SM sub-partition for a merge warp, so the merge grid
+// of the previous call and this grid's CTAs can be resident together.
+__global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
+  using C = Cfg<kCompressed>;
+  constexpr int kWarps = C::kWarps;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const SmemLayout L = smem_layout<kCompressed>(a.batch);
+  uint64_t* item_full = reinterpret_cast<uint64_t*>(smem + L.item_full);
+  uint64_t* item_empty = reinterpret_cast<uint64_t*>(smem + L.item_empty);
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + L.q_full);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+  int* combine_stage = reinterpret_cast<int*>(smem + L.misc + 16);
+  ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + L.desc);
+  int* meta = reinterpret_cast<int*>(smem + L.meta);
+  uint8_t* qbuf = smem + L.qbuf;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  int* prefix = reinterpret_cast<int*>(smem + L.prefix);
+  uint8_t* tails = smem + L.tails;
+  uint8_t* stages = smem + L.stages;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- prologue: barriers, pages per request and their prefix sums, the CTA ranges
+  if (tid < 2) {
+    mbar_init(&item_full[tid], 1);
+    mbar_init(&q_full[tid], 1);
+    mbar_init(&item_empty[tid], kWarps);
+  }
+  if (tid < kWarps * kWarpStages) mbar_init(&bars[tid], 1);
+  if (tid == 0) *abort_flag = 0;
+  fence_mbar_init();
+  const int HS = a.hkv * a.slices;
+  // While the preceding grid drains (this grid is launched early, see allow_next_grid): L2 hints.
+  // (1) lines of seq_lens, the page table and, up to 8 MB, the directory, spread over the grid;
+  // (2) for short calls, the K/V records of this CTA's first kPrefetchTiles tiles, planned from
+  //     relaxed reads of lengths, page table and directory that may still change.  Nothing read
+  //     here is used after the wait: the plan is redone from the final values.
+  {
+    const size_t n_len = (static_cast<size_t>(a.batch) * 4 + 127) / 128;
+    const size_t n_tab = (static_cast<size_t>(a.batch) * a.max_pages * 4 + 127) / 128;
+    const size_t dir_bytes = static_cast<size_t>(a.num_pages) * a.hkv * 4;
+    const size_t n_dir = kCompressed && dir_bytes <= (8u << 20) ? (dir_bytes + 127) / 128 : 0;
+    const size_t stride = static_cast<size_t>(gridDim.x) * C::kThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * C::kThreads + tid; i < n_len + n_tab + n_dir; i += stride) {
+      const void* line = i < n_len ? static_cast<const void*>(reinterpret_cast<const uint8_t*>(a.seq_lens) + 128 * i)
+                         : i < n_len + n_tab
+                             ? static_cast<const void*>(reinterpret_cast<const uint8_t*>(a.page_table) + 128 * (i - n_len))
+                             : static_cast<const void*>(reinterpret_cast<const uint8_t*>(a.dir) + 128 * (i - n_len - n_tab));
+      prefetch_l2(line);
+    }
+    if (a.prefetch) load_lengths<true, C::kThreads>(a, prefix, tails, tid);
+    if (a.prefetch && warp == kWarps) {
+      const Ranges g = make_ranges(a, HS * prefix[a.batch]);
+      int budget = C::kPrefetchTiles;
+      walk_range<true>(a, prefix, tails, g, HS, [&](const ItemDesc& d) -> bool {
+        resolve_tiles<kCompressed, true>(a, d, meta, lane);
+        __syncwarp();
+        const int n = min(d.units, budget);
+        prefetch_item_tiles<kCompressed>(a, d, meta, n, lane);
+        __syncwarp();
+        budget -= n;
+        return budget > 0;
+      });
+    }
+    __syncthreads();
+  }
+  wait_prior_grid();          // inputs may come from the preceding grid
+  allow_next_grid();
+  load_lengths<false, C::kThreads>(a, prefix, tails, tid);
+  const int total = HS * prefix[a.batch];       // pages (items) of all pairs (the host bounds it below 2^30)
+  const Ranges g = make_ranges(a, total);
   const uint64_t policy = l2_evict_first_policy();
 
   if (warp == kWarps) {
     // ============================================================== metadata warp
-    // Walk this CTA's page range [lo, hi) pair by pair, publishing one item at a time (double
-    // buffered), then an end marker.
+    // Walk this CTA's page range, publishing one item at a time (double buffered), then an end
+    // marker.
     int k = 0;
-    bool ok = true;
     auto publish = [&](const ItemDesc& d) -> bool {
       const int buf = k & 1;
       bool good = true;
@@ -399,31 +550,7 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
       ++k;
       return true;
     };
-    const long long lo_l = static_cast<long long>(blockIdx.x) * g.W;
-    const int hi = static_cast<int>(min(lo_l + g.W, static_cast<long long>(total)));
-    int t = static_cast<int>(min(lo_l, static_cast<long long>(total)));
-    int b = 0;
-    {   // the request holding page t: largest b with HS * prefix[b] <= t
-      int l = 0, h = a.batch;
-      while (h - l > 1) {
-        const int mid = (l + h) >> 1;
-        if (HS * prefix[mid] <= t) l = mid; else h = mid;
-      }
-      b = l;
-    }
-    while (ok && t < hi) {
-      while (HS * prefix[b + 1] <= t) ++b;       // skip requests without pages
-      const int n = prefix[b + 1] - prefix[b];
-      const int r = (t - HS * prefix[b]) / n;
-      const int S = HS * prefix[b] + r * n;
-      const int seg_end = min(hi, S + n);
-      const bool single = pair_chunks(g, S, n) == 1;
-      int c = chunks_before(g, S, blockIdx.x);
-      for (int pt = t; ok && pt < seg_end; pt += g.pmax, ++c)
-        ok = publish(describe_piece(a, b, r, pt - S, min(pt + g.pmax, seg_end) - S, c, single));
-      t = seg_end;
-    }
-    if (ok) {
+    if (walk_range<false>(a, prefix, tails, g, HS, publish)) {
       ItemDesc end_marker{};
       end_marker.b = -1;
       publish(end_marker);
@@ -432,6 +559,12 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
   }
 
   // ================================================================== consumer warps
+  // partials per pair, for the merge kernel (spread over all CTAs; off the metadata warp's path)
+  for (int p = blockIdx.x * (kWarps * 32) + tid; p < a.batch * HS; p += gridDim.x * (kWarps * 32)) {
+    const int b = p / HS, r = p - b * HS;
+    const int n = prefix[b + 1] - prefix[b];
+    a.chunk_counts[p] = a.chunk_pages > 0 ? n : n > 0 ? pair_chunks(g, HS * prefix[b] + r * n, n) : 0;
+  }
   const int gi = lane >> 2, ti = lane & 3;
   uint8_t* my_stages = stages + static_cast<size_t>(warp) * kWarpStages * C::kStageBytes;
   uint64_t* my_bars = bars + warp * kWarpStages;
@@ -589,8 +722,10 @@ __global__ void __launch_bounds__(Cfg<kCompressed>::kThreads, 1) attn_kernel(con
           uint32_t va[8];
           if (comp) rebuild_lane(vp + j * kSlotBytes, lane, va);
           else load_raw_lane(vp + j * kRawBlockBytes, lane, va);
-          va[0] &= keep_a; va[1] &= keep_a; va[4] &= keep_a; va[5] &= keep_a;
-          va[2] &= keep_b; va[3] &= keep_b; va[6] &= keep_b; va[7] &= keep_b;
+          if (ntok < 16) {         // the context's last tile only
+            va[0] &= keep_a; va[1] &= keep_a; va[4] &= keep_a; va[5] &= keep_a;
+            va[2] &= keep_b; va[3] &= keep_b; va[6] &= keep_b; va[7] &= keep_b;
+          }
           mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bh0, bh1);
           mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bh0, bh1);
           mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bl0, bl1);
@@ -690,21 +825,36 @@ struct MergeArgs {
 
 // One warp per (request, query head): lse = log2 sum_i 2^lse_i, out = sum_i 2^(lse_i - lse) o_i.
 // Requests with one chunk were finished by the attention kernel; empty requests get 0 / -inf.
-__global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
+// The first 32 chunk LSEs and the first kPreload chunk outputs are loaded together with the chunk
+// count (slots past the count hold stale values and are never used), so the chain is one round
+// trip to L2 instead of three.  Blocks of two warps; the kernel's 64 registers per thread fit on an
+// SM sub-partition beside four attention warps of at most 112 registers.
+constexpr int kPreload = 8;
+constexpr int kMergeWarps = 2;
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  wait_prior_grid();                       // the attention grid's partials
+  // The next grid (the next call's attention) may launch right away: its CTAs take SMs as this
+  // call's attention CTAs retire and use the wait to prefetch; they read nothing final before
+  // this grid completes.
   allow_next_grid();
-  const int idx = blockIdx.x * 4 + warp;
+  wait_prior_grid();                       // the attention grid's partials
+  const int idx = blockIdx.x * kMergeWarps + warp;
   if (idx >= a.batch * a.hq) return;
   const int b = idx / a.hq, h = idx - b * a.hq;
   const int gq = h / a.group;
+  const float* pl = a.part_lse + static_cast<size_t>(idx) * a.max_chunks;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + static_cast<size_t>(idx) * a.max_chunks * ZF_HEAD_DIM) + lane;
+  const float lse_lane = lane < a.max_chunks ? pl[lane] : -CUDART_INF_F;
+  float4 pre[kPreload];
+#pragma unroll
+  for (int j = 0; j < kPreload; ++j)
+    pre[j] = j < a.max_chunks ? po[static_cast<size_t>(j) * (ZF_HEAD_DIM / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
   const int nch = a.chunk_counts[(b * (a.hq / a.group) + gq) * a.slices + (h - gq * a.group) / kHeadsPerSlice];
   float4* outp = reinterpret_cast<float4*>(a.out + static_cast<size_t>(idx) * ZF_HEAD_DIM) + lane;
   if (nch == 1) return;
-  const float* pl = a.part_lse + static_cast<size_t>(idx) * a.max_chunks;
   // chunk log-sum-exps, one per lane: max and sum of 2^(lse_i - max) by warp reductions
-  float M = -CUDART_INF_F;
-  for (int i = lane; i < nch; i += 32) M = fmaxf(M, pl[i]);
+  float M = lane < nch ? lse_lane : -CUDART_INF_F;
+  for (int i = lane + 32; i < nch; i += 32) M = fmaxf(M, pl[i]);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, d));
   if (nch == 0 || M == -CUDART_INF_F) {
@@ -712,18 +862,27 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
     if (lane == 0) a.lse[idx] = -CUDART_INF_F;
     return;
   }
-  float lsum = 0.f;
-  for (int i = lane; i < nch; i += 32) lsum += exp2f(pl[i] - M);
+  const float w0 = lane < nch ? fast_exp2(lse_lane - M) : 0.f;
+  float lsum = w0;
+  for (int i = lane + 32; i < nch; i += 32) lsum += fast_exp2(pl[i] - M);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, d);
   // weighted sum of the chunk outputs: lane owns 4 channels; weights come from the owning lane
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* po = reinterpret_cast<const float4*>(a.part_o + static_cast<size_t>(idx) * a.max_chunks * ZF_HEAD_DIM) + lane;
+#pragma unroll
+  for (int j = 0; j < kPreload; ++j) {
+    const float f = __shfl_sync(0xFFFFFFFFu, w0, j);
+    if (j < nch) {
+      acc.x += f * pre[j].x;
+      acc.y += f * pre[j].y;
+      acc.z += f * pre[j].z;
+      acc.w += f * pre[j].w;
+    }
+  }
   for (int c0 = 0; c0 < nch; c0 += 32) {
-    const float w = c0 + lane < nch ? exp2f(pl[c0 + lane] - M) : 0.f;
+    const float w = c0 == 0 ? w0 : (c0 + lane < nch ? fast_exp2(pl[c0 + lane] - M) : 0.f);
     const int n = min(32, nch - c0);
-#pragma unroll 8
-    for (int j = 0; j < n; ++j) {
+    for (int j = c0 == 0 ? kPreload : 0; j < n; ++j) {
       const float f = __shfl_sync(0xFFFFFFFFu, w, j);
       const float4 v = po[static_cast<size_t>(c0 + j) * (ZF_HEAD_DIM / 4)];
       acc.x += f * v.x;
@@ -732,32 +891,73 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
       acc.w += f * v.w;
     }
   }
-  const float inv = 1.f / lsum;
+  const float inv = __fdividef(1.f, lsum);
   *outp = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lane == 0) a.lse[idx] = (M + log2f(lsum)) * kLn2;
+  if (lane == 0) a.lse[idx] = (M + fast_log2(lsum)) * kLn2;
 }
 
 // ------------------------------------------------------------------------------- host planner
-static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, int num_sms) {
+// Work split for one call, from the sizes alone (requests assumed at max_pages).  Two modes, whichever
+// the cost model (rounds of tiles per warp on the busiest CTA, plus one round per item) prefers:
+//  * balanced ranges: every CTA gets the same number of pages, wherever requests start and end;
+//    best for long and ragged contexts;
+//  * fixed chunks of cp pages, items dealt round-robin: for short contexts, where the per-item cost
+//    dominates and chunks that never straddle a request boundary save items.
+static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, int num_sms, int warps) {
   Plan p;
   const int group = hq / hkv;
   p.slices = (group + kHeadsPerSlice - 1) / kHeadsPerSlice;
   const long long pairs = static_cast<long long>(batch) * hkv * p.slices;
   const long long total_max = pairs * max_pages;     // pages when every request is full length
-  p.grid = static_cast<int>(total_max < num_sms ? (total_max > 0 ? total_max : 1) : num_sms);
-  // The kernel gives each CTA max(ceil(total / grid), min_range_pages) pages; a floor keeps the
-  // number of partials per pair, and so the workspace, bounded when requests are short.
-  const long long balanced = (total_max + p.grid - 1) / p.grid;
-  p.min_range_pages = static_cast<int>(balanced / kMinRangeDivisor > 1 ? balanced / kMinRangeDivisor : 1);
-  // A pair of n pages meets at most ceil(n / W) + 1 CTA ranges and is cut every pmax pages in
-  // each, so it has at most floor(n / pmax) + ceil(n / W) + 1 partials.
-  const int pmax = kMaxItemTiles / (page_size / ZF_BLOCK_TOKENS);
-  p.max_chunks = max_pages / pmax + (max_pages + p.min_range_pages - 1) / p.min_range_pages + 1;
+  const int tpp = page_size / ZF_BLOCK_TOKENS;
+  const int pmax = kMaxItemTiles / tpp;
+  const int grid_b = static_cast<int>(total_max < num_sms ? (total_max > 0 ? total_max : 1) : num_sms);
+  const long long balanced = (total_max + grid_b - 1) / grid_b;
+  auto rounds = [&](long long tiles) { return (tiles + warps - 1) / warps; };
+  // balanced: the busiest CTA meets up to 1 + W / max_pages requests and cuts every pmax pages
+  const long long cost_b = rounds(balanced * tpp) + 1 + 1 + (balanced + max_pages - 1) / max_pages + balanced / pmax;
+  long long cost_c = LLONG_MAX;
+  int best_cp = 0;
+  const int cp_max = max_pages < pmax ? max_pages : pmax;
+  for (int cp = 1; cp <= cp_max; ++cp) {
+    const long long items = pairs * ((max_pages + cp - 1) / cp);
+    const long long grid = items < num_sms ? items : num_sms;
+    const long long cost = ((items + grid - 1) / grid) * (rounds(static_cast<long long>(cp) * tpp) + 1);
+    if (cost <= cost_c) {        // ties go to the larger chunk (fewer partials)
+      cost_c = cost;
+      best_cp = cp;
+    }
+  }
+  if (best_cp > 0 && cost_c < cost_b) {
+    p.chunk_pages = best_cp;
+    p.max_chunks = (max_pages + best_cp - 1) / best_cp;
+    const long long items = pairs * p.max_chunks;
+    p.grid = static_cast<int>(items < num_sms ? items : num_sms);
+  } else {
+    p.grid = grid_b;
+    // The kernel gives each CTA max(ceil(total / grid), min_range_pages) pages; a floor keeps the
+    // number of partials per pair, and so the workspace, bounded when requests are short.
+    p.min_range_pages = static_cast<int>(balanced / kMinRangeDivisor > 1 ? balanced / kMinRangeDivisor : 1);
+    // A pair of n pages meets at most ceil(n / W) + 1 CTA ranges and is cut every pmax pages in
+    // each, so it has at most floor(n / pmax) + ceil(n / W) + 1 partials.
+    p.max_chunks = max_pages / pmax + (max_pages + p.min_range_pages - 1) / p.min_range_pages + 1;
+  }
+  // Short calls (a few rounds of tiles per CTA) are dominated by their start-up; they plan and
+  // prefetch their first tiles while the preceding grid drains.  Long calls skip it (when nothing
+  // precedes them it would only delay their start), and so do the shortest.
+  p.prefetch = balanced * tpp >= kPrefetchMinTilesPerCta && balanced * tpp <= kPrefetchMaxTilesPerCta;
   const size_t n = static_cast<size_t>(batch) * hq * p.max_chunks;
   p.part_o_bytes = n * ZF_HEAD_DIM * 4;
   p.part_lse_bytes = (n * 4 + 255) & ~static_cast<size_t>(255);
   p.ws_bytes = p.part_o_bytes + p.part_lse_bytes + ((static_cast<size_t>(pairs) * 4 + 255) & ~static_cast<size_t>(255));
   return p;
+}
+
+// Workspace that serves both attention variants (the larger of their plans).
+static size_t plan_workspace(int batch, int hq, int hkv, int page_size, int max_pages, int num_sms) {
+  const size_t c = make_plan(batch, hq, hkv, page_size, max_pages, num_sms, Cfg<true>::kWarps).ws_bytes;
+  const size_t d = make_plan(batch, hq, hkv, page_size, max_pages, num_sms, Cfg<false>::kWarps).ws_bytes;
+  return c > d ? c : d;
 }
 
 // Raise a kernel's dynamic shared-memory limit once per (device, kernel); the limit only grows.
@@ -810,7 +1010,7 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   if (c->num_pages >= (1 << 26) || c->num_raw_slots >= (1 << 26)) return ZF_ERR_UNSUPPORTED;
   int sms = 0;
   if ((st = current_sm_count(&sms)) != ZF_OK) return st;
-  const Plan p = make_plan(batch, hq, c->num_kv_heads, c->page_size, max_pages, sms);
+  const Plan p = make_plan(batch, hq, c->num_kv_heads, c->page_size, max_pages, sms, Cfg<kCompressed>::kWarps);
   if (ws_bytes < p.ws_bytes) return ZF_ERR_WORKSPACE_TOO_SMALL;
 
   AttnArgs a{};
@@ -839,6 +1039,8 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   a.max_pages = max_pages;
   a.max_chunks = p.max_chunks;
   a.min_range_pages = p.min_range_pages;
+  a.chunk_pages = p.chunk_pages;
+  a.prefetch = p.prefetch ? 1 : 0;
   a.comp_head_bytes = static_cast<int64_t>(c->page_size / 4) * kSlotBytes;
   a.raw_head_bytes = static_cast<int64_t>(c->page_size / 4) * kRawBlockBytes;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -875,8 +1077,8 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   m.max_chunks = p.max_chunks;
   const int rows = batch * hq;
   cudaLaunchConfig_t mcfg = cfg;
-  mcfg.gridDim = dim3((rows + 3) / 4);
-  mcfg.blockDim = dim3(128);
+  mcfg.gridDim = dim3((rows + kMergeWarps - 1) / kMergeWarps);
+  mcfg.blockDim = dim3(kMergeWarps * 32);
   mcfg.dynamicSmemBytes = 0;
   if (cudaLaunchKernelEx(&mcfg, merge_kernel, m) != cudaSuccess) return ZF_ERR_CUDA;
   return ZF_OK;
@@ -892,8 +1094,8 @@ extern "C" size_t zf_decode_attn_workspace_size(int32_t batch, int32_t num_q_hea
   if (page_size < ZF_BLOCK_TOKENS || page_size % ZF_BLOCK_TOKENS || page_size > ZF_MAX_PAGE_SIZE) return 0;
   int sms = 0;
   if (current_sm_count(&sms) != ZF_OK) return 0;
-  const Plan p = make_plan(batch, num_q_heads, num_kv_heads, page_size, max_pages_per_req, sms);
-  return p.ws_bytes > 0 ? p.ws_bytes : 256;
+  const size_t ws = plan_workspace(batch, num_q_heads, num_kv_heads, page_size, max_pages_per_req, sms);
+  return ws > 0 ? ws : 256;
 }
 
 extern "C" zf_status zf_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch, int32_t num_q_heads,
@@ -951,7 +1153,7 @@ extern "C" zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t
   int sms = 0;
   zf_status st = current_sm_count(&sms);
   if (st != ZF_OK) return st;
-  const Plan p = make_plan(batch, num_q_heads, cache->num_kv_heads, P, max_pages_per_req, sms);
+  const Plan p = make_plan(batch, num_q_heads, cache->num_kv_heads, P, max_pages_per_req, sms, Cfg<true>::kWarps);
   if (p.ws_bytes > ZF_STATIC_WORKSPACE_BYTES) return ZF_ERR_STATIC_WORKSPACE_EXCEEDED;
   void* ws = nullptr;
   if ((st = static_workspace_address(&ws)) != ZF_OK) return st;

@@ -15,9 +15,6 @@ constexpr int kRawBlockBytes = ZF_RAW_BLOCK_BYTES;
 constexpr int kHeaderAt = 768;
 constexpr int kEscapesAt = 772;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // a pipeline wait gives up after 2 s
-// try_wait may suspend the thread up to this long (it resumes as soon as the phase completes),
-// so waiting warps do not spend issue slots polling.
-constexpr uint32_t kSuspendHintNs = 200000u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -48,14 +45,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// try_wait blocks for a system-dependent time before it returns false, so a waiting warp spends
+// few issue slots polling.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return done != 0;
 }
@@ -81,6 +80,24 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
   return policy;
+}
+
+// Hint: bring the 128-byte line holding `p` into L2 (no value is read; safe on any valid address).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Hint: bring `bytes` (a multiple of 16, `src` 16-byte aligned) starting at `src` into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Relaxed (atomic, unordered) 32-bit load: a well-defined read of a value another grid may be
+// writing at the same time.
+__device__ __forceinline__ int ld_relaxed(const int32_t* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // 1-D bulk copy global -> shared, completion signalled on `bar` as transaction bytes.
@@ -116,6 +133,13 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// log2(x) with the hardware approximation (PTX lg2.approx.ftz.f32).
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -183,7 +207,7 @@ __device__ __forceinline__ void rebuild_lane(const uint8_t* slot, int lane, uint
   const uint32_t header = *reinterpret_cast<const uint32_t*>(slot + kHeaderAt);
   const uint4 lo = *reinterpret_cast<const uint4*>(slot + 16 * lane);
   const uint2 code = *reinterpret_cast<const uint2*>(slot + 512 + 8 * lane);
-  const uint32_t base4 = (header & 0x7Fu) * 0x01010101u;
+  const uint32_t base4 = __byte_perm(header, 0u, 0x0000u);   // header byte 0 = base/2 (bit 7 clear)
   rebuild8(lo.x, lo.y, code.x, base4, &a[0]);
   rebuild8(lo.z, lo.w, code.y, base4, &a[4]);
   const uint32_t n_esc = (header >> 8) & 7u;

@@ -35,6 +35,7 @@ struct CodecArgs {
   const int32_t* n_valid;
   const int32_t* raw_slots;
   int32_t num_pages, hkv, page_size, num_raw, flags;
+  int32_t raw_out;         // decompress: 1 = write the raw block layout of a dense cache
 };
 
 // Natural-layout address of this lane's 16 values of block (tile, group): token tau = lane/2,
@@ -237,6 +238,13 @@ __global__ void __launch_bounds__(kCodecThreads) decompress_kernel(CodecArgs a) 
                              (static_cast<size_t>(slot) * a.hkv + h) * nblk * 512 + static_cast<size_t>(bi) * 512;
       load_raw_lane(reinterpret_cast<const uint8_t*>(base), lane, v);
     }
+    if (a.raw_out) {                     // raw block layout: the inverse of load_raw_lane
+      uint8_t* blk = reinterpret_cast<uint8_t*>(is_value ? a.dst_v : a.dst_k) +
+                     ((static_cast<size_t>(i) * a.hkv + h) * nblk + bi) * kRawBlockBytes;
+      *reinterpret_cast<uint4*>(blk + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<uint4*>(blk + 512 + 16 * lane) = make_uint4(v[4], v[5], v[6], v[7]);
+      continue;
+    }
     uint16_t* st = stage[warp];
     *reinterpret_cast<uint4*>(st + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
     *reinterpret_cast<uint4*>(st + 16 * lane + 8) = make_uint4(v[4], v[5], v[6], v[7]);
@@ -291,8 +299,8 @@ extern "C" zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_
   return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
 }
 
-extern "C" zf_status zf_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n, uint16_t* dst_k,
-                                   uint16_t* dst_v, void* stream) {
+static zf_status launch_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n, uint16_t* dst_k,
+                                   uint16_t* dst_v, int raw_out, void* stream) {
   zf_status st = check_cache(cache, /*need_comp=*/false, /*need_raw=*/false, /*need_dir=*/true);
   if (st != ZF_OK) return st;
   if (n < 0) return ZF_ERR_INVALID_ARGUMENT;
@@ -305,6 +313,17 @@ extern "C" zf_status zf_decompress(const zf_cache* cache, const int32_t* page_id
   a.dst_k = dst_k; a.dst_v = dst_v; a.page_ids = page_ids;
   a.num_pages = cache->num_pages; a.hkv = cache->num_kv_heads; a.page_size = cache->page_size;
   a.num_raw = cache->num_raw_slots;
+  a.raw_out = raw_out;
   decompress_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
+}
+
+extern "C" zf_status zf_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n, uint16_t* dst_k,
+                                   uint16_t* dst_v, void* stream) {
+  return launch_decompress(cache, page_ids, n, dst_k, dst_v, 0, stream);
+}
+
+extern "C" zf_status zf_decompress_to_raw(const zf_cache* cache, const int32_t* page_ids, int32_t n,
+                                          uint16_t* dst_k_raw, uint16_t* dst_v_raw, void* stream) {
+  return launch_decompress(cache, page_ids, n, dst_k_raw, dst_v_raw, 1, stream);
 }

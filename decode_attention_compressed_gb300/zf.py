@@ -42,6 +42,8 @@ SIGNATURES = {
     "zf_encode_pages": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                    _c_void_p, _c_int32, _c_int32, _c_void_p]),
     "zf_decompress": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p, _c_void_p]),
+    "zf_decompress_to_raw": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p,
+                                        _c_void_p]),
     "zf_decode_attn_workspace_size": (_c_size_t, [_c_int32, _c_int32, _c_int32, _c_int32, _c_int32]),
     "zf_decode_attn": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_void_p, _c_int32,
                                   _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
@@ -166,6 +168,21 @@ def decompress(cache: Cache, page_ids, stream=None):
     d = cache.desc()
     _check("zf_decompress", lib().zf_decompress(ctypes.byref(d), _ptr(ids), n, _ptr(k), _ptr(v), _stream(stream)))
     return k, v
+
+
+def decompress_to_raw(cache: Cache, page_ids, dense: Cache, stream=None):
+    """zf_decompress_to_raw: page_ids[i] of `cache` into raw slot i of the dense cache `dense`
+    (same kv heads and page size, at least len(page_ids) raw slots).  Returns the id tensor (keep it
+    alive until the stream has consumed it)."""
+    dev = cache.device
+    ids = _dev_i32(page_ids, dev)
+    n = int(ids.numel())
+    if dense.num_kv_heads != cache.num_kv_heads or dense.page_size != cache.page_size or dense.num_raw_slots < n:
+        raise ValueError("the dense cache must match the kv heads and page size and hold n raw slots")
+    d = cache.desc()
+    _check("zf_decompress_to_raw", lib().zf_decompress_to_raw(ctypes.byref(d), _ptr(ids), n, _ptr(dense.k_raw),
+                                                               _ptr(dense.v_raw), _stream(stream)))
+    return ids
 
 
 def workspace_size(batch, num_q_heads, num_kv_heads, page_size, max_pages) -> int:

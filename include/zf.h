@@ -137,6 +137,19 @@ zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_k, const ui
 zf_status zf_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n,
                         uint16_t* dst_k, uint16_t* dst_v, void* stream);
 
+/*
+ * zf_decompress_to_raw — zf_decompress into the raw block layout of a dense cache: page_ids[i] is
+ * written to raw slot i of dst_k_raw / dst_v_raw ([n][num_kv_heads][page_size/4][512] BF16, the
+ * layout of zf_cache.k_raw / v_raw), so zf_dense_decode_attn can attend over the result directly.
+ * This is the restore-then-attend pattern that ZipFusion §II.B (Compression for Faster Decode
+ * Attention) measures: each layer is restored into a shared buffer before a dense attention
+ * kernel reads it.  It is kept as a measured baseline for the fused path.  The bytes written equal
+ * those zf_encode_pages with ZF_ENCODE_FORCE_RAW writes for the same source pages.  Same argument
+ * checks and device error reporting as zf_decompress.
+ */
+zf_status zf_decompress_to_raw(const zf_cache* cache, const int32_t* page_ids, int32_t n,
+                               uint16_t* dst_k_raw, uint16_t* dst_v_raw, void* stream);
+
 /* Workspace bytes zf_decode_attn / zf_dense_decode_attn need for these sizes on the current
  * device (split-KV partial outputs and log-sum-exps).  0 on invalid sizes. */
 size_t zf_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,

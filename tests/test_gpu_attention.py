@@ -39,6 +39,10 @@ CASES = {
     "page64_gqa4": (W(2, 16, 4, 64, 700, pool="random", seed=9), [700, 129]),
     "empty_requests": (W(4, 8, 2, 16, 40, seed=10), [0, 40, 0, 3]),
     "long_chunked": (W(1, 8, 1, 16, 3000, seed=11), [3000]),
+    # more (request, kv head) pairs than SMs: the planner takes balanced page ranges, so ranges
+    # cross request boundaries and skip empty requests
+    "balanced_ragged": (W(40, 8, 4, 16, 1024, pool="random", seed=12),
+                        [0 if i in (3, 17) else 1024 if i == 5 else (37 * i * i + 11 * i) % 1025 for i in range(40)]),
 }
 
 

@@ -140,3 +140,27 @@ def test_decompress_of_invalid_entries(zf):
     torch.cuda.synchronize()
     assert (k == 0).all() and (v == 0).all()
     assert gc.status_word() == (zf.DEV_BAD_DIR | zf.DEV_BAD_PAGE_ID)
+
+
+@pytest.mark.parametrize("name", ["qwen2_7b_maxbatch", "long_ctx"])
+def test_decompress_to_raw_matches_a_raw_encode_and_attends(zf, name):
+    """Restore-then-attend baseline: pages decompressed into a dense cache's raw layout are the
+    bytes a force-raw encode of the source writes, and dense attention over them matches the
+    oracle."""
+    layer = I.make_layer(SMALL[name])
+    gc = H.gpu_cache_from(layer, zf)
+    n = layer.num_pages
+    dense = zf.Cache(n, gc.num_kv_heads, gc.page_size, n, compressed=False)
+    zf.decompress_to_raw(gc, list(range(n)), dense)
+    want = H.gpu_cache_from(layer, zf, force_raw=True)
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    assert torch.equal(dense.k_raw, want.k_raw[:n]) and torch.equal(dense.v_raw, want.v_raw[:n])
+    dev = torch.device("cuda")
+    out, lse = zf.dense_decode_attn(dense, layer.q.to(dev), layer.page_table.to(dev), layer.seq_lens.to(dev),
+                                    layer.scale)
+    torch.cuda.synchronize()
+    oc = H.oracle_cache_from(layer, O)
+    ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q), oc, layer.page_table.numpy(), layer.seq_lens.numpy(),
+                                          layer.scale)
+    H.compare_attention(out, lse, ref_out, ref_lse)

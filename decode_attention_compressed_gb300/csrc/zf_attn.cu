@@ -644,17 +644,37 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         const bool comp = kCompressed && kind == kKindComp;
         const int ntok = min(16, d.t1 - (d.t0 + 16 * u));
 
-        // ---- S^T (16 tokens x 8 heads) = K (16 x 128) . Q^T (128 x 8); two accumulation chains
+        // ---- S^T (16 tokens x 8 heads) = K (16 x 128) . Q^T (128 x 8); two accumulation chains.
+        // The common case (compressed, no escape in the four K blocks) runs a branch-free loop.
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t hdr[4] = {0u, 0u, 0u, 0u};
+        bool fast = false;
+        if (comp) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t ka[8];
-          if (comp) rebuild_lane(kp + j * kSlotBytes, lane, ka);
-          else load_raw_lane(kp + j * kRawBlockBytes, lane, ka);
-          const uint4 q = *reinterpret_cast<const uint4*>(qrow + 64 * j);
-          float(&acc)[4] = (j & 1) ? sb : sa;
-          mma_bf16(acc, ka[0], ka[1], ka[2], ka[3], q.x, q.y);
-          mma_bf16(acc, ka[4], ka[5], ka[6], ka[7], q.z, q.w);
+          for (int j = 0; j < 4; ++j) hdr[j] = *reinterpret_cast<const uint32_t*>(kp + j * kSlotBytes + kHeaderAt);
+          fast = ((hdr[0] | hdr[1] | hdr[2] | hdr[3]) & kHeaderEscMask) == 0;
+        }
+        if (fast) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t ka[8];
+            rebuild_lane_noesc(kp + j * kSlotBytes, lane, __byte_perm(hdr[j], 0u, 0x0000u), ka);
+            const uint4 q = *reinterpret_cast<const uint4*>(qrow + 64 * j);
+            float(&acc)[4] = (j & 1) ? sb : sa;
+            mma_bf16(acc, ka[0], ka[1], ka[2], ka[3], q.x, q.y);
+            mma_bf16(acc, ka[4], ka[5], ka[6], ka[7], q.z, q.w);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t ka[8];
+            if (comp) rebuild_lane(kp + j * kSlotBytes, lane, ka);
+            else load_raw_lane(kp + j * kRawBlockBytes, lane, ka);
+            const uint4 q = *reinterpret_cast<const uint4*>(qrow + 64 * j);
+            float(&acc)[4] = (j & 1) ? sb : sa;
+            mma_bf16(acc, ka[0], ka[1], ka[2], ka[3], q.x, q.y);
+            mma_bf16(acc, ka[4], ka[5], ka[6], ka[7], q.z, q.w);
+          }
         }
         const uint8_t* vp = kp + C::kVOffset;
         if (kCompressed && !comp) {      // raw tile in the compressed kernel: V goes where K was
@@ -716,20 +736,39 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         const uint32_t bh0 = transpose8x8(h01), bh1 = transpose8x8(h23);
         const uint32_t bl0 = transpose8x8(r01), bl1 = transpose8x8(r23);
 
-        // ---- O^T (128 channels x 8 heads) += V^T (128 x 16 tokens) . P^T (16 x 8)
+        // ---- O^T (128 channels x 8 heads) += V^T (128 x 16 tokens) . P^T (16 x 8).  Branch-free
+        // loop for a full compressed tile without escapes in its V blocks.
+        fast = false;
+        if (comp && ntok == 16) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t va[8];
-          if (comp) rebuild_lane(vp + j * kSlotBytes, lane, va);
-          else load_raw_lane(vp + j * kRawBlockBytes, lane, va);
-          if (ntok < 16) {         // the context's last tile only
-            va[0] &= keep_a; va[1] &= keep_a; va[4] &= keep_a; va[5] &= keep_a;
-            va[2] &= keep_b; va[3] &= keep_b; va[6] &= keep_b; va[7] &= keep_b;
+          for (int j = 0; j < 4; ++j) hdr[j] = *reinterpret_cast<const uint32_t*>(vp + j * kSlotBytes + kHeaderAt);
+          fast = ((hdr[0] | hdr[1] | hdr[2] | hdr[3]) & kHeaderEscMask) == 0;
+        }
+        if (fast) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t va[8];
+            rebuild_lane_noesc(vp + j * kSlotBytes, lane, __byte_perm(hdr[j], 0u, 0x0000u), va);
+            mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bh0, bh1);
+            mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bh0, bh1);
+            mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bl0, bl1);
+            mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bl0, bl1);
           }
-          mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bh0, bh1);
-          mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bh0, bh1);
-          mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bl0, bl1);
-          mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bl0, bl1);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t va[8];
+            if (comp) rebuild_lane(vp + j * kSlotBytes, lane, va);
+            else load_raw_lane(vp + j * kRawBlockBytes, lane, va);
+            if (ntok < 16) {         // the context's last tile only
+              va[0] &= keep_a; va[1] &= keep_a; va[4] &= keep_a; va[5] &= keep_a;
+              va[2] &= keep_b; va[3] &= keep_b; va[6] &= keep_b; va[7] &= keep_b;
+            }
+            mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bh0, bh1);
+            mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bh0, bh1);
+            mma_bf16(o[2 * j], va[0], va[1], va[2], va[3], bl0, bl1);
+            mma_bf16(o[2 * j + 1], va[4], va[5], va[6], va[7], bl0, bl1);
+          }
         }
       }
       __syncwarp();                // the stage may now be refilled

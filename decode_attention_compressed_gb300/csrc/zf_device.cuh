@@ -14,6 +14,7 @@ constexpr int kSlotBytes = ZF_SLOT_BYTES;        // 784
 constexpr int kRawBlockBytes = ZF_RAW_BLOCK_BYTES;
 constexpr int kHeaderAt = 768;
 constexpr int kEscapesAt = 772;
+constexpr uint32_t kHeaderEscMask = 0x700u;    // header bits 8-10: number of escapes
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // a pipeline wait gives up after 2 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -173,11 +174,10 @@ __host__ __device__ __forceinline__ int block_position(bool is_value, int tau, i
 // crossing a byte.  Output: four BF16 pairs, value 2i in the low half of out[i].
 __device__ __forceinline__ void rebuild8(uint32_t lo0, uint32_t lo1, uint32_t code, uint32_t base4,
                                          uint32_t* out) {
-  const uint32_t n0 = code & 0x0F0F0F0Fu;            // codes of values 0..3, one per byte
-  const uint32_t n1 = (code >> 4) & 0x0F0F0F0Fu;     // codes of values 4..7
-  // n * 0x11 copies each nibble into both halves of its byte; keep bit 7 (sign) and bits 0-2.
-  const uint32_t h0 = ((n0 * 0x11u) & 0x87878787u) + base4;
-  const uint32_t h1 = ((n1 * 0x11u) & 0x87878787u) + base4;
+  // values 0..3 (low nibbles): offset in bits 0-2 stays, sign bit 3 moves to bit 7;
+  // values 4..7 (high nibbles): offset in bits 4-6 moves to bits 0-2, sign bit 7 stays.
+  const uint32_t h0 = base4 + (code & 0x07070707u) + ((code & 0x08080808u) << 4);
+  const uint32_t h1 = base4 + ((code >> 4) & 0x07070707u) + (code & 0x80808080u);
   out[0] = __byte_perm(lo0, h0, 0x5140);
   out[1] = __byte_perm(lo0, h0, 0x7362);
   out[2] = __byte_perm(lo1, h1, 0x5140);
@@ -199,6 +199,16 @@ __device__ __forceinline__ void patch_escapes(const uint8_t* slot, uint32_t n_es
         if ((idx >> 1) == static_cast<uint32_t>(i)) a[i] = (a[i] & ~mask) | val;
     }
   }
+}
+
+// This lane's 16 values of a compressed block that has no escapes; base4 = header byte 0 (base/2)
+// in every byte.
+__device__ __forceinline__ void rebuild_lane_noesc(const uint8_t* slot, int lane, uint32_t base4,
+                                                   uint32_t (&a)[8]) {
+  const uint4 lo = *reinterpret_cast<const uint4*>(slot + 16 * lane);
+  const uint2 code = *reinterpret_cast<const uint2*>(slot + 512 + 8 * lane);
+  rebuild8(lo.x, lo.y, code.x, base4, &a[0]);
+  rebuild8(lo.z, lo.w, code.y, base4, &a[4]);
 }
 
 // This lane's 16 values (storage positions 16*lane..16*lane+15) of a compressed block in

@@ -167,36 +167,50 @@ __host__ __device__ __forceinline__ int block_position(bool is_value, int tau, i
 }
 
 // ------------------------------------------------------------------------- in-register rebuild
-// Eight values from 8 low bytes (lo0: values 0-3, lo1: values 4-7) and one code word
-// (byte k = code k | code k+4 << 4).  A code is sign << 3 | exponent offset; the high byte of a
-// value is sign << 7 | (base/2 + offset).  `base4` holds base/2 in every byte: base/2 + offset
-// is the 7-bit exponent>>1 field, so one 32-bit add fills four high bytes without any carry
-// crossing a byte.  Output: four BF16 pairs, value 2i in the low half of out[i].
-__device__ __forceinline__ void rebuild8(uint32_t lo0, uint32_t lo1, uint32_t code, uint32_t base4,
-                                         uint32_t* out) {
-  // values 0..3 (low nibbles): offset in bits 0-2 stays, sign bit 3 moves to bit 7;
-  // values 4..7 (high nibbles): offset in bits 4-6 moves to bits 0-2, sign bit 7 stays.
-  const uint32_t h0 = base4 + (code & 0x07070707u) + ((code & 0x08080808u) << 4);
-  const uint32_t h1 = base4 + ((code >> 4) & 0x07070707u) + (code & 0x80808080u);
-  out[0] = __byte_perm(lo0, h0, 0x5140);
-  out[1] = __byte_perm(lo0, h0, 0x7362);
-  out[2] = __byte_perm(lo1, h1, 0x5140);
-  out[3] = __byte_perm(lo1, h1, 0x7362);
+// High bytes of a lane's 16 values from its two code words (byte k of a word = code k | code k+4
+// << 4).  A code is sign << 3 | exponent offset; the high byte of a value is sign << 7 |
+// (base/2 + offset).  `base4` holds base/2 in every byte: base/2 + offset is the 7-bit exponent>>1
+// field, so one 32-bit add fills four high bytes without any carry crossing a byte.
+// Output: word w holds the high bytes of values 4w..4w+3, one per byte.
+__device__ __forceinline__ void high_bytes(uint2 code, uint32_t base4, uint32_t (&h)[4]) {
+  // values 0..3 of a word (low nibbles): offset bits 0-2 stay, sign bit 3 moves to bit 7;
+  // values 4..7 (high nibbles): offset bits 4-6 move to bits 0-2, sign bit 7 stays.
+  h[0] = base4 + (code.x & 0x07070707u) + ((code.x & 0x08080808u) << 4);
+  h[1] = base4 + ((code.x >> 4) & 0x07070707u) + (code.x & 0x80808080u);
+  h[2] = base4 + (code.y & 0x07070707u) + ((code.y & 0x08080808u) << 4);
+  h[3] = base4 + ((code.y >> 4) & 0x07070707u) + (code.y & 0x80808080u);
 }
 
-// Replace the exponent>>1 field of escaped values owned by this lane (positions 16*lane..+15).
-__device__ __forceinline__ void patch_escapes(const uint8_t* slot, uint32_t n_esc, int lane, uint32_t (&a)[8]) {
+// Interleave low and high bytes into four BF16 pairs per 8 values: value 2i in the low half of
+// a[i].
+__device__ __forceinline__ void interleave(uint4 lo, const uint32_t (&h)[4], uint32_t (&a)[8]) {
+  a[0] = __byte_perm(lo.x, h[0], 0x5140);
+  a[1] = __byte_perm(lo.x, h[0], 0x7362);
+  a[2] = __byte_perm(lo.y, h[1], 0x5140);
+  a[3] = __byte_perm(lo.y, h[1], 0x7362);
+  a[4] = __byte_perm(lo.z, h[2], 0x5140);
+  a[5] = __byte_perm(lo.z, h[2], 0x7362);
+  a[6] = __byte_perm(lo.w, h[3], 0x5140);
+  a[7] = __byte_perm(lo.w, h[3], 0x7362);
+}
+
+// Replace the exponent>>1 field of the escaped values this lane owns (positions 16*lane..+15).
+// `tail` is the block's last 16 bytes: the header word, then the six escape entries
+// (position << 7 | exponent >> 1).  Entry position p is value p & 15 of lane p >> 4, whose high
+// byte is byte p & 3 of h[(p >> 2) & 3].
+__device__ __forceinline__ void patch_escapes(uint4 tail, uint32_t n_esc, int lane, uint32_t (&h)[4]) {
   for (uint32_t e = 0; e < n_esc; ++e) {
-    const uint32_t entry = *reinterpret_cast<const uint16_t*>(slot + kEscapesAt + 2 * e);
+    const uint32_t pair = e < 2 ? tail.y : (e < 4 ? tail.z : tail.w);
+    const uint32_t entry = (e & 1u) ? pair >> 16 : pair & 0xFFFFu;
     const uint32_t p = entry >> 7;
-    if ((p >> 4) == static_cast<uint32_t>(lane)) {
-      const uint32_t idx = p & 15u;
-      const uint32_t shift = (idx & 1u) ? 24u : 8u;
-      const uint32_t mask = 0x7Fu << shift;
-      const uint32_t val = (entry & 0x7Fu) << shift;
+    // branch-free: lanes that do not own the value apply an empty mask
+    const uint32_t sh = (p & 3u) * 8u, w = (p >> 2) & 3u;
+    const uint32_t mask = (p >> 4) == static_cast<uint32_t>(lane) ? 0x7Fu << sh : 0u;
+    const uint32_t val = ((entry & 0x7Fu) << sh) & mask;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if ((idx >> 1) == static_cast<uint32_t>(i)) a[i] = (a[i] & ~mask) | val;
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t mi = w == static_cast<uint32_t>(i) ? mask : 0u;
+      h[i] = (h[i] & ~mi) | (val & mi);
     }
   }
 }
@@ -207,21 +221,23 @@ __device__ __forceinline__ void rebuild_lane_noesc(const uint8_t* slot, int lane
                                                    uint32_t (&a)[8]) {
   const uint4 lo = *reinterpret_cast<const uint4*>(slot + 16 * lane);
   const uint2 code = *reinterpret_cast<const uint2*>(slot + 512 + 8 * lane);
-  rebuild8(lo.x, lo.y, code.x, base4, &a[0]);
-  rebuild8(lo.z, lo.w, code.y, base4, &a[4]);
+  uint32_t h[4];
+  high_bytes(code, base4, h);
+  interleave(lo, h, a);
 }
 
 // This lane's 16 values (storage positions 16*lane..16*lane+15) of a compressed block in
-// shared or global memory.
+// shared or global memory.  The header and the escape entries come in one 16-byte load.
 __device__ __forceinline__ void rebuild_lane(const uint8_t* slot, int lane, uint32_t (&a)[8]) {
-  const uint32_t header = *reinterpret_cast<const uint32_t*>(slot + kHeaderAt);
+  const uint4 tail = *reinterpret_cast<const uint4*>(slot + kHeaderAt);
   const uint4 lo = *reinterpret_cast<const uint4*>(slot + 16 * lane);
   const uint2 code = *reinterpret_cast<const uint2*>(slot + 512 + 8 * lane);
-  const uint32_t base4 = __byte_perm(header, 0u, 0x0000u);   // header byte 0 = base/2 (bit 7 clear)
-  rebuild8(lo.x, lo.y, code.x, base4, &a[0]);
-  rebuild8(lo.z, lo.w, code.y, base4, &a[4]);
-  const uint32_t n_esc = (header >> 8) & 7u;
-  if (n_esc) patch_escapes(slot, n_esc, lane, a);
+  const uint32_t base4 = __byte_perm(tail.x, 0u, 0x0000u);   // header byte 0 = base/2 (bit 7 clear)
+  uint32_t h[4];
+  high_bytes(code, base4, h);
+  const uint32_t n_esc = (tail.x >> 8) & 7u;
+  if (n_esc) patch_escapes(tail, n_esc, lane, h);
+  interleave(lo, h, a);
 }
 
 // This lane's 16 values of a raw block.  Raw blocks are half-major (position 256*half + 8*lane + r

@@ -68,30 +68,74 @@ def read_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples taken while the timed region runs."""
+    """SM clock and clock-event reasons sampled while the timed region runs: NVML (read-only
+    queries through ctypes, about one sample per millisecond from a thread), else nvidia-smi."""
 
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
+        self.rows = []            # (sm_mhz, max_mhz, [reason names])
+        self.nvml = None
         self.proc = None
         self.path = None
 
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            return None
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) != 0:
+            return None
+        return lib, h, mx.value
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, h, mx = self.nvml
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(1), ctypes.byref(clk)) == 0:
+                names = []
+                if lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                    names = [n for bit, n in self.REASONS.items() if rs.value & bit]
+                self.rows.append((float(clk.value), float(mx), names))
+            time.sleep(0.001)
+
     def __enter__(self):
+        try:
+            self.nvml = self._nvml_open()
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.thread.start()
+            return self
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self.nvml is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -101,23 +145,27 @@ class ClockSampler:
             self.fh.close()
 
     def summary(self):
-        if self.proc is None or not self.path:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        rows = []
-        for line in open(self.path):
-            w = [x.strip() for x in line.split(",")]
-            if len(w) >= 9:
-                try:
-                    rows.append((float(w[1]), float(w[2]), w[5], w[6], w[7], w[8]))
-                except ValueError:
-                    pass
-        os.unlink(self.path)
+        rows = list(self.rows)
+        source = "nvml"
+        if self.nvml is None:
+            source = "nvidia-smi"
+            if self.proc is None or not self.path:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+            names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+            for line in open(self.path):
+                w = [x.strip() for x in line.split(",")]
+                if len(w) >= 9:
+                    try:
+                        rows.append((float(w[1]), float(w[2]),
+                                     [n for n, v in zip(names, w[5:9]) if v.lower().startswith("active")]))
+                    except ValueError:
+                        pass
+            os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({n for r in rows for n, v in zip(names, r[2:]) if v.lower().startswith("active")})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0, "source": source}
+        reasons = sorted({n for r in rows for n in r[2]})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": source}
 
 
 # ------------------------------------------------------------------------------------ GPU arm

@@ -43,6 +43,13 @@ CASES = {
     # cross request boundaries and skip empty requests
     "balanced_ragged": (W(40, 8, 4, 16, 1024, pool="random", seed=12),
                         [0 if i in (3, 17) else 1024 if i == 5 else (37 * i * i + 11 * i) % 1025 for i in range(40)]),
+    # GQA 16 (two 8-head slices per kv head) with balanced ranges
+    "balanced_two_slices": (W(48, 32, 2, 16, 1024, pool="random", seed=16),
+                            [0 if i % 11 == 4 else (53 * i * i + 7 * i + 1) % 1025 for i in range(48)]),
+    # other page sizes: 2, 3 and 8 tiles per page (items cut at 128, 85 and 32 pages)
+    "page32_ragged": (W(5, 8, 2, 32, 900, pool="random", seed=13), [900, 0, 33, 511, 64]),
+    "page48_gqa2": (W(3, 4, 2, 48, 500, pool="random", seed=14), [500, 47, 49]),
+    "page128_gqa16": (W(2, 32, 2, 128, 1000, pool="random", seed=15), [1000, 129]),
 }
 
 

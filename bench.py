@@ -45,11 +45,18 @@ def read_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources with comments and blank space removed: a committed ncu capture
+    stays valid across comment-only edits and is dropped when any code changes."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_compressed_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(f.encode() + text.encode())
     return h.hexdigest()[:16]
 
 

@@ -8,11 +8,12 @@
 // split-KV partial results are combined by a split-result merge.
 //
 // Design for sm_103a (one CTA per SM, persistent):
-//  * work is balanced by pages, not by items: the pages of all (request b, kv head g, head slice)
-//    pairs, laid end to end, are cut into one equal contiguous range per CTA, so a ragged batch
-//    gives every SM the same number of tiles.  Where a range meets a pair it forms that pair's
-//    chunk(s), cut further into items of at most 256 tiles; each item yields one partial;
-//  * the last warp is the metadata warp: it walks the CTA's range, and runs one item ahead,
+//  * work split (host planner, from the sizes): either balanced page ranges — the pages of all
+//    (request b, kv head g, head slice) pairs, laid end to end, cut into one equal contiguous range
+//    per CTA, so a ragged batch gives every SM the same number of tiles; where a range meets a
+//    pair it forms that pair's partial(s), cut further into items of at most 256 tiles — or, for
+//    short contexts, fixed chunks of pages dealt round-robin; each item yields one partial;
+//  * the last warp is the metadata warp: it walks the CTA's items, and runs one item ahead,
 //    resolving the item's page ids through the page table and the directory into shared memory
 //    and staging the item's q rows; an end marker closes the CTA's item stream;
 //  * the consumer warps each stream their own 16-token tiles (tile u of an item goes to warp
@@ -28,8 +29,10 @@
 //    movmatrix, and accumulates O^T = V^T P^T with P split into a BF16 high part and a BF16
 //    remainder (two MMAs) so P keeps ~16 significant bits; V blocks are rebuilt right before use;
 //  * at the end of an item the warps' (m, l, O) are merged through shared memory and written as
-//    the item's partial (or as the final output when the request has a single chunk);
-//  * a second kernel merges each (request, head)'s chunk partials by log-sum-exp.
+//    the item's partial (or as the final output when the pair has a single partial);
+//  * a second kernel merges each (request, head)'s partials by log-sum-exp;
+//  * consecutive calls overlap: the merge kernel lets the next grid launch at once, and that grid
+//    warms L2 (and, for short calls, prefetches its first tiles) while it waits for this one.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>

@@ -62,7 +62,8 @@ constexpr int kWarpStages = 2;
 constexpr int kTileCompBytes = 4 * kSlotBytes;      // 3136: one 16-token tile of K (or V), compressed
 constexpr int kTileRawBytes = 4 * kRawBlockBytes;   // 4096
 constexpr int kHeadsPerSlice = 8;                   // MMA n
-constexpr int kMaxItemTiles = 256;                  // 16-token tiles per work item (metadata buffer size)
+constexpr int kMaxItemTiles = 512;                  // 16-token tiles per work item (metadata buffer size)
+constexpr int kMaxItemPages = 256;                  // pages per work item (page-table loads per lane: /32)
 // q rows in shared memory: channel words permuted so that lane (gi, ti) finds the four B-fragment
 // words of k-steps 2j and 2j+1 (words 16j + ti + {0, 4, 8, 12}) in one 16-byte read at word
 // 16j + 4ti; rows padded to 320 bytes so the eight rows of a warp's reads hit distinct banks.
@@ -210,7 +211,7 @@ __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int
 // kSpec: relaxed loads of values that may still change, and no error reports (prefetch planning).
 template <bool kCompressed, bool kSpec = false>
 __device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc& d, int* meta, int lane) {
-  constexpr int kPer = kMaxItemTiles / 32;
+  constexpr int kPer = kMaxItemPages / 32;
   const int tpp = a.page_size >> 4;
   const int npg = d.npg;
   const int32_t* row = a.page_table + static_cast<size_t>(d.b) * a.max_pages + d.pg0;
@@ -361,7 +362,7 @@ __device__ __forceinline__ void load_lengths(const AttnArgs& a, int* prefix, uin
 __device__ __forceinline__ Ranges make_ranges(const AttnArgs& a, int total) {
   Ranges g;
   g.W = max((total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x), a.min_range_pages);
-  g.pmax = kMaxItemTiles / (a.page_size / ZF_BLOCK_TOKENS);
+  g.pmax = min(kMaxItemTiles / (a.page_size / ZF_BLOCK_TOKENS), kMaxItemPages);
   g.ppc = (g.W + g.pmax - 1) / g.pmax;
   return g;
 }
@@ -954,7 +955,7 @@ static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, 
   const long long pairs = static_cast<long long>(batch) * hkv * p.slices;
   const long long total_max = pairs * max_pages;     // pages when every request is full length
   const int tpp = page_size / ZF_BLOCK_TOKENS;
-  const int pmax = kMaxItemTiles / tpp;
+  const int pmax = kMaxItemTiles / tpp < kMaxItemPages ? kMaxItemTiles / tpp : kMaxItemPages;
   const int grid_b = static_cast<int>(total_max < num_sms ? (total_max > 0 ? total_max : 1) : num_sms);
   const long long balanced = (total_max + grid_b - 1) / grid_b;
   auto rounds = [&](long long tiles) { return (tiles + warps - 1) / warps; };

@@ -312,13 +312,12 @@ def run_gpu(args, rank, world, local_rank):
     workspace = zf.new_workspace(ws_bytes, device)
 
     def step(dense=False, events=None):
-        if append is not None and not dense:
-            append.step()
+        if append is not None:
+            append.step(dense)
         for i, ent in enumerate(layers):
             lay = ent["layer"]
-            use_append = append is not None and not dense
-            lens = append.lens if use_append else lay.seq_lens
-            table = append.table if use_append else lay.page_table
+            lens = append.lens if append is not None else lay.seq_lens
+            table = append.table if append is not None else lay.page_table
             if events is not None:
                 events[i][0].record()
             zf.decode_attn(ent["dense"] if dense else ent["cache"], lay.q, table, lens, lay.scale,
@@ -495,7 +494,9 @@ def run_gpu(args, rank, world, local_rank):
 
 class LongContextAppend:
     """Long-context step: every request appends one token to its tail page and that page is
-    re-encoded through zf_encode_pages (raw while partial, compressed once it is full).
+    re-encoded through zf_encode_pages (raw while partial, compressed once it is full).  The dense
+    comparator's step appends too: the same tail pages written raw into the dense cache (the slot
+    of a page id is the id itself there).
 
     All requests have the same length, so the tail page index is shared.  Tail pages (natural
     layout) come from a seeded staging buffer [new page][request][Hkv][P][128]; per-step lengths,
@@ -535,18 +536,19 @@ class LongContextAppend:
         self.n = 0
         self.lens = self.base_lens
 
-    def step(self):
+    def step(self, dense=False):
         import ctypes
         import torch
         if self.n >= self.max_steps:
             raise RuntimeError("more append steps than planned")
         j = self.page_of_step[self.n]
-        d = self.ent["cache"].desc()
+        d = self.ent["dense" if dense else "cache"].desc()
         P = ctypes.c_void_p
+        slots = self.ids_all[j] if dense else self.raw_slots
         code = self.zf.lib().zf_encode_pages(
             ctypes.byref(d), P(self.src_k[j].data_ptr()), P(self.src_v[j].data_ptr()), P(self.ids_all[j].data_ptr()),
-            P(self.fill_all[self.n].data_ptr()), P(self.raw_slots.data_ptr()), self.w.batch, 0,
-            torch.cuda.current_stream().cuda_stream)
+            P(self.fill_all[self.n].data_ptr()), P(slots.data_ptr()), self.w.batch,
+            self.zf.ENCODE_FORCE_RAW if dense else 0, torch.cuda.current_stream().cuda_stream)
         if code != 0:
             raise RuntimeError(f"zf_encode_pages failed: {code}")
         self.lens = self.lens_all[self.n]

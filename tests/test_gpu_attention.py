@@ -225,3 +225,32 @@ def test_full_size_sampled(zf, name):
     k, v = zf.decompress(gc, sample_pages)
     idx = torch.as_tensor(sample_pages, device="cuda")
     assert torch.equal(k, layer.k_pages[idx]) and torch.equal(v, layer.v_pages[idx])
+
+
+def test_back_to_back_calls_with_inputs_changed_between_them(zf):
+    """Consecutive calls on one stream whose page table and lengths are rewritten in place between
+    them (a shape where each call plans and prefetches its first tiles before the previous grid
+    has finished): each call sees its own inputs."""
+    w = W(2, 32, 32, 16, 2048, pool="random", seed=23)
+    layer = I.make_layer(w, seq_lens=[2048, 2048])
+    gc = H.gpu_cache_from(layer, zf)
+    dev = torch.device("cuda")
+    q = layer.q.to(dev)
+    table_a, lens_a = layer.page_table.clone(), layer.seq_lens.clone()
+    table_b = torch.flip(layer.page_table, dims=[0]).contiguous()   # the requests swap their pages
+    lens_b = torch.tensor([1500, 77], dtype=lens_a.dtype)
+    table_dev, lens_dev = table_a.to(dev), lens_a.to(dev)
+    ws = zf.new_workspace(zf.workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.page_size, w.max_pages))
+    outs = []
+    for table, lens in ((table_a, lens_a), (table_b, lens_b), (table_a, lens_a)):
+        table_dev.copy_(table.to(dev), non_blocking=True)
+        lens_dev.copy_(lens.to(dev), non_blocking=True)
+        o, l = zf.decode_attn(gc, q, table_dev, lens_dev, layer.scale, workspace=ws)
+        outs.append((o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    oc = H.oracle_cache_from(layer, O)
+    for (o, l), (table, lens) in zip(outs, ((table_a, lens_a), (table_b, lens_b), (table_a, lens_a))):
+        ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q), oc, table.numpy(), lens.numpy(), layer.scale)
+        H.compare_attention(o, l, ref_out, ref_lse)
+    assert torch.equal(outs[0][0], outs[2][0]) and torch.equal(outs[0][1], outs[2][1])

@@ -115,7 +115,13 @@ struct Plan {
 // What the metadata warp publishes for an item.
 struct ItemDesc {
   int b, c, g, t0, t1, units, h0, nh, single, pg0, npg;   // pg0, npg: the item's pages in the request
+  int planned;   // first item only: the plan made before the wait held, its first tiles are in flight
 };
+
+__device__ __forceinline__ bool same_piece(const ItemDesc& x, const ItemDesc& y) {
+  return x.b == y.b && x.c == y.c && x.g == y.g && x.t0 == y.t0 && x.t1 == y.t1 && x.units == y.units &&
+         x.h0 == y.h0 && x.nh == y.nh && x.single == y.single && x.pg0 == y.pg0 && x.npg == y.npg;
+}
 
 struct SmemLayout {
   size_t stages, item_full, q_full, item_empty, misc, desc, meta, qbuf, bars, prefix, tails, total;
@@ -130,7 +136,7 @@ __host__ __device__ inline SmemLayout smem_layout(int batch) {
   s.item_full = at; at += 2 * 8;                          // count 1: tiles of the item resolved
   s.q_full = at; at += 2 * 8;                             // count 1: q rows of the item staged
   s.item_empty = at; at += 2 * 8;
-  s.misc = at; at += 16 + 16 * 4;                         // [0] abort flag, [16..] combine stage per warp
+  s.misc = at; at += 16 + 16 * 4;    // [0] abort flag, [4] lengths changed, [16..] combine stage per warp
   s.desc = at; at += 2 * 64;
   s.meta = at; at += 2 * kMaxItemTiles * 4;
   s.qbuf = at; at += 2 * kHeadsPerSlice * kQRowBytes;
@@ -192,6 +198,7 @@ __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int
   ItemDesc d;
   d.b = b;
   d.c = c;
+  d.planned = 0;
   d.g = a.slices == 1 ? r : r / a.slices;
   const int s = r - d.g * a.slices;
   d.single = single;
@@ -209,9 +216,12 @@ __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int
 // Resolve the item's pages into one entry per tile: meta[u] = slot << 5 | tile_in_page << 2 | kind
 // (all 32 lanes).  All page-table loads are issued before the directory loads that depend on them.
 // kSpec: relaxed loads of values that may still change, and no error reports (prefetch planning).
+// keep_pid / keep_dir (optional): the page ids and directory entries read, per k (-1 past npg).
+constexpr int kPagesPerLane = kMaxItemPages / 32;
 template <bool kCompressed, bool kSpec = false>
-__device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc& d, int* meta, int lane) {
-  constexpr int kPer = kMaxItemPages / 32;
+__device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc& d, int* meta, int lane,
+                                              int* keep_pid = nullptr, int* keep_dir = nullptr) {
+  constexpr int kPer = kPagesPerLane;
   const int tpp = a.page_size >> 4;
   const int npg = d.npg;
   const int32_t* row = a.page_table + static_cast<size_t>(d.b) * a.max_pages + d.pg0;
@@ -220,6 +230,10 @@ __device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc&
   for (int k = 0; k < kPer; ++k) {
     const int i = lane + 32 * k;
     pid[k] = i < npg ? (kSpec ? ld_relaxed(row + i) : row[i]) : -1;
+    if (keep_pid != nullptr) {
+      keep_pid[k] = pid[k];
+      keep_dir[k] = -1;
+    }
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
@@ -230,6 +244,7 @@ __device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc&
       if (pid[k] >= 0 && pid[k] < a.num_pages) {
         const int32_t* dp = a.dir + static_cast<size_t>(pid[k]) * a.hkv + d.g;
         const int dd = kSpec ? ld_relaxed(dp) : *dp;
+        if (keep_dir != nullptr) keep_dir[k] = dd;
         if (dd == ZF_DIR_COMPRESSED) {
           kind = kKindComp;
           slot = pid[k];
@@ -326,8 +341,12 @@ __device__ __forceinline__ void prefetch_item_tiles(const AttnArgs& a, const Ite
 // (prefix[0] = 0); tokens of each request's last page, minus 1, into tails[b].  All threads; ends
 // with a barrier.
 // kSpec: relaxed loads, no error reports.
+// Returns the (clamped) length of request tid, -1 past the batch.  changed (batch <= kThreads, one
+// request per thread): set when that length differs from held, the one an earlier pass returned.
 template <bool kSpec, int kThreads>
-__device__ __forceinline__ void load_lengths(const AttnArgs& a, int* prefix, uint8_t* tails, int tid) {
+__device__ __forceinline__ int load_lengths(const AttnArgs& a, int* prefix, uint8_t* tails, int tid, int held = -1,
+                                            volatile int* changed = nullptr) {
+  int mine = -1;
   const int warp = tid >> 5, lane = tid & 31;
   const int max_len = a.max_pages * a.page_size;
   for (int b = tid; b < a.batch; b += kThreads) {
@@ -336,6 +355,8 @@ __device__ __forceinline__ void load_lengths(const AttnArgs& a, int* prefix, uin
       if (!kSpec && blockIdx.x == 0) report(a.status, ZF_DEV_BAD_SEQ_LEN);
       len = min(max(len, 0), max_len);
     }
+    if (b == tid) mine = len;
+    if (changed != nullptr && b == tid && len != held) *changed = 1;
     const int pages = (len + a.page_size - 1) / a.page_size;
     prefix[b + 1] = a.chunk_pages > 0 ? (pages + a.chunk_pages - 1) / a.chunk_pages : pages;
     tails[b] = static_cast<uint8_t>(len - (pages - 1) * a.page_size - 1);   // unused when pages == 0
@@ -357,6 +378,7 @@ __device__ __forceinline__ void load_lengths(const AttnArgs& a, int* prefix, uin
     if (lane == 0) prefix[0] = 0;
   }
   __syncthreads();
+  return mine;
 }
 
 __device__ __forceinline__ Ranges make_ranges(const AttnArgs& a, int total) {
@@ -436,16 +458,26 @@ __device__ __forceinline__ bool walk_range(const AttnArgs& a, const int* prefix,
 }
 
 // Stage q rows of an item into qbuf (permuted, padded layout; rows past nh are zero).
-__device__ __forceinline__ void stage_q(const AttnArgs& a, const ItemDesc& d, uint8_t* qb, int lane) {
-  // 8 rows x 64 words; lane handles word w = lane and lane + 32 of every row
+// q rows of an item: 8 rows x 64 words, lane holds words lane and lane + 32 of every row (rows
+// past nh are zero); store_q writes them to qbuf in the permuted, padded layout.
+__device__ __forceinline__ void load_q(const AttnArgs& a, const ItemDesc& d, int lane, uint32_t (&v)[2 * kHeadsPerSlice]) {
+#pragma unroll
   for (int r = 0; r < kHeadsPerSlice; ++r) {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(d.b) * a.hq + d.h0 + min(r, d.nh - 1)) * ZF_HEAD_DIM);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) v[2 * r + h] = r < d.nh ? src[lane + 32 * h] : 0u;
+  }
+}
+
+__device__ __forceinline__ void store_q(uint8_t* qb, int lane, const uint32_t (&v)[2 * kHeadsPerSlice]) {
+#pragma unroll
+  for (int r = 0; r < kHeadsPerSlice; ++r) {
     uint32_t* dst = reinterpret_cast<uint32_t*>(qb + r * kQRowBytes);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int w = lane + 32 * h;              // channel word w = 16j + 4r' + t  (t < 4, r' < 4)
       const int j = w >> 4, rr = (w >> 2) & 3, t = w & 3;
-      dst[16 * j + 4 * t + rr] = r < d.nh ? src[w] : 0u;
+      dst[16 * j + 4 * t + rr] = v[2 * r + h];
     }
   }
 }
@@ -463,6 +495,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
   uint64_t* item_empty = reinterpret_cast<uint64_t*>(smem + L.item_empty);
   uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + L.q_full);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+  volatile int* lengths_changed = reinterpret_cast<volatile int*>(smem + L.misc + 4);
   int* combine_stage = reinterpret_cast<int*>(smem + L.misc + 16);
   ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + L.desc);
   int* meta = reinterpret_cast<int*>(smem + L.meta);
@@ -481,14 +514,23 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
     mbar_init(&item_empty[tid], kWarps);
   }
   if (tid < kWarps * kWarpStages) mbar_init(&bars[tid], 1);
-  if (tid == 0) *abort_flag = 0;
+  if (tid == 0) {
+    *abort_flag = 0;
+    *lengths_changed = 0;
+  }
   fence_mbar_init();
   const int HS = a.hkv * a.slices;
+  // A short call plans its first item before the wait and checks the plan after it (one request
+  // per thread, so each thread can hold the length it read).
+  const bool plan_early = a.prefetch && a.batch <= C::kThreads;
+  int held_len = -1;                      // the length of request tid read before the wait
+  int plan_pid[kPagesPerLane], plan_dir[kPagesPerLane];   // metadata warp: what the plan read
   // While the preceding grid drains (this grid is launched early, see allow_next_grid): L2 hints.
   // (1) lines of seq_lens, the page table and, up to 8 MB, the directory, spread over the grid;
   // (2) for short calls, the K/V records of this CTA's first kPrefetchTiles tiles, planned from
-  //     relaxed reads of lengths, page table and directory that may still change.  Nothing read
-  //     here is used after the wait: the plan is redone from the final values.
+  //     relaxed reads of lengths, page table and directory that may still change.  The first
+  //     item's plan (desc[0], meta buffer 0) is kept: after the wait it is used only if every
+  //     value it was made from reads the same again.
   {
     const size_t n_len = (static_cast<size_t>(a.batch) * 4 + 127) / 128;
     const size_t n_tab = (static_cast<size_t>(a.batch) * a.max_pages * 4 + 127) / 128;
@@ -502,15 +544,21 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
                              : static_cast<const void*>(reinterpret_cast<const uint8_t*>(a.dir) + 128 * (i - n_len - n_tab));
       prefetch_l2(line);
     }
-    if (a.prefetch) load_lengths<true, C::kThreads>(a, prefix, tails, tid);
+    if (a.prefetch) held_len = load_lengths<true, C::kThreads>(a, prefix, tails, tid);
     if (a.prefetch && warp == kWarps) {
+      if (lane == 0) desc[0].b = -1;     // no planned first item (yet)
       const Ranges g = make_ranges(a, HS * prefix[a.batch]);
       int budget = C::kPrefetchTiles;
+      bool first = true;
       walk_range<true>(a, prefix, tails, g, HS, [&](const ItemDesc& d) -> bool {
-        resolve_tiles<kCompressed, true>(a, d, meta, lane);
+        int* mb = meta + (first ? 0 : kMaxItemTiles);
+        if (first) resolve_tiles<kCompressed, true>(a, d, mb, lane, plan_pid, plan_dir);
+        else resolve_tiles<kCompressed, true>(a, d, mb, lane);
         __syncwarp();
+        if (first && lane == 0) desc[0] = d;
+        first = false;
         const int n = min(d.units, budget);
-        prefetch_item_tiles<kCompressed>(a, d, meta, n, lane);
+        prefetch_item_tiles<kCompressed>(a, d, mb, n, lane);
         __syncwarp();
         budget -= n;
         return budget > 0;
@@ -520,17 +568,73 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
   }
   wait_prior_grid();          // inputs may come from the preceding grid
   allow_next_grid();
-  load_lengths<false, C::kThreads>(a, prefix, tails, tid);
+  const uint64_t policy = l2_evict_first_policy();
+  uint32_t inflight = 0;        // consumer: bit s: stage s has copies armed and not yet waited for
+  bool prefetched = false;      // consumer: this warp's first tile of the current item is already in flight
+  // The planned first item.  The metadata warp re-reads the plan's page-table and directory
+  // entries and loads its q rows alongside the lengths below (one round trip instead of lengths,
+  // then page table, then directory); each consumer warp then starts the copy of its first tile
+  // (K/V are final after the wait, and the plan's addresses are in range whatever it read), before
+  // the plan is confirmed.  The copies go out after the lengths, not before: a burst of tile copies
+  // ahead of them slows those small loads down.
+  ItemDesc plan{};
+  plan.b = -1;
+  int check_pid[kPagesPerLane], check_dir[kPagesPerLane];
+  uint32_t qv[2 * kHeadsPerSlice];
+  int plan_tile = kKindInvalid;     // consumer: the plan's entry for this warp's first tile
+  if (plan_early) {
+    plan = desc[0];
+    if (warp < kWarps && plan.b >= 0 && warp < plan.units) plan_tile = meta[warp];   // read before the barrier
+    if (warp == kWarps && plan.b >= 0) {
+      const int32_t* row = a.page_table + static_cast<size_t>(plan.b) * a.max_pages + plan.pg0;
+#pragma unroll
+      for (int k = 0; k < kPagesPerLane; ++k) {
+        const int i = lane + 32 * k;
+        check_pid[k] = i < plan.npg ? row[i] : -1;
+        check_dir[k] = kCompressed && i < plan.npg && plan_pid[k] >= 0 && plan_pid[k] < a.num_pages
+                           ? a.dir[static_cast<size_t>(plan_pid[k]) * a.hkv + plan.g]
+                           : -1;
+      }
+      load_q(a, plan, lane, qv);
+    }
+  }
+  load_lengths<false, C::kThreads>(a, prefix, tails, tid, held_len, plan_early ? lengths_changed : nullptr);
+  if (warp < kWarps && (plan_tile & 3) != kKindInvalid &&
+      issue_tile<kCompressed>(a, plan, &plan_tile, 0, stages + static_cast<size_t>(warp) * kWarpStages * C::kStageBytes,
+                              &bars[warp * kWarpStages], lane, policy)) {
+    inflight = 1u;
+    prefetched = true;
+  }
   const int total = HS * prefix[a.batch];       // pages (items) of all pairs (the host bounds it below 2^30)
   const Ranges g = make_ranges(a, total);
-  const uint64_t policy = l2_evict_first_policy();
 
   if (warp == kWarps) {
     // ============================================================== metadata warp
     // Walk this CTA's page range, publishing one item at a time (double buffered), then an end
     // marker.
+    // The plan holds if no length changed and every page of the planned item reads the same page
+    // id and directory entry as before, all of them valid (so the skipped resolve would have
+    // reported nothing).
+    bool plan_ok = false;
+    if (plan.b >= 0) {
+      bool ok = true;
+#pragma unroll
+      for (int k = 0; k < kPagesPerLane; ++k) {
+        const int i = lane + 32 * k;
+        if (i < plan.npg) {
+          const int pid = plan_pid[k], dd = plan_dir[k];
+          ok = ok && check_pid[k] == pid;
+          if (kCompressed)
+            ok = ok && pid >= 0 && pid < a.num_pages && check_dir[k] == dd &&
+                 (dd == ZF_DIR_COMPRESSED || (dd >= 0 && dd < a.num_raw));
+          else
+            ok = ok && pid >= 0 && pid < a.num_raw;
+        }
+      }
+      plan_ok = __all_sync(0xFFFFFFFFu, ok) && !*lengths_changed;
+    }
     int k = 0;
-    auto publish = [&](const ItemDesc& d) -> bool {
+    auto publish = [&](const ItemDesc& piece) -> bool {
       const int buf = k & 1;
       bool good = true;
       if (lane == 0) good = !*abort_flag && mbar_wait(&item_empty[buf], ((k >> 1) & 1u) ^ 1u);
@@ -542,14 +646,18 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         }
         return false;
       }
-      if (d.b >= 0) resolve_tiles<kCompressed>(a, d, meta + buf * kMaxItemTiles, lane);
+      ItemDesc d = piece;
+      // the first item as planned: meta buffer 0 already holds its tiles and qv its q rows
+      d.planned = k == 0 && plan_ok && d.b >= 0 && same_piece(d, plan);
+      if (d.b >= 0 && !d.planned) resolve_tiles<kCompressed>(a, d, meta + buf * kMaxItemTiles, lane);
       __syncwarp();
       if (lane == 0) {
         desc[buf] = d;
         mbar_arrive(&item_full[buf]);        // release: the tiles can be fetched
       }
       if (d.b >= 0) {
-        stage_q(a, d, qbuf + buf * kHeadsPerSlice * kQRowBytes, lane);
+        if (!d.planned) load_q(a, d, lane, qv);
+        store_q(qbuf + buf * kHeadsPerSlice * kQRowBytes, lane, qv);
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full[buf]);   // release: the q rows
       }
@@ -577,8 +685,6 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
   bool aborted = false;
   int sidx = 0;                 // stage of the next tile to consume
   uint32_t phase = 0;           // bit s: parity of the next wait on stage s
-  uint32_t inflight = 0;        // bit s: stage s has copies armed and not yet waited for
-  bool prefetched = false;      // this warp's first tile of the current item is already in flight
   for (int k = 0;; ++k) {
     const int buf = k & 1;
     if (!aborted && (*abort_flag || !mbar_wait(&item_full[buf], (k >> 1) & 1u))) {
@@ -590,6 +696,20 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
     if (consumer_any<kWarps>(aborted || desc[buf].b < 0)) break;
     const ItemDesc d = desc[buf];
     const int* m = meta + buf * kMaxItemTiles;
+    if (k == 0 && prefetched && !d.planned) {
+      // the copy started from the plan is not this item's: let it land, then start over
+      prefetched = false;
+      if (!aborted) {
+        if (*abort_flag || !mbar_wait(&my_bars[0], phase & 1u)) {
+          aborted = true;
+          *abort_flag = 1;
+          report(a.status, ZF_DEV_TIMEOUT);
+        } else {
+          phase ^= 1u;
+          inflight &= ~1u;
+        }
+      }
+    }
     // Q^T as the B operand (k = channel, n = head): one 16-byte read gives this lane's words of
     // k-steps 2j and 2j+1 (rows past the group's heads are zero)
     const uint8_t* qrow = qbuf + (buf * kHeadsPerSlice + gi) * kQRowBytes + 16 * ti;

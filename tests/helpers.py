@@ -19,6 +19,28 @@ def zf_module():
     return zf
 
 
+def late_writer():
+    """The test-only kernel of late_writer.cu (built on first use into tests/_build): late_copy(src0,
+    dst0, n0, src1, dst1, n1, delay_ns, stream) lets the next grid start at once and copies the
+    int32 arrays about delay_ns later."""
+    import ctypes
+    import os
+    import subprocess
+    here = os.path.dirname(os.path.abspath(__file__))
+    out_dir = os.path.join(here, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, "liblate_writer.so")
+    src = os.path.join(here, "late_writer.cu")
+    if not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+        subprocess.run([B.nvcc(), *B.ARCH, "-O2", "-shared", "-Xcompiler", "-fPIC", src, "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    fn = lib.late_copy
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                   ctypes.c_longlong, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn
+
+
 def np_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy().view(np.uint16)
 

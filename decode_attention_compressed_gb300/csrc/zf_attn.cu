@@ -32,7 +32,8 @@
 //    the item's partial (or as the final output when the pair has a single partial);
 //  * a second kernel merges each (request, head)'s partials by log-sum-exp;
 //  * consecutive calls overlap: the merge kernel lets the next grid launch at once, and that grid
-//    warms L2 (and, for short calls, prefetches its first tiles) while it waits for this one.
+//    warms L2 while it waits for this one; a short call also plans its first item (and prefetches
+//    its first tiles into L2) then, and after the wait keeps that plan if what it read is unchanged.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -75,6 +76,7 @@ constexpr int kMinRangeDivisor = 16;
 // the preceding call's tail is too short to hide the extra planning)
 constexpr int kPrefetchMinTilesPerCta = 16;
 constexpr int kPrefetchMaxTilesPerCta = 512;
+constexpr int kPlanMinTilesPerCta = 4;            // early planning of the first item: from here up to the max
 // planner: items of at least this many rounds (tiles per consumer warp) count as long
 constexpr int kLongItemRounds = 5;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -100,7 +102,8 @@ struct AttnArgs {
   int32_t batch, hq, hkv, group, slices, page_size, num_pages, num_raw, max_pages, max_chunks;
   int32_t min_range_pages;   // lower bound of the pages per CTA range
   int32_t chunk_pages;       // > 0: fixed chunks of this many pages, items dealt round-robin
-  int32_t prefetch;          // plan and prefetch the first tiles while the preceding grid drains
+  int32_t prefetch;          // prefetch the first tiles into L2 while the preceding grid drains
+  int32_t plan_first;        // plan the first item while the preceding grid drains
   int64_t comp_head_bytes;   // bytes of one (page, kv head) K record, compressed
   int64_t raw_head_bytes;    // bytes of one (page, kv head) K record, raw
   float scale_log2;          // softmax_scale * log2(e)
@@ -108,7 +111,7 @@ struct AttnArgs {
 
 struct Plan {
   int grid = 0, max_chunks = 0, slices = 1, min_range_pages = 1, chunk_pages = 0;
-  bool prefetch = false;
+  bool prefetch = false, plan_first = false;
   size_t part_o_bytes = 0, part_lse_bytes = 0, ws_bytes = 0;
 };
 
@@ -124,7 +127,7 @@ __device__ __forceinline__ bool same_piece(const ItemDesc& x, const ItemDesc& y)
 }
 
 struct SmemLayout {
-  size_t stages, item_full, q_full, item_empty, misc, desc, meta, qbuf, bars, prefix, tails, total;
+  size_t stages, item_full, q_full, item_empty, misc, desc, meta, qbuf, bars, prefix, lens, total;
 };
 
 template <bool kCompressed>
@@ -142,7 +145,7 @@ __host__ __device__ inline SmemLayout smem_layout(int batch) {
   s.qbuf = at; at += 2 * kHeadsPerSlice * kQRowBytes;
   s.bars = at; at += static_cast<size_t>(C::kWarps) * kWarpStages * 8;
   s.prefix = at; at += static_cast<size_t>(batch + 1) * 4;
-  s.tails = at; at += static_cast<size_t>(batch);        // tokens in each request's last page, minus 1
+  s.lens = at; at += static_cast<size_t>(batch) * 4;     // each request's length, clamped
   s.total = (at + 127) & ~static_cast<size_t>(127);
   return s;
 }
@@ -191,10 +194,9 @@ __device__ __forceinline__ int pair_chunks(const Ranges& g, int S, int n) {
   return chunks_before(g, S, kl) + (tail + g.pmax - 1) / g.pmax;
 }
 
-// The item covering pages [pg0, pg1) of pair (b, r) as partial c.
-// n: pages of request b; tail: tokens in its last page.
+// The item covering pages [pg0, pg1) of pair (b, r) as partial c; L: the length of request b.
 __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int r, int pg0, int pg1, int c,
-                                                   bool single, int n, int tail) {
+                                                   bool single, int L) {
   ItemDesc d;
   d.b = b;
   d.c = c;
@@ -204,7 +206,6 @@ __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int
   d.single = single;
   d.pg0 = pg0;
   d.npg = pg1 - pg0;
-  const int L = (n - 1) * a.page_size + tail;
   d.t0 = pg0 * a.page_size;
   d.t1 = min(pg1 * a.page_size, L);
   d.units = (d.t1 - d.t0 + 15) >> 4;
@@ -338,13 +339,13 @@ __device__ __forceinline__ void prefetch_item_tiles(const AttnArgs& a, const Ite
 }
 
 // Pages of every request (chunks, when chunk_pages > 0) into prefix[b + 1], then prefix sums
-// (prefix[0] = 0); tokens of each request's last page, minus 1, into tails[b].  All threads; ends
+// (prefix[0] = 0); each request's length (clamped) into lens[b].  All threads; ends
 // with a barrier.
 // kSpec: relaxed loads, no error reports.
 // Returns the (clamped) length of request tid, -1 past the batch.  changed (batch <= kThreads, one
 // request per thread): set when that length differs from held, the one an earlier pass returned.
 template <bool kSpec, int kThreads>
-__device__ __forceinline__ int load_lengths(const AttnArgs& a, int* prefix, uint8_t* tails, int tid, int held = -1,
+__device__ __forceinline__ int load_lengths(const AttnArgs& a, int* prefix, int* lens, int tid, int held = -1,
                                             volatile int* changed = nullptr) {
   int mine = -1;
   const int warp = tid >> 5, lane = tid & 31;
@@ -359,7 +360,7 @@ __device__ __forceinline__ int load_lengths(const AttnArgs& a, int* prefix, uint
     if (changed != nullptr && b == tid && len != held) *changed = 1;
     const int pages = (len + a.page_size - 1) / a.page_size;
     prefix[b + 1] = a.chunk_pages > 0 ? (pages + a.chunk_pages - 1) / a.chunk_pages : pages;
-    tails[b] = static_cast<uint8_t>(len - (pages - 1) * a.page_size - 1);   // unused when pages == 0
+    lens[b] = len;
   }
   __syncthreads();
   if (warp == 0) {
@@ -394,8 +395,8 @@ __device__ __forceinline__ Ranges make_ranges(const AttnArgs& a, int total) {
 //  * balanced mode (chunk_pages == 0): this CTA's page range, pair by pair;
 //  * chunked mode: items (request, chunk, kv head / slice) of chunk_pages pages, dealt round-robin
 //    (item i to CTA i % grid); prefix holds chunk counts.
-template <bool kSpec, typename Emit>
-__device__ __forceinline__ bool walk_range(const AttnArgs& a, const int* prefix, const uint8_t* tails, const Ranges& g,
+template <typename Emit>
+__device__ __forceinline__ bool walk_range(const AttnArgs& a, const int* prefix, const int* lens, const Ranges& g,
                                            int HS, Emit&& emit) {
   if (a.chunk_pages > 0) {
     const int cp = a.chunk_pages;
@@ -408,10 +409,9 @@ __device__ __forceinline__ bool walk_range(const AttnArgs& a, const int* prefix,
         if (prefix[mid] <= j) l = mid; else h = mid;
       }
       const int c = j - prefix[l];
-      const int len = min(max(kSpec ? ld_relaxed(a.seq_lens + l) : a.seq_lens[l], 0), a.max_pages * a.page_size);
+      const int len = lens[l];
       const int n = (len + a.page_size - 1) / a.page_size;
-      if (!emit(describe_piece(a, l, r, c * cp, min(c * cp + cp, n), c, prefix[l + 1] - prefix[l] == 1, n,
-                               tails[l] + 1)))
+      if (!emit(describe_piece(a, l, r, c * cp, min(c * cp + cp, n), c, prefix[l + 1] - prefix[l] == 1, len)))
         return false;
     }
     return true;
@@ -442,7 +442,7 @@ __device__ __forceinline__ bool walk_range(const AttnArgs& a, const int* prefix,
   while (true) {
     const int seg_end = min(hi, S + n);
     for (int pt = t; pt < seg_end; pt += g.pmax, ++c)
-      if (!emit(describe_piece(a, b, r, pt - S, min(pt + g.pmax, seg_end) - S, c, single, n, tails[b] + 1)))
+      if (!emit(describe_piece(a, b, r, pt - S, min(pt + g.pmax, seg_end) - S, c, single, lens[b])))
         return false;
     t = seg_end;
     if (t >= hi) return true;
@@ -502,7 +502,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
   uint8_t* qbuf = smem + L.qbuf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* prefix = reinterpret_cast<int*>(smem + L.prefix);
-  uint8_t* tails = smem + L.tails;
+  int* lens = reinterpret_cast<int*>(smem + L.lens);
   uint8_t* stages = smem + L.stages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -520,9 +520,9 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
   }
   fence_mbar_init();
   const int HS = a.hkv * a.slices;
-  // A short call plans its first item before the wait and checks the plan after it (one request
-  // per thread, so each thread can hold the length it read).
-  const bool plan_early = a.prefetch && a.batch <= C::kThreads;
+  // A call plans its first item before the wait and checks the plan after it (one request per
+  // thread, so each thread can hold the length it read).
+  const bool plan_early = a.plan_first && a.batch <= C::kThreads;
   int held_len = -1;                      // the length of request tid read before the wait
   int plan_pid[kPagesPerLane], plan_dir[kPagesPerLane];   // metadata warp: what the plan read
   // While the preceding grid drains (this grid is launched early, see allow_next_grid): L2 hints.
@@ -544,13 +544,14 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
                              : static_cast<const void*>(reinterpret_cast<const uint8_t*>(a.dir) + 128 * (i - n_len - n_tab));
       prefetch_l2(line);
     }
-    if (a.prefetch) held_len = load_lengths<true, C::kThreads>(a, prefix, tails, tid);
-    if (a.prefetch && warp == kWarps) {
+    const bool spec = a.prefetch || plan_early;
+    if (spec) held_len = load_lengths<true, C::kThreads>(a, prefix, lens, tid);
+    if (spec && warp == kWarps) {
       if (lane == 0) desc[0].b = -1;     // no planned first item (yet)
       const Ranges g = make_ranges(a, HS * prefix[a.batch]);
-      int budget = C::kPrefetchTiles;
+      int budget = a.prefetch ? C::kPrefetchTiles : 0;
       bool first = true;
-      walk_range<true>(a, prefix, tails, g, HS, [&](const ItemDesc& d) -> bool {
+      walk_range(a, prefix, lens, g, HS, [&](const ItemDesc& d) -> bool {
         int* mb = meta + (first ? 0 : kMaxItemTiles);
         if (first) resolve_tiles<kCompressed, true>(a, d, mb, lane, plan_pid, plan_dir);
         else resolve_tiles<kCompressed, true>(a, d, mb, lane);
@@ -558,7 +559,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         if (first && lane == 0) desc[0] = d;
         first = false;
         const int n = min(d.units, budget);
-        prefetch_item_tiles<kCompressed>(a, d, mb, n, lane);
+        if (n > 0) prefetch_item_tiles<kCompressed>(a, d, mb, n, lane);
         __syncwarp();
         budget -= n;
         return budget > 0;
@@ -598,7 +599,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
       load_q(a, plan, lane, qv);
     }
   }
-  load_lengths<false, C::kThreads>(a, prefix, tails, tid, held_len, plan_early ? lengths_changed : nullptr);
+  load_lengths<false, C::kThreads>(a, prefix, lens, tid, held_len, plan_early ? lengths_changed : nullptr);
   if (warp < kWarps && (plan_tile & 3) != kKindInvalid &&
       issue_tile<kCompressed>(a, plan, &plan_tile, 0, stages + static_cast<size_t>(warp) * kWarpStages * C::kStageBytes,
                               &bars[warp * kWarpStages], lane, policy)) {
@@ -664,7 +665,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
       ++k;
       return true;
     };
-    if (walk_range<false>(a, prefix, tails, g, HS, publish)) {
+    if (walk_range(a, prefix, lens, g, HS, publish)) {
       ItemDesc end_marker{};
       end_marker.b = -1;
       publish(end_marker);
@@ -1121,10 +1122,14 @@ static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, 
     // each, so it has at most floor(n / pmax) + ceil(n / W) + 1 partials.
     p.max_chunks = max_pages / pmax + (max_pages + p.min_range_pages - 1) / p.min_range_pages + 1;
   }
-  // Short calls (a few rounds of tiles per CTA) are dominated by their start-up; they plan and
-  // prefetch their first tiles while the preceding grid drains.  Long calls skip it (when nothing
-  // precedes them it would only delay their start), and so do the shortest.
+  // Short calls (a few rounds of tiles per CTA) are dominated by their start-up: they plan their
+  // first item while the preceding grid drains, and those above a few tiles per CTA also prefetch
+  // their first tiles into L2.  Long calls do neither (measured on GB300: planning early made the
+  // Llama-3-8B batch-64 call 2.7% slower, the prefetch slower still).  Below the prefetch range
+  // the plan still pays (LLaMA-7B MHA at 512 tokens, 7 tiles per CTA: 11.2 -> 10.5 us per call),
+  // down to a few tiles per CTA (a single 8-head 512-token call, 2 tiles per CTA, lost 0.1-1.6 us).
   p.prefetch = balanced * tpp >= kPrefetchMinTilesPerCta && balanced * tpp <= kPrefetchMaxTilesPerCta;
+  p.plan_first = balanced * tpp >= kPlanMinTilesPerCta && balanced * tpp <= kPrefetchMaxTilesPerCta;
   const size_t n = static_cast<size_t>(batch) * hq * p.max_chunks;
   p.part_o_bytes = n * ZF_HEAD_DIM * 4;
   p.part_lse_bytes = (n * 4 + 255) & ~static_cast<size_t>(255);
@@ -1220,6 +1225,7 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   a.min_range_pages = p.min_range_pages;
   a.chunk_pages = p.chunk_pages;
   a.prefetch = p.prefetch ? 1 : 0;
+  a.plan_first = p.plan_first ? 1 : 0;
   a.comp_head_bytes = static_cast<int64_t>(c->page_size / 4) * kSlotBytes;
   a.raw_head_bytes = static_cast<int64_t>(c->page_size / 4) * kRawBlockBytes;
   a.scale_log2 = scale * 1.4426950408889634f;

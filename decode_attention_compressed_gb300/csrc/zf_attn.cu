@@ -215,7 +215,9 @@ __device__ __forceinline__ ItemDesc describe_piece(const AttnArgs& a, int b, int
 }
 
 // Resolve the item's pages into one entry per tile: meta[u] = slot << 5 | tile_in_page << 2 | kind
-// (all 32 lanes).  All page-table loads are issued before the directory loads that depend on them.
+// (all 32 lanes).  Two rounds of independent loads: every page-table entry, then every directory
+// entry they name; only then are the entries classified and written (classifying each page as
+// its directory entry arrives made one dependent round trip per page and lane: up to 8 in a row).
 // kSpec: relaxed loads of values that may still change, and no error reports (prefetch planning).
 // keep_pid / keep_dir (optional): the page ids and directory entries read, per k (-1 past npg).
 constexpr int kPagesPerLane = kMaxItemPages / 32;
@@ -226,14 +228,25 @@ __device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc&
   const int tpp = a.page_size >> 4;
   const int npg = d.npg;
   const int32_t* row = a.page_table + static_cast<size_t>(d.b) * a.max_pages + d.pg0;
-  int pid[kPer];
+  int pid[kPer], dir[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int i = lane + 32 * k;
     pid[k] = i < npg ? (kSpec ? ld_relaxed(row + i) : row[i]) : -1;
-    if (keep_pid != nullptr) {
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    dir[k] = -2;                                   // no entry read (never a valid one)
+    if (kCompressed && pid[k] >= 0 && pid[k] < a.num_pages) {
+      const int32_t* dp = a.dir + static_cast<size_t>(pid[k]) * a.hkv + d.g;
+      dir[k] = kSpec ? ld_relaxed(dp) : *dp;
+    }
+  }
+  if (keep_pid != nullptr) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
       keep_pid[k] = pid[k];
-      keep_dir[k] = -1;
+      keep_dir[k] = dir[k] == -2 ? -1 : dir[k];
     }
   }
 #pragma unroll
@@ -243,9 +256,7 @@ __device__ __forceinline__ void resolve_tiles(const AttnArgs& a, const ItemDesc&
     int kind = kKindInvalid, slot = 0;
     if (kCompressed) {
       if (pid[k] >= 0 && pid[k] < a.num_pages) {
-        const int32_t* dp = a.dir + static_cast<size_t>(pid[k]) * a.hkv + d.g;
-        const int dd = kSpec ? ld_relaxed(dp) : *dp;
-        if (keep_dir != nullptr) keep_dir[k] = dd;
+        const int dd = dir[k];
         if (dd == ZF_DIR_COMPRESSED) {
           kind = kKindComp;
           slot = pid[k];

@@ -173,6 +173,13 @@ size_t zf_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
  *               it must not be shared with a concurrent call.
  *   batch <= ZF_MAX_BATCH.  Two kernels are enqueued (attention, then merge); results are
  *   deterministic (no atomics).
+ *   Both are launched with programmatic stream serialisation: when the kernel ahead of them in
+ *   the stream allows it (griddepcontrol.launch_dependents; this library's merge kernel does), the
+ *   attention grid starts early.  Before its grid-dependency wait it only warms L2 and, for short
+ *   calls, plans its first item from relaxed reads of seq_lens, page_table and the directory and
+ *   prefetches the first tiles into L2; after the wait every length, page-table and directory
+ *   entry it uses is read again (a plan whose inputs changed is dropped) and q and the K/V data
+ *   are read only then, so inputs written by that preceding kernel are always seen.
  */
 zf_status zf_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch,
                          int32_t num_q_heads, const int32_t* page_table, int32_t max_pages_per_req,

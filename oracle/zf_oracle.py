@@ -440,6 +440,39 @@ def decode_attention(q_bits, cache: Cache, page_table, seq_lens, scale: float, p
     return out, lse
 
 
+def decode_attention_multi(q_bits, cache: Cache, page_table, seq_lens, scale: float, pairs=None):
+    """Decode attention for T new tokens per request (what zf_decode_attn_multi computes):
+    speculative verification or multi-token decode.  The pages treat one new token per step; this
+    extension takes the plain causal reading: the T query tokens of request b sit at positions
+    L-T .. L-1 (L = seq_lens[b], their own keys and values already in the cache), and token t
+    attends to the keys at positions 0 .. L-T+t, each one exactly as a single-token decode over
+    that prefix.
+
+    q_bits: [B][T][Hq][128] BF16 bits.  Returns out [B][T][Hq][128], lse [B][T][Hq].
+    `pairs`, if given, lists (b, t, h) to evaluate (others are left 0 / -inf).
+    """
+    B, T, Hq, D = q_bits.shape
+    Hkv = cache.num_kv_heads
+    group = Hq // Hkv
+    out = np.zeros((B, T, Hq, D))
+    lse = np.full((B, T, Hq), -math.inf)
+    want = sorted(pairs) if pairs is not None else [(b, t, h) for b in range(B) for t in range(T) for h in range(Hq)]
+    q = bf16_to_f64(q_bits)
+    by_b = {}
+    for b, t, h in want:
+        by_b.setdefault(b, []).append((t, h))
+    for b, ths in by_b.items():
+        L = int(seq_lens[b])
+        heads = sorted({h // group for _, h in ths})
+        K, V = gather_sequence(cache, page_table[b], L, heads)
+        K, V = bf16_to_f64(K), bf16_to_f64(V)
+        for t, h in ths:
+            g = h // group
+            visible = max(L - T + t + 1, 0)
+            out[b, t, h], lse[b, t, h], _ = attention_one(q[b, t, h], K[:visible, g, :], V[:visible, g, :], scale)
+    return out, lse
+
+
 def merge_partials(outs, lses):
     """Split-result merge: lse = ln sum_i exp(lse_i); out = sum_i exp(lse_i - lse) out_i,
     where out_i is the normalised output of chunk i."""

@@ -167,3 +167,68 @@ def test_dense_kv_bytes_formula():
     assert dense_kv_bytes(32, 128, 32, 8192) == 4 * 2 ** 30
     assert dense_kv_bytes(8, 128, 36, 32768) / 2 ** 30 == 4.5
     assert dense_kv_bytes(10, 128, 40, 32768) / 2 ** 30 == 6.25
+
+
+# ---- several new tokens per request (speculative verification): token t of T at position
+# L - T + t attends to positions 0 .. L - T + t (the causal rule, one token's decode per prefix)
+def _multi_q(rng, B, T, Hq):
+    return rand_bits(rng, (B, T, Hq, 128))
+
+
+def test_multi_token_with_one_token_is_the_decode():
+    L, cache, k, v = _small_paged(seed=11)
+    q = L.q.numpy().view(np.uint16)
+    table, lens = L.page_table.numpy(), L.seq_lens.numpy()
+    out, lse = O.decode_attention(q, cache, table, lens, L.scale)
+    mout, mlse = O.decode_attention_multi(q[:, None], cache, table, lens, L.scale)
+    assert (mout[:, 0] == out).all() and (mlse[:, 0] == lse).all()
+
+
+def test_multi_token_identical_keys_give_mean_of_the_visible_values():
+    """Closed form: with every key of a head equal, token t's weights are uniform over the
+    L - T + t + 1 positions it sees, so out is the mean of those V rows and lse is
+    scale * q.k + ln(count)."""
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, P, T = 2, 4, 2, 16, 5
+    lens = (37, 5)
+    w = I.Workload("t", B, Hq, Hkv, P, max(lens), seed=12)
+    lay = I.make_layer(w, seq_lens=list(lens))
+    k = lay.k_pages.numpy().view(np.uint16).copy()
+    v = lay.v_pages.numpy().view(np.uint16)
+    krow = rand_bits(rng, (Hkv, 128), 2.0)
+    k[:] = krow[None, :, None, :]
+    npg = lay.num_pages
+    cache = O.Cache(num_pages=npg, num_kv_heads=Hkv, page_size=P, num_raw=npg)
+    O.encode_pages(cache, k, v, list(range(npg)), lay.n_valid.numpy(), list(range(npg)))
+    q = _multi_q(rng, B, T, Hq)
+    table = lay.page_table.numpy()
+    out, lse = O.decode_attention_multi(q, cache, table, np.array(lens), 0.125)
+    for b in range(B):
+        Lb = lens[b]
+        vseq = np.concatenate([v[p].transpose(1, 0, 2) for p in table[b, : -(-Lb // P)]])[:Lb]
+        for t in range(T):
+            n = Lb - T + t + 1
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                if n <= 0:
+                    assert (out[b, t, h] == 0).all() and np.isneginf(lse[b, t, h])
+                    continue
+                mean = O.bf16_to_f64(vseq[:n, g]).mean(axis=0)
+                assert np.abs(out[b, t, h] - mean).max() < 1e-12
+                s = 0.125 * float(O.bf16_to_f64(krow[g]) @ O.bf16_to_f64(q[b, t, h]))
+                assert abs(lse[b, t, h] - (s + math.log(n))) < 1e-12
+
+
+def test_multi_token_each_token_is_a_single_token_decode_of_its_prefix():
+    L, cache, k, v = _small_paged(seed=13, lens=(37, 16, 70))
+    rng = np.random.default_rng(13)
+    T = 4
+    q = _multi_q(rng, 3, T, 8)
+    table, lens = L.page_table.numpy(), L.seq_lens.numpy()
+    out, lse = O.decode_attention_multi(q, cache, table, lens, L.scale)
+    for t in range(T):
+        ref, ref_lse = O.decode_attention(q[:, t], cache, table, lens - (T - 1 - t), L.scale)
+        assert (out[:, t] == ref).all() and (lse[:, t] == ref_lse).all()
+    sub, sub_lse = O.decode_attention_multi(q, cache, table, lens, L.scale, pairs=[(2, 3, 5), (0, 1, 0)])
+    assert (sub[2, 3, 5] == out[2, 3, 5]).all() and sub_lse[0, 1, 0] == lse[0, 1, 0]
+    assert (sub[1] == 0).all() and np.isneginf(sub_lse[1]).all()

@@ -91,3 +91,21 @@ def test_merge_without_renormalisation_is_caught(monkeypatch):
         return np.mean(np.asarray(outs), axis=0), float(np.max(lses))
     monkeypatch.setattr(O, "merge_partials", bad_merge)
     _fails(TA.test_split_merge_equals_unsplit)
+
+
+def test_multi_token_off_by_one_is_caught(monkeypatch):
+    """Token t seeing one position fewer than its own (a causal limit of L - T + t, exclusive)."""
+    real = O.attention_one
+
+    def drop_last(q, K, V, scale):
+        return real(q, K[:-1], V[:-1], scale) if len(K) else real(q, K, V, scale)
+
+    def bad_multi(q_bits, cache, page_table, seq_lens, scale, pairs=None):
+        monkeypatch.setattr(O, "attention_one", drop_last)
+        try:
+            return real_multi(q_bits, cache, page_table, seq_lens, scale, pairs)
+        finally:
+            monkeypatch.setattr(O, "attention_one", real)
+    real_multi = O.decode_attention_multi
+    monkeypatch.setattr(O, "decode_attention_multi", bad_multi)
+    _fails(TA.test_multi_token_identical_keys_give_mean_of_the_visible_values)

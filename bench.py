@@ -176,10 +176,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------ GPU arm
-def tile_bytes(layer, dirs, compressed: bool) -> int:
+def tile_bytes(layer, dirs, compressed: bool, tokens: int = 1) -> int:
     """Algorithmic bytes one attention launch reads: per (request, kv head), every 16-token tile
     holding context tokens costs 6272 bytes (compressed page) or 8192 bytes (raw page), plus q,
-    page table, seq_lens, out and lse."""
+    page table, seq_lens, out and lse (q, out and lse once per new token)."""
     import torch
     w = layer.workload
     P = w.page_size
@@ -197,8 +197,8 @@ def tile_bytes(layer, dirs, compressed: bool) -> int:
             total += int(per.sum())
         else:
             total += int(tiles.sum()) * 8192 * w.num_kv_heads
-    total += w.batch * w.num_q_heads * 128 * 2 + table.numel() * 4 + w.batch * 4
-    total += w.batch * w.num_q_heads * (128 * 4 + 4)
+    total += tokens * w.batch * w.num_q_heads * 128 * 2 + table.numel() * 4 + w.batch * 4
+    total += tokens * w.batch * w.num_q_heads * (128 * 4 + 4)
     return total
 
 
@@ -300,15 +300,27 @@ def run_gpu(args, rank, world, local_rank):
     w = workload_of(args)
     layers = setup_layers(zf, I, w, device)
     stream = torch.cuda.current_stream()
-    outs = [(torch.empty(w.batch, w.num_q_heads, 128, device=device),
-             torch.empty(w.batch, w.num_q_heads, device=device)) for _ in layers]
+    T = args.tokens
+    if T > 1 and w.name == "long_ctx":
+        raise SystemExit("--tokens > 1 is not combined with the long-context append step")
+    # several new tokens per request: each layer's queries [batch][T][heads][128] (zf_decode_attn_multi)
+    qs = [I.make_multi_queries(w, T, layer=i, device=device) if T > 1 else ent["layer"].q
+          for i, ent in enumerate(layers)]
+    oshape = (w.batch, T, w.num_q_heads) if T > 1 else (w.batch, w.num_q_heads)
+    outs = [(torch.empty(*oshape, 128, device=device), torch.empty(*oshape, device=device)) for _ in layers]
+
+    def attn(cache, q, table, lens, scale, out, lse, dense=False):
+        if T > 1:
+            zf.decode_attn_multi(cache, q, table, lens, scale, out=out, lse=lse, workspace=workspace, dense=dense)
+        else:
+            zf.decode_attn(cache, q, table, lens, scale, out=out, lse=lse, workspace=workspace, dense=dense)
 
     append = None
     max_pages = int(layers[0]["layer"].page_table.shape[1])
     if w.name == "long_ctx":
         append = LongContextAppend(zf, I, w, layers[0], device, 2 * (args.steps + args.warmup))
         max_pages = int(append.table.shape[1])
-    ws_bytes = zf.workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.page_size, max_pages)
+    ws_bytes = zf.workspace_size_multi(w.batch, T, w.num_q_heads, w.num_kv_heads, w.page_size, max_pages)
     workspace = zf.new_workspace(ws_bytes, device)
 
     def step(dense=False, events=None):
@@ -320,8 +332,7 @@ def run_gpu(args, rank, world, local_rank):
             table = append.table if append is not None else lay.page_table
             if events is not None:
                 events[i][0].record()
-            zf.decode_attn(ent["dense"] if dense else ent["cache"], lay.q, table, lens, lay.scale,
-                           out=outs[i][0], lse=outs[i][1], workspace=workspace, dense=dense)
+            attn(ent["dense"] if dense else ent["cache"], qs[i], table, lens, lay.scale, outs[i][0], outs[i][1], dense)
             if events is not None:
                 events[i][1].record()
 
@@ -396,8 +407,7 @@ def run_gpu(args, rank, world, local_rank):
         for i, ent in enumerate(layers):
             lay = ent["layer"]
             zf.decompress_to_raw(ent["cache"], all_ids[i], shared)
-            zf.decode_attn(shared, lay.q, lay.page_table, lay.seq_lens, lay.scale, out=outs[i][0], lse=outs[i][1],
-                           workspace=workspace, dense=True)
+            attn(shared, qs[i], lay.page_table, lay.seq_lens, lay.scale, outs[i][0], outs[i][1], dense=True)
 
     g_restore = capture(restore_step)
     restore_ms, _, _ = timed(g_restore.replay)
@@ -406,11 +416,11 @@ def run_gpu(args, rank, world, local_rank):
     # end to end through the public API: every layer's q and seq_lens from pinned host memory (one
     # copy of the stacked step inputs), the 32 calls, every layer's out + lse back (one copy each)
     L = len(layers)
-    q_host = torch.stack([ent["layer"].q.cpu() for ent in layers]).pin_memory()
+    q_host = torch.stack([q.cpu() for q in qs]).pin_memory()
     lens_host = torch.stack([ent["layer"].seq_lens.cpu() for ent in layers]).pin_memory()
     q_dev, lens_dev = torch.empty_like(q_host, device=device), torch.empty_like(lens_host, device=device)
-    out_dev = torch.empty((L, w.batch, w.num_q_heads, 128), device=device)
-    lse_dev = torch.empty((L, w.batch, w.num_q_heads), device=device)
+    out_dev = torch.empty((L, *oshape, 128), device=device)
+    lse_dev = torch.empty((L, *oshape), device=device)
     out_host = torch.empty(out_dev.shape, pin_memory=True)
     lse_host = torch.empty(lse_dev.shape, pin_memory=True)
 
@@ -419,8 +429,7 @@ def run_gpu(args, rank, world, local_rank):
         lens_dev.copy_(lens_host, non_blocking=True)
         for i, ent in enumerate(layers):
             lay = ent["layer"]
-            zf.decode_attn(ent["cache"], q_dev[i], lay.page_table, lens_dev[i], lay.scale, out=out_dev[i],
-                           lse=lse_dev[i], workspace=workspace)
+            attn(ent["cache"], q_dev[i], lay.page_table, lens_dev[i], lay.scale, out_dev[i], lse_dev[i])
         out_host.copy_(out_dev, non_blocking=True)
         lse_host.copy_(lse_dev, non_blocking=True)
 
@@ -434,8 +443,8 @@ def run_gpu(args, rank, world, local_rank):
         e2e_ms = e2e_eager_ms = None
         h2d = d2h = 0
 
-    comp_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], True) for ent in layers)
-    dense_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], False) for ent in layers)
+    comp_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], True, T) for ent in layers)
+    dense_bytes = sum(tile_bytes(ent["layer"], ent["dirs"], False, T) for ent in layers)
     uncompressed = sum(dense_equiv_bytes(ent["layer"]) for ent in layers)
     stored = sum(ent["cache"].stored_bytes(ent["num_pages"]) for ent in layers)
     dense_stored = sum(ent["num_pages"] * w.num_kv_heads * 2 * w.page_size * 128 * 2 for ent in layers)
@@ -455,7 +464,8 @@ def run_gpu(args, rank, world, local_rank):
         vs_baseline=None, dtype="bf16", data="synthetic (seeded, distributions of the workload)",
         config={"workload": w.name, "note": w.note, "batch": w.batch, "q_heads": w.num_q_heads,
                 "kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": w.page_size, "ctx": w.ctx,
-                "layers_per_step": w.layers, "parallelism": "replicas" if world > 1 else "single",
+                "layers_per_step": w.layers, "new_tokens_per_request": T,
+                "parallelism": "replicas" if world > 1 else "single",
                 "l2": f"no flush: {comp_bytes / 1e9:.2f} GB of compressed KV read per step "
                       f"(> {L2_BYTES / 2**20:.0f} MiB L2)"},
         kv_gbs_compressed=round(comp_bytes / (ms_step * 1e-3) / 1e9, 1),
@@ -477,12 +487,13 @@ def run_gpu(args, rank, world, local_rank):
         launch_mode="cuda_graph (one graph per decode step)" if use_graph else "eager",
         eager={"us_per_step": round(eager_ms * 1e3, 3), "dense_us_per_step": round(eager_dense_ms * 1e3, 3),
                "e2e_us_per_step": round(e2e_eager_ms * 1e3, 3) if e2e_eager_ms else None},
-        roofline={"kernel": "attn_kernel<compressed> + merge_kernel (one zf_decode_attn call; "
+        roofline={"kernel": "attn_kernel<compressed> + merge_kernel (one "
+                            + ("zf_decode_attn_multi" if T > 1 else "zf_decode_attn") + " call; "
                             + ("step time / layers" if use_graph else "events around each call") + ")",
                   "bound": "hbm",
                   "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                   "peak_source": peak_kind, "bytes_per_launch": int(per_launch), "call_us": round(call_ms * 1e3, 3),
-                  "traffic": read_traffic(w.name)},
+                  "traffic": read_traffic(w.name) if T == 1 else None},
         e2e={"value": round(e2e_ms * 1e3, 3) if e2e_ms else None, "unit": "us/step", "h2d_bytes_per_step": h2d,
              "d2h_bytes_per_step": d2h},
         gpu_launches=args.steps * len(layers) * 2 + (args.steps if append is not None else 0),
@@ -636,6 +647,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=1,
+                    help="new tokens per request per call (speculative verification; zf_decode_attn_multi)")
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first N layers of a multi-layer workload (profiling captures)")
     ap.add_argument("--batch", type=int, default=None,

@@ -81,6 +81,9 @@ constexpr int kPlanMinTilesPerCta = 4;            // early planning of the first
 constexpr int kLongItemRounds = 5;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p <= 2^8 between max updates
+// running max before any visible score: finite, so that a column whose scores are all hidden (a
+// new token that sees none of an item's positions) gets p = 2^(-inf - kNoScore) = 0, not NaN
+constexpr float kNoScore = -1e30f;
 
 enum : int { kKindComp = 0, kKindRaw = 1, kKindInvalid = 2 };
 
@@ -100,6 +103,7 @@ struct AttnArgs {
   float* part_lse;
   int32_t* chunk_counts;     // [batch][hkv * slices] partials per pair, for the merge kernel
   int32_t batch, hq, hkv, group, slices, page_size, num_pages, num_raw, max_pages, max_chunks;
+  int32_t tokens;            // new tokens per request T: query head qh = head * T + token (hq, group count them)
   int32_t min_range_pages;   // lower bound of the pages per CTA range
   int32_t chunk_pages;       // > 0: fixed chunks of this many pages, items dealt round-robin
   int32_t prefetch;          // prefetch the first tiles into L2 while the preceding grid drains
@@ -120,6 +124,12 @@ struct ItemDesc {
   int b, c, g, t0, t1, units, h0, nh, single, pg0, npg;   // pg0, npg: the item's pages in the request
   int planned;   // first item only: the plan made before the wait held, its first tiles are in flight
 };
+
+// Row of q, out and lse (stored [batch][T][heads]) for query head qh = head * T + token of request b.
+__device__ __forceinline__ size_t query_row(int b, int qh, int T, int hq) {
+  const int h = qh / T, t = qh - h * T;
+  return (static_cast<size_t>(b) * T + t) * (hq / T) + h;
+}
 
 __device__ __forceinline__ bool same_piece(const ItemDesc& x, const ItemDesc& y) {
   return x.b == y.b && x.c == y.c && x.g == y.g && x.t0 == y.t0 && x.t1 == y.t1 && x.units == y.units &&
@@ -471,10 +481,13 @@ __device__ __forceinline__ bool walk_range(const AttnArgs& a, const int* prefix,
 // Stage q rows of an item into qbuf (permuted, padded layout; rows past nh are zero).
 // q rows of an item: 8 rows x 64 words, lane holds words lane and lane + 32 of every row (rows
 // past nh are zero); store_q writes them to qbuf in the permuted, padded layout.
+template <bool kMulti>
 __device__ __forceinline__ void load_q(const AttnArgs& a, const ItemDesc& d, int lane, uint32_t (&v)[2 * kHeadsPerSlice]) {
 #pragma unroll
   for (int r = 0; r < kHeadsPerSlice; ++r) {
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(d.b) * a.hq + d.h0 + min(r, d.nh - 1)) * ZF_HEAD_DIM);
+    const int qh = d.h0 + min(r, d.nh - 1);
+    const size_t row = kMulti ? query_row(d.b, qh, a.tokens, a.hq) : static_cast<size_t>(d.b) * a.hq + qh;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q + row * ZF_HEAD_DIM);
 #pragma unroll
     for (int h = 0; h < 2; ++h) v[2 * r + h] = r < d.nh ? src[lane + 32 * h] : 0u;
   }
@@ -493,7 +506,10 @@ __device__ __forceinline__ void store_q(uint8_t* qb, int lane, const uint32_t (&
   }
 }
 
-template <bool kCompressed>
+// kMulti: several new tokens per request (query head qh = head * T + token, a causal mask on the
+// last positions, rows of q / out / lse mapped through query_row); a separate instantiation, so
+// the single-token kernels are compiled exactly as without it.
+template <bool kCompressed, bool kMulti>
 // At most 112 registers per thread (the compiler needs 104 for the compressed variant, without
 // spills): 16 warps then leave room on every SM sub-partition for a merge warp, so the merge grid
 // of the previous call and this grid's CTAs can be resident together.
@@ -607,7 +623,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
                            ? a.dir[static_cast<size_t>(plan_pid[k]) * a.hkv + plan.g]
                            : -1;
       }
-      load_q(a, plan, lane, qv);
+      load_q<kMulti>(a, plan, lane, qv);
     }
   }
   load_lengths<false, C::kThreads>(a, prefix, lens, tid, held_len, plan_early ? lengths_changed : nullptr);
@@ -668,7 +684,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         mbar_arrive(&item_full[buf]);        // release: the tiles can be fetched
       }
       if (d.b >= 0) {
-        if (!d.planned) load_q(a, d, lane, qv);
+        if (!d.planned) load_q<kMulti>(a, d, lane, qv);
         store_q(qbuf + buf * kHeadsPerSlice * kQRowBytes, lane, qv);
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full[buf]);   // release: the q rows
@@ -726,7 +742,10 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
     // k-steps 2j and 2j+1 (rows past the group's heads are zero)
     const uint8_t* qrow = qbuf + (buf * kHeadsPerSlice + gi) * kQRowBytes + 16 * ti;
 
-    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+    float m0 = kMulti ? kNoScore : -CUDART_INF_F, m1 = m0, l0 = 0.f, l1 = 0.f;
+    // several new tokens: the token of column c (query head d.h0 + c) is (d.h0 + c) % T and sees
+    // positions up to causal_lim + token
+    const int causal_lim = kMulti ? lens[d.b] - a.tokens : 0;
     float o[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -841,6 +860,17 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
           keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
           keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
         }
+        if (kMulti) {
+          const int pos = d.t0 + 16 * u + gi;          // this lane's first row; the second is pos + 8
+          if (pos + 8 > causal_lim) {
+            const int ta = causal_lim + (d.h0 + 2 * ti) % a.tokens;
+            const int tb = causal_lim + (d.h0 + 2 * ti + 1) % a.tokens;
+            if (pos > ta) x0 = -CUDART_INF_F;
+            if (pos > tb) x1 = -CUDART_INF_F;
+            if (pos + 8 > ta) x2 = -CUDART_INF_F;
+            if (pos + 8 > tb) x3 = -CUDART_INF_F;
+          }
+        }
         const bool grow = fmaxf(x0, x2) > m0 + kRescaleThreshold || fmaxf(x1, x3) > m1 + kRescaleThreshold;
         if (__any_sync(0xFFFFFFFFu, grow)) {
           float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
@@ -849,7 +879,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, dd));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, dd));
           }
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: token 0 is valid
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: token 0 is valid (kNoScore at least)
           const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
           m0 = mn0;
           m1 = mn1;
@@ -974,8 +1004,9 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         const float lse2 = lsum > 0.f ? M + log2f(lsum) : -CUDART_INF_F;
         const size_t bh = static_cast<size_t>(d.b) * a.hq + d.h0 + hh;
         if (d.single) {
-          *reinterpret_cast<float4*>(a.out + bh * ZF_HEAD_DIM + 4 * lane) = acc;
-          if (lane == 0) a.lse[bh] = lse2 * kLn2;
+          const size_t row = kMulti ? query_row(d.b, d.h0 + hh, a.tokens, a.hq) : bh;
+          *reinterpret_cast<float4*>(a.out + row * ZF_HEAD_DIM + 4 * lane) = acc;
+          if (lane == 0) a.lse[row] = lse2 * kLn2;
         } else {
           const size_t pidx = bh * a.max_chunks + d.c;
           *reinterpret_cast<float4*>(a.part_o + pidx * ZF_HEAD_DIM + 4 * lane) = acc;
@@ -997,7 +1028,7 @@ struct MergeArgs {
   float* out;
   float* lse;
   const int32_t* chunk_counts;
-  int32_t batch, hq, group, slices, max_chunks;
+  int32_t batch, hq, group, slices, max_chunks, tokens;
 };
 
 // One warp per (request, query head): lse = log2 sum_i 2^lse_i, out = sum_i 2^(lse_i - lse) o_i.
@@ -1008,6 +1039,7 @@ struct MergeArgs {
 // SM sub-partition beside four attention warps of at most 112 registers.
 constexpr int kPreload = 8;
 constexpr int kMergeWarps = 2;
+template <bool kMulti>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The next grid (the next call's attention) may launch right away: its CTAs take SMs as this
@@ -1027,7 +1059,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
   for (int j = 0; j < kPreload; ++j)
     pre[j] = j < a.max_chunks ? po[static_cast<size_t>(j) * (ZF_HEAD_DIM / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
   const int nch = a.chunk_counts[(b * (a.hq / a.group) + gq) * a.slices + (h - gq * a.group) / kHeadsPerSlice];
-  float4* outp = reinterpret_cast<float4*>(a.out + static_cast<size_t>(idx) * ZF_HEAD_DIM) + lane;
+  const size_t row = kMulti ? query_row(b, h, a.tokens, a.hq) : static_cast<size_t>(idx);
+  float4* outp = reinterpret_cast<float4*>(a.out + row * ZF_HEAD_DIM) + lane;
   if (nch == 1) return;
   // chunk log-sum-exps, one per lane: max and sum of 2^(lse_i - max) by warp reductions
   float M = lane < nch ? lse_lane : -CUDART_INF_F;
@@ -1036,7 +1069,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
   for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, d));
   if (nch == 0 || M == -CUDART_INF_F) {
     *outp = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane == 0) a.lse[idx] = -CUDART_INF_F;
+    if (lane == 0) a.lse[row] = -CUDART_INF_F;
     return;
   }
   const float w0 = lane < nch ? fast_exp2(lse_lane - M) : 0.f;
@@ -1070,7 +1103,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
   }
   const float inv = __fdividef(1.f, lsum);
   *outp = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lane == 0) a.lse[idx] = (M + fast_log2(lsum)) * kLn2;
+  if (lane == 0) a.lse[row] = (M + fast_log2(lsum)) * kLn2;
 }
 
 // ------------------------------------------------------------------------------- host planner
@@ -1158,7 +1191,7 @@ static size_t plan_workspace(int batch, int hq, int hkv, int page_size, int max_
 // Raise a kernel's dynamic shared-memory limit once per (device, kernel); the limit only grows.
 static zf_status ensure_smem_limit(const void* kernel, int which, size_t bytes) {
   static std::mutex mu;
-  static size_t done[64][2] = {};
+  static size_t done[64][4] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ZF_ERR_CUDA;
   if (dev < 0 || dev >= 64) return ZF_ERR_UNSUPPORTED;
@@ -1187,14 +1220,23 @@ static bool attn_shape_ok(int batch, int hq, int hkv, int max_pages) {
   return static_cast<long long>(batch) * hkv * slices * max_pages < (1ll << 30);
 }
 
+// Query heads as the kernel counts them: every (head, new token) pair of a request is one, so a
+// call with T tokens is planned like a call with T times the heads (and T times the GQA group).
+static bool tokens_ok(int32_t tokens, int32_t hq) {
+  return tokens >= 1 && tokens <= ZF_MAX_TOKENS && static_cast<long long>(hq) * tokens <= INT_MAX / ZF_HEAD_DIM;
+}
+
 template <bool kCompressed>
-static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t batch, int32_t hq,
+static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t batch, int32_t tokens, int32_t hq_in,
                                   const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
                                   float scale, float* out, float* lse, void* workspace, size_t ws_bytes,
                                   void* stream) {
   zf_status st = check_cache(c, kCompressed, true, kCompressed);
   if (st != ZF_OK) return st;
-  if (!attn_shape_ok(batch, hq, c->num_kv_heads, max_pages)) return ZF_ERR_INVALID_ARGUMENT;
+  if (!tokens_ok(tokens, hq_in)) return ZF_ERR_INVALID_ARGUMENT;
+  const int32_t hq = hq_in * tokens;
+  if (!attn_shape_ok(batch, hq_in, c->num_kv_heads, max_pages) || !attn_shape_ok(batch, hq, c->num_kv_heads, max_pages))
+    return ZF_ERR_INVALID_ARGUMENT;
   if (batch == 0) return ZF_OK;
   if (!q || !page_table || !seq_lens || !out || !lse || !workspace) return ZF_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
@@ -1227,6 +1269,7 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   a.hq = hq;
   a.hkv = c->num_kv_heads;
   a.group = hq / c->num_kv_heads;
+  a.tokens = tokens;
   a.slices = p.slices;
   a.page_size = c->page_size;
   a.num_pages = c->num_pages;
@@ -1243,9 +1286,10 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t smem = smem_layout<kCompressed>(batch).total;
-  if ((st = ensure_smem_limit(reinterpret_cast<const void*>(attn_kernel<kCompressed>), kCompressed ? 1 : 0,
-                             smem)) != ZF_OK)
-    return st;
+  const bool multi = tokens > 1;
+  const void* kernel = multi ? reinterpret_cast<const void*>(attn_kernel<kCompressed, true>)
+                             : reinterpret_cast<const void*>(attn_kernel<kCompressed, false>);
+  if ((st = ensure_smem_limit(kernel, (kCompressed ? 1 : 0) + (multi ? 2 : 0), smem)) != ZF_OK) return st;
   // programmatic dependent launch: each kernel may start while its predecessor in the stream
   // drains, and waits for it (griddepcontrol.wait) before touching inputs or the workspace
   cudaLaunchAttribute pdl[1];
@@ -1258,7 +1302,9 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_kernel<kCompressed>, a) != cudaSuccess) return ZF_ERR_CUDA;
+  if ((multi ? cudaLaunchKernelEx(&cfg, attn_kernel<kCompressed, true>, a)
+             : cudaLaunchKernelEx(&cfg, attn_kernel<kCompressed, false>, a)) != cudaSuccess)
+    return ZF_ERR_CUDA;
 
   MergeArgs m{};
   m.part_o = a.part_o;
@@ -1271,12 +1317,15 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   m.group = a.group;
   m.slices = a.slices;
   m.max_chunks = p.max_chunks;
+  m.tokens = tokens;
   const int rows = batch * hq;
   cudaLaunchConfig_t mcfg = cfg;
   mcfg.gridDim = dim3((rows + kMergeWarps - 1) / kMergeWarps);
   mcfg.blockDim = dim3(kMergeWarps * 32);
   mcfg.dynamicSmemBytes = 0;
-  if (cudaLaunchKernelEx(&mcfg, merge_kernel, m) != cudaSuccess) return ZF_ERR_CUDA;
+  if ((multi ? cudaLaunchKernelEx(&mcfg, merge_kernel<true>, m) : cudaLaunchKernelEx(&mcfg, merge_kernel<false>, m)) !=
+      cudaSuccess)
+    return ZF_ERR_CUDA;
   return ZF_OK;
 }
 
@@ -1294,19 +1343,43 @@ extern "C" size_t zf_decode_attn_workspace_size(int32_t batch, int32_t num_q_hea
   return ws > 0 ? ws : 256;
 }
 
+extern "C" size_t zf_decode_attn_multi_workspace_size(int32_t batch, int32_t tokens, int32_t num_q_heads,
+                                                      int32_t num_kv_heads, int32_t page_size,
+                                                      int32_t max_pages_per_req) {
+  if (!tokens_ok(tokens, num_q_heads) || !attn_shape_ok(batch, num_q_heads, num_kv_heads, max_pages_per_req)) return 0;
+  return zf_decode_attn_workspace_size(batch, num_q_heads * tokens, num_kv_heads, page_size, max_pages_per_req);
+}
+
 extern "C" zf_status zf_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch, int32_t num_q_heads,
                                     const int32_t* page_table, int32_t max_pages_per_req, const int32_t* seq_lens,
                                     float softmax_scale, float* out, float* lse, void* workspace,
                                     size_t workspace_bytes, void* stream) {
-  return launch_attention<true>(cache, q, batch, num_q_heads, page_table, max_pages_per_req, seq_lens, softmax_scale,
-                                out, lse, workspace, workspace_bytes, stream);
+  return launch_attention<true>(cache, q, batch, 1, num_q_heads, page_table, max_pages_per_req, seq_lens,
+                                softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t batch, int32_t tokens,
+                                          int32_t num_q_heads, const int32_t* page_table, int32_t max_pages_per_req,
+                                          const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  return launch_attention<true>(cache, q, batch, tokens, num_q_heads, page_table, max_pages_per_req, seq_lens,
+                                softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 extern "C" zf_status zf_dense_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch,
                                           int32_t num_q_heads, const int32_t* page_table, int32_t max_pages_per_req,
                                           const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
                                           void* workspace, size_t workspace_bytes, void* stream) {
-  return launch_attention<false>(cache, q, batch, num_q_heads, page_table, max_pages_per_req, seq_lens,
+  return launch_attention<false>(cache, q, batch, 1, num_q_heads, page_table, max_pages_per_req, seq_lens,
+                                 softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" zf_status zf_dense_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t batch,
+                                                int32_t tokens, int32_t num_q_heads, const int32_t* page_table,
+                                                int32_t max_pages_per_req, const int32_t* seq_lens,
+                                                float softmax_scale, float* out, float* lse, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+  return launch_attention<false>(cache, q, batch, tokens, num_q_heads, page_table, max_pages_per_req, seq_lens,
                                  softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
@@ -1353,6 +1426,6 @@ extern "C" zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t
   if (p.ws_bytes > ZF_STATIC_WORKSPACE_BYTES) return ZF_ERR_STATIC_WORKSPACE_EXCEEDED;
   void* ws = nullptr;
   if ((st = static_workspace_address(&ws)) != ZF_OK) return st;
-  return launch_attention<true>(cache, q, batch, num_q_heads, page_table, max_pages_per_req, seq_lens,
+  return launch_attention<true>(cache, q, batch, 1, num_q_heads, page_table, max_pages_per_req, seq_lens,
                                 softmax_scale, out, lse, ws, ZF_STATIC_WORKSPACE_BYTES, stream);
 }

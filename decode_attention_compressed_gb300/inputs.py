@@ -100,6 +100,15 @@ def _bits(x: torch.Tensor) -> torch.Tensor:
     return x.to(torch.bfloat16).view(torch.int16)
 
 
+def make_multi_queries(w: Workload, tokens: int, layer: int = 0, device="cpu") -> torch.Tensor:
+    """Queries of `tokens` new tokens per request, N(0, 1) cast to BF16: [batch][tokens][q heads][128]
+    BF16 bits (int16)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed * 1000 + 500 + layer)
+    return _bits(torch.randn(w.batch, tokens, w.num_q_heads, HEAD_DIM, generator=gen, device=dev))
+
+
 def make_layer(w: Workload, layer: int = 0, device="cpu", seq_lens=None) -> LayerInputs:
     """Generate one layer's pages, page table and query for workload `w`."""
     dev = torch.device(device)

@@ -52,6 +52,13 @@ SIGNATURES = {
                                         _c_void_p]),
     "zf_decode_attn_static": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_void_p,
                                          _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p]),
+    "zf_decode_attn_multi_workspace_size": (_c_size_t, [_c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32]),
+    "zf_decode_attn_multi": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
+                                        _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p,
+                                        _c_size_t, _c_void_p]),
+    "zf_dense_decode_attn_multi": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
+                                              _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
+                                              _c_void_p, _c_size_t, _c_void_p]),
 }
 
 _LIB = None
@@ -220,6 +227,35 @@ def decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse
 
 def dense_decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, **kw):
     return decode_attn(cache, q, page_table, seq_lens, scale, dense=True, **kw)
+
+
+def workspace_size_multi(batch, tokens, num_q_heads, num_kv_heads, page_size, max_pages) -> int:
+    return int(lib().zf_decode_attn_multi_workspace_size(batch, tokens, num_q_heads, num_kv_heads, page_size,
+                                                         max_pages))
+
+
+def decode_attn_multi(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse=None, workspace=None,
+                      stream=None, dense=False):
+    """zf_decode_attn_multi: T new tokens per request.  q [B][T][Hq][128] int16 (BF16 bits); token t
+    of request b attends to positions 0 .. seq_lens[b] - T + t.  Returns (out [B][T][Hq][128] f32,
+    lse [B][T][Hq] f32).  dense=True runs zf_dense_decode_attn_multi."""
+    B, T, Hq, _ = q.shape
+    max_pages = int(page_table.shape[1])
+    scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else scale
+    dev = cache.device
+    if out is None:
+        out = torch.empty((B, T, Hq, HEAD_DIM), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(workspace_size_multi(B, T, Hq, cache.num_kv_heads, cache.page_size, max_pages), dev)
+    d = cache.desc()
+    name = "zf_dense_decode_attn_multi" if dense else "zf_decode_attn_multi"
+    code = getattr(lib(), name)(ctypes.byref(d), _ptr(q), B, T, Hq, _ptr(page_table), max_pages, _ptr(seq_lens),
+                                scale, _ptr(out), _ptr(lse), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(name, code)
+    return out, lse
 
 
 STATIC_WORKSPACE_BYTES = 32 << 20

@@ -81,6 +81,7 @@ typedef int32_t zf_status;
 #define ZF_DIR_COMPRESSED (-1)
 #define ZF_DIR_INVALID (-2)
 #define ZF_MAX_BATCH 4096              /* requests per zf_decode_attn call */
+#define ZF_MAX_TOKENS 64               /* new tokens per request in zf_decode_attn_multi */
 #define ZF_MAX_PAGE_SIZE 128
 
 #define ZF_ENCODE_FORCE_RAW 1          /* zf_encode_pages flag: store every page raw */
@@ -186,6 +187,32 @@ zf_status zf_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch
                          const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes zf_decode_attn_multi / zf_dense_decode_attn_multi need (0 on invalid sizes). */
+size_t zf_decode_attn_multi_workspace_size(int32_t batch, int32_t tokens, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t page_size,
+                                           int32_t max_pages_per_req);
+
+/*
+ * zf_decode_attn_multi — decode attention for `tokens` (T) new tokens per request at once
+ * (speculative verification, multi-token decode).  The pages treat one new token per step; this
+ * call takes the plain causal reading of several: the T tokens of request b sit at positions
+ * L-T .. L-1 (L = seq_lens[b]; their keys and values are already in the cache) and token t
+ * attends to positions 0 .. L-T+t, exactly as zf_decode_attn over that prefix would.
+ *   q:   [batch][T][num_q_heads][128] BF16.
+ *   out: [batch][T][num_q_heads][128] float32;  lse: [batch][T][num_q_heads] float32.
+ *   1 <= T <= ZF_MAX_TOKENS.  A token that sees no position (L - T + t < 0) gets out = 0 and
+ *   lse = -inf.  The (head, token) pairs of one kv head are computed like a GQA group T times
+ *   larger: the 8 columns of a tensor-core tile take 8 of them, and each group of 8 reads the kv
+ *   head's K/V tiles once, so the bytes read do not grow with T while (q heads per kv head) x T
+ *   <= 8 (MHA up to 8 tokens, GQA-4 up to 2) and grow by one read per further 8.  Other arguments,
+ *   workspace and ordering as zf_decode_attn (workspace: zf_decode_attn_multi_workspace_size).
+ *   T = 1 is zf_decode_attn.
+ */
+zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t batch, int32_t tokens,
+                               int32_t num_q_heads, const int32_t* page_table, int32_t max_pages_per_req,
+                               const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * zf_dense_decode_attn — the same decode attention over an uncompressed BF16 paged cache: page
  * id p of the page table is read from raw slot p of cache->k_raw / cache->v_raw (raw block
@@ -199,6 +226,13 @@ zf_status zf_dense_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t
                                int32_t max_pages_per_req, const int32_t* seq_lens,
                                float softmax_scale, float* out, float* lse, void* workspace,
                                size_t workspace_bytes, void* stream);
+
+/* zf_dense_decode_attn_multi — zf_decode_attn_multi over the uncompressed cache (the comparator). */
+zf_status zf_dense_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t batch,
+                                     int32_t tokens, int32_t num_q_heads, const int32_t* page_table,
+                                     int32_t max_pages_per_req, const int32_t* seq_lens,
+                                     float softmax_scale, float* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, void* stream);
 
 /*
  * zf_decode_attn_static — zf_decode_attn for callers that cannot allocate device memory.

@@ -119,3 +119,19 @@ def test_python_binding_has_no_fallback(zf, monkeypatch, tmp_path):
     monkeypatch.setattr(zf, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(zf.ZfError):
         zf.lib()
+
+
+@pytest.mark.parametrize("dense", [False, True])
+def test_multi_token_attention_rejects_bad_token_counts(zf, dense):
+    d = _desc(zf)
+    f = zf.lib().zf_dense_decode_attn_multi if dense else zf.lib().zf_decode_attn_multi
+
+    def call(tokens, hq=8):
+        return f(ctypes.byref(d), 0x10000, 2, tokens, hq, 0x50000, 4, 0x60000, 0.1, 0x20000, 0x30000, 0x40000,
+                 1 << 20, None)
+    assert call(0) == -1
+    assert call(-3) == -1
+    assert call(65) == -1                                            # above ZF_MAX_TOKENS
+    assert call(2, hq=7) == -1                                       # heads still a multiple of kv heads
+    assert zf.lib().zf_decode_attn_multi_workspace_size(1, 0, 8, 2, 16, 4) == 0
+    assert zf.lib().zf_decode_attn_multi_workspace_size(1, 2, 7, 2, 16, 4) == 0

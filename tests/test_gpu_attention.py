@@ -287,3 +287,67 @@ def test_inputs_written_by_the_preceding_grid_after_it_lets_the_call_start(zf, c
     oc = H.oracle_cache_from(layer, O, force_raw=dense)
     ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q), oc, table_b.numpy(), lens_b.numpy(), layer.scale)
     H.compare_attention(o, l, ref_out, ref_lse)
+
+
+# ---- several new tokens per request (zf_decode_attn_multi): token t of T sees positions up to
+# seq_len - T + t
+MULTI_CASES = {
+    "mha_t4": (W(2, 8, 8, 16, 300, pool="random", seed=41), [300, 77], 4),
+    "gqa4_t2": (W(3, 8, 2, 16, 200, pool="random", seed=42), [200, 33, 17], 2),
+    "gqa4_t3_two_slices": (W(2, 8, 2, 16, 180, seed=43), [180, 90], 3),
+    "gqa7_t2_spikes": (W(2, 14, 2, 16, 250, pool="random", k_sigma=0.7, n_outlier=0, spike_prob=0.02, v_std=0.5,
+                          seed=44), [250, 40], 2),
+    "page64_t8": (W(2, 4, 4, 64, 400, pool="random", seed=45), [400, 129], 8),
+    "tokens_that_see_nothing": (W(3, 4, 2, 16, 10, seed=46), [3, 1, 10], 4),
+    "one_token": (W(2, 8, 2, 16, 100, seed=47), [100, 31], 1),
+}
+
+
+@pytest.mark.parametrize("dense", [False, True])
+@pytest.mark.parametrize("name", sorted(MULTI_CASES))
+def test_multi_token_cases(zf, name, dense):
+    w, lens, T = MULTI_CASES[name]
+    layer = I.make_layer(w, seq_lens=lens)
+    gc = H.gpu_cache_from(layer, zf, force_raw=dense)
+    q = I.make_multi_queries(w, T)
+    dev = torch.device("cuda")
+    out, lse = zf.decode_attn_multi(gc, q.to(dev), layer.page_table.to(dev), layer.seq_lens.to(dev), layer.scale,
+                                    dense=dense)
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    oc = H.oracle_cache_from(layer, O, force_raw=dense)
+    ref_out, ref_lse = O.decode_attention_multi(H.np_bits(q), oc, layer.page_table.numpy(), layer.seq_lens.numpy(),
+                                                layer.scale)
+    H.compare_attention(out, lse, ref_out, ref_lse)
+    if T == 1:   # the same bits as the single-token entry point
+        o1, l1 = zf.decode_attn(gc, q[:, 0].contiguous().to(dev), layer.page_table.to(dev),
+                                layer.seq_lens.to(dev), layer.scale, dense=dense)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, out[:, 0]) and torch.equal(l1, lse[:, 0])
+
+
+def test_multi_token_full_size_sampled(zf):
+    """Four new tokens per request on the LLaMA-7B MHA 8K shape (one layer), in the benchmark's
+    launch configuration; sampled (request, token, head) outputs against the float64 attention."""
+    w = I.WORKLOADS["llama7b_mha_8192"]
+    T = 4
+    layer = I.make_layer(w, layer=0, device="cuda")
+    npg = layer.num_pages
+    gc = zf.Cache(npg, w.num_kv_heads, w.page_size, npg)
+    zf.encode_pages(gc, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, list(range(npg)))
+    q = I.make_multi_queries(w, T, device="cuda")
+    out, lse = zf.decode_attn_multi(gc, q, layer.page_table, layer.seq_lens, layer.scale)
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    picks = [(0, t, h) for t in range(T) for h in (0, 13, 31)]
+    qn, table, lens = H.np_bits(q), layer.page_table.cpu().numpy(), layer.seq_lens.cpu().numpy()
+    ref_out = np.zeros(tuple(out.shape))
+    ref_lse = np.full(tuple(lse.shape), -math.inf)
+    for b, t, h in picks:
+        L = int(lens[b]) - T + t + 1
+        pages = torch.as_tensor(table[b, : -(-L // w.page_size)], dtype=torch.long, device="cuda")
+        K = H.np_bits(layer.k_pages[pages, h].reshape(-1, 128))[:L]
+        V = H.np_bits(layer.v_pages[pages, h].reshape(-1, 128))[:L]
+        ref_out[b, t, h], ref_lse[b, t, h], _ = O.attention_one(O.bf16_to_f64(qn[b, t, h]), O.bf16_to_f64(K),
+                                                                O.bf16_to_f64(V), layer.scale)
+    H.compare_attention(out, lse, ref_out, ref_lse, pairs=picks)

@@ -1,5 +1,6 @@
-// zf_decode_attn / zf_dense_decode_attn: split-KV decode attention over a paged KV cache whose
-// full pages are stored compressed, plus the split-result merge.
+// zf_decode_attn / zf_dense_decode_attn (and their _multi forms for several new tokens per
+// request): split-KV decode attention over a paged KV cache whose full pages are stored
+// compressed, plus the split-result merge.
 //
 // ZipFusion §III.C (Attention over the Compressed KV Cache): compressed blocks are copied
 // HBM -> shared memory as they are, each thread rebuilds the exact BF16 operands of a
@@ -11,8 +12,9 @@
 //  * work split (host planner, from the sizes): either balanced page ranges — the pages of all
 //    (request b, kv head g, head slice) pairs, laid end to end, cut into one equal contiguous range
 //    per CTA, so a ragged batch gives every SM the same number of tiles; where a range meets a
-//    pair it forms that pair's partial(s), cut further into items of at most 256 tiles — or, for
-//    short contexts, fixed chunks of pages dealt round-robin; each item yields one partial;
+//    pair it forms that pair's partial(s), cut further into items of at most 256 pages and 512
+//    tiles — or, for short contexts, fixed chunks of pages dealt round-robin; each item yields
+//    one partial;
 //  * the last warp is the metadata warp: it walks the CTA's items, and runs one item ahead,
 //    resolving the item's page ids through the page table and the directory into shared memory
 //    and staging the item's q rows; an end marker closes the CTA's item stream;

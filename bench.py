@@ -44,13 +44,17 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources the attention kernels are compiled from
+KERNEL_SOURCES = ("zf_attn.cu", "zf_device.cuh", "zf_host.h")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources with comments and blank space removed: a committed ncu capture
-    stays valid across comment-only edits and is dropped when any code changes."""
+    """Hash of the attention kernels' sources with comments and blank space removed: a committed
+    ncu capture stays valid across comment-only edits and is dropped when their code changes."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_compressed_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)

@@ -35,6 +35,16 @@ class ZfCacheDesc(ctypes.Structure):
     ]
 
 
+class ZfKvStats(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int64), ("free_pages", _c_int32), ("free_raw_slots", _c_int32),
+        ("active_requests", _c_int32), ("partial_pages", _c_int32), ("pending_pages", _c_int32),
+        ("raw_full_pages", _c_int32), ("compressed_pages", _c_int32), ("new_page_capacity", _c_int32),
+    ]
+
+
+_P32 = ctypes.POINTER(_c_int32)
+
 # name -> (restype, argtypes), mirroring include/zf.h
 SIGNATURES = {
     "zf_status_string": (ctypes.c_char_p, [_c_int32]),
@@ -59,6 +69,16 @@ SIGNATURES = {
     "zf_dense_decode_attn_multi": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
                                               _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
                                               _c_void_p, _c_size_t, _c_void_p]),
+    "zf_kv_create": (_c_int32, [_c_int32, _c_int32, _c_int32, _c_int32, _c_int32, ctypes.POINTER(_c_void_p)]),
+    "zf_kv_destroy": (None, [_c_void_p]),
+    "zf_kv_admit": (_c_int32, [_c_void_p, _c_int32, _c_int32, _P32, _P32, _P32, _P32]),
+    "zf_kv_append": (_c_int32, [_c_void_p, _P32, _c_int32, _P32, _P32, _P32]),
+    "zf_kv_pending": (_c_int32, [_c_void_p, _P32, _P32, _c_int32, _P32]),
+    "zf_kv_reclaim": (_c_int32, [_c_void_p, _P32, _P32, _c_int32]),
+    "zf_kv_release": (_c_int32, [_c_void_p, _c_int32]),
+    "zf_kv_export": (_c_int32, [_c_void_p, _P32, _P32]),
+    "zf_kv_get_stats": (_c_int32, [_c_void_p, ctypes.POINTER(ZfKvStats)]),
+    "zf_kv_plan_pages": (_c_int32, [ctypes.c_int64, _c_int32, _c_int32, _c_int32, _P32, _P32]),
 }
 
 _LIB = None
@@ -278,3 +298,97 @@ def decode_attn_static(cache: Cache, q, page_table, seq_lens, scale=None, out=No
                                        _ptr(seq_lens), scale, _ptr(out), _ptr(lse), _stream(stream))
     _check("zf_decode_attn_static", code)
     return out, lse
+
+
+# --------------------------------------------------------------------------------- page manager
+ERR_CAPACITY = -6
+
+
+def _i32(values):
+    arr = (_c_int32 * max(len(values), 1))(*values)
+    return arr
+
+
+class KvManager:
+    """zf_kv: host-side page manager (page ids and raw slots shared by all layers).  Each call
+    returns the encode list (page_ids, n_valid, raw_slots) that zf_encode_pages takes."""
+
+    def __init__(self, num_pages, num_raw_slots, page_size, max_requests, max_pages_per_req):
+        self.page_size, self.max_requests, self.max_pages = page_size, max_requests, max_pages_per_req
+        h = _c_void_p()
+        _check("zf_kv_create", lib().zf_kv_create(num_pages, num_raw_slots, page_size, max_requests,
+                                                   max_pages_per_req, ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            lib().zf_kv_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def admit(self, req, length):
+        n_max = -(-length // self.page_size)
+        ids, nv, rs, n = (_c_int32 * max(n_max, 1))(), (_c_int32 * max(n_max, 1))(), (_c_int32 * max(n_max, 1))(), _c_int32()
+        _check("zf_kv_admit", lib().zf_kv_admit(self._h, req, length, ids, nv, rs, ctypes.byref(n)))
+        return list(ids[: n.value]), list(nv[: n.value]), list(rs[: n.value])
+
+    def append(self, reqs):
+        n = len(reqs)
+        ids, nv, rs = (_c_int32 * max(n, 1))(), (_c_int32 * max(n, 1))(), (_c_int32 * max(n, 1))()
+        _check("zf_kv_append", lib().zf_kv_append(self._h, _i32(reqs), n, ids, nv, rs))
+        return list(ids[:n]), list(nv[:n]), list(rs[:n])
+
+    def pending(self):
+        n = _c_int32()
+        code = lib().zf_kv_pending(self._h, None, None, 0, ctypes.byref(n))
+        if code not in (0, -1):
+            _check("zf_kv_pending", code)
+        k = n.value
+        ids, rs = (_c_int32 * max(k, 1))(), (_c_int32 * max(k, 1))()
+        _check("zf_kv_pending", lib().zf_kv_pending(self._h, ids, rs, k, ctypes.byref(n)))
+        return list(ids[:k]), list(rs[:k])
+
+    def reclaim(self, page_ids, kept_raw):
+        _check("zf_kv_reclaim", lib().zf_kv_reclaim(self._h, _i32(page_ids), _i32([int(bool(x)) for x in kept_raw]),
+                                                    len(page_ids)))
+
+    def reclaim_from(self, caches):
+        """Reclaim every pending page from the directories of `caches` (one per layer): a page keeps
+        its raw slot if any page-head of it is stored raw in any of them."""
+        ids, _ = self.pending()
+        if not ids:
+            return 0
+        idx = torch.as_tensor(ids, dtype=torch.long)
+        kept = torch.zeros(len(ids), dtype=torch.bool)
+        for c in caches:
+            kept |= (c.dir.index_select(0, idx.to(c.dir.device)).cpu() >= 0).any(dim=1)
+        self.reclaim(ids, kept.tolist())
+        return len(ids)
+
+    def release(self, req):
+        _check("zf_kv_release", lib().zf_kv_release(self._h, req))
+
+    def export(self):
+        table = (_c_int32 * (self.max_requests * self.max_pages))()
+        lens = (_c_int32 * self.max_requests)()
+        _check("zf_kv_export", lib().zf_kv_export(self._h, table, lens))
+        t = torch.tensor(list(table), dtype=torch.int32).reshape(self.max_requests, self.max_pages)
+        return t, torch.tensor(list(lens), dtype=torch.int32)
+
+    def stats(self) -> dict:
+        st = ZfKvStats()
+        _check("zf_kv_get_stats", lib().zf_kv_get_stats(self._h, ctypes.byref(st)))
+        return {name: getattr(st, name) for name, _ in ZfKvStats._fields_}
+
+
+def kv_plan_pages(bytes_per_layer, num_kv_heads, page_size, num_raw_slots):
+    """(page ids, dense pages) that bytes_per_layer holds (zf_kv_plan_pages)."""
+    a, b = _c_int32(), _c_int32()
+    _check("zf_kv_plan_pages", lib().zf_kv_plan_pages(int(bytes_per_layer), num_kv_heads, page_size, num_raw_slots,
+                                                       ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value

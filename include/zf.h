@@ -62,6 +62,7 @@ typedef int32_t zf_status;
 #define ZF_ERR_WORKSPACE_TOO_SMALL (-3)
 #define ZF_ERR_CUDA (-4)               /* a CUDA runtime call failed (launch or attribute) */
 #define ZF_ERR_STATIC_WORKSPACE_EXCEEDED (-5) /* zf_decode_attn_static: sizes need more than ZF_STATIC_WORKSPACE_BYTES */
+#define ZF_ERR_CAPACITY (-6)           /* zf_kv: not enough free page ids or raw slots; nothing changed */
 
 /* Bits of the device status word (zf_cache.status). */
 #define ZF_DEV_BAD_PAGE_ID 0x1         /* page id outside [0, num_pages) */
@@ -259,6 +260,82 @@ zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t* q, int32_
                                 int32_t num_q_heads, const int32_t* page_table,
                                 int32_t max_pages_per_req, const int32_t* seq_lens,
                                 float softmax_scale, float* out, float* lse, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * zf_kv — host-side page manager for the caches above.  ZipFusion §III.D (KV Cache Management and
+ * Scheduling): a page stays uncompressed while it fills so that tokens can be appended in place,
+ * a full page is compressed afterwards and keeps its page id, new pages must accept writes before
+ * compression (so capacity for them is counted in uncompressed storage) and capacity grows back as
+ * compression releases that storage.  §II.C (Compression for Higher Serving Capacity): the
+ * storage compression frees is what lets more requests in.
+ * A page id names one compressed slot in every layer's cache, a raw slot one uncompressed page in
+ * every layer's raw pool (all layers use the same ids and slots, sized alike).  Every page being
+ * written holds a raw slot: a request's partial last page while it fills, a full page until the
+ * caller reports, from the directory, whether its encode compressed it (zf_kv_reclaim): a page
+ * whose page-heads all compressed returns its raw slot, one with any page-head left raw (more
+ * than six escapes in a block) keeps it until its request is released.  The manager only does
+ * the bookkeeping: the caller writes the listed pages with zf_encode_pages (whose page_ids,
+ * n_valid and raw_slots arrays the calls below fill) and uploads the page table and lengths.
+ * Host code; not thread-safe; no GPU calls.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct zf_kv zf_kv;
+
+typedef struct zf_kv_stats {
+  int64_t tokens;             /* tokens held by active requests */
+  int32_t free_pages;         /* page ids not held */
+  int32_t free_raw_slots;     /* raw slots not held */
+  int32_t active_requests;
+  int32_t partial_pages;      /* last pages still filling (each holds a raw slot) */
+  int32_t pending_pages;      /* full pages whose raw slot awaits zf_kv_reclaim */
+  int32_t raw_full_pages;     /* full pages left raw by their encode (raw slot held) */
+  int32_t compressed_pages;   /* full pages stored compressed (no raw slot) */
+  int32_t new_page_capacity;  /* pages that can be opened now: min(free ids, free raw slots) */
+} zf_kv_stats;
+
+/* A manager for num_pages page ids and num_raw_slots raw slots, pages of page_size tokens, request
+ * slots 0 .. max_requests-1 of at most max_pages_per_req pages each.  *out = NULL on error. */
+zf_status zf_kv_create(int32_t num_pages, int32_t num_raw_slots, int32_t page_size, int32_t max_requests,
+                       int32_t max_pages_per_req, zf_kv** out);
+void zf_kv_destroy(zf_kv* kv);
+
+/* Admit request slot `req` (inactive) with a prompt of `len` tokens: takes ceil(len / page_size)
+ * page ids and as many raw slots (every page is written uncompressed first) and writes the
+ * encode list for the prompt — page_ids / n_valid / raw_slots, *n entries — in page order.
+ * ZF_ERR_CAPACITY when the pool cannot hold it. */
+zf_status zf_kv_admit(zf_kv* kv, int32_t req, int32_t len, int32_t* page_ids, int32_t* n_valid,
+                      int32_t* raw_slots, int32_t* n);
+
+/* One new token for each of the n distinct active requests reqs[i]: entry i of the outputs is the
+ * page that holds it (page id, tokens in it, raw slot) — one zf_encode_pages call writes them all.
+ * A request whose last page is full opens a new page (id + raw slot) first; a page that becomes
+ * full here is compressed by that encode and its raw slot is pending until zf_kv_reclaim.  All or
+ * nothing: ZF_ERR_CAPACITY (or an invalid request) changes no request. */
+zf_status zf_kv_append(zf_kv* kv, const int32_t* reqs, int32_t n, int32_t* page_ids, int32_t* n_valid,
+                       int32_t* raw_slots);
+
+/* Full pages whose raw slot is pending, ascending page id: up to `capacity` (page id, raw slot)
+ * pairs; *n = their total count (ZF_ERR_INVALID_ARGUMENT when it exceeds capacity). */
+zf_status zf_kv_pending(const zf_kv* kv, int32_t* page_ids, int32_t* raw_slots, int32_t capacity, int32_t* n);
+
+/* After the encodes of these pending pages have run: kept_raw[i] != 0 when any page-head of
+ * page_ids[i], in any layer, is stored raw (directory entry >= 0); those keep their raw slot, the
+ * others return it to the pool.  Every id must be pending, with no repeats. */
+zf_status zf_kv_reclaim(zf_kv* kv, const int32_t* page_ids, const int32_t* kept_raw, int32_t n);
+
+/* Return request `req`'s page ids and raw slots to the pools. */
+zf_status zf_kv_release(zf_kv* kv, int32_t req);
+
+/* page_table [max_requests][max_pages_per_req] (-1 past a request's pages) and seq_lens
+ * [max_requests] (0 for inactive slots), host arrays, as zf_decode_attn takes them. */
+zf_status zf_kv_export(const zf_kv* kv, int32_t* page_table, int32_t* seq_lens);
+
+zf_status zf_kv_get_stats(const zf_kv* kv, zf_kv_stats* out);
+
+/* Sizing: page ids a layer's cache of bytes_per_layer holds next to num_raw_slots raw slots
+ * (compressed K and V slots plus directory entries per page id), and the pages the same bytes
+ * hold as a dense BF16 cache. */
+zf_status zf_kv_plan_pages(int64_t bytes_per_layer, int32_t num_kv_heads, int32_t page_size,
+                           int32_t num_raw_slots, int32_t* num_pages, int32_t* dense_pages);
 
 #ifdef __cplusplus
 }

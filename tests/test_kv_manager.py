@@ -1,0 +1,195 @@
+"""zf_kv, the host-side page manager (CPU only: bookkeeping, no GPU calls).
+
+ZipFusion §III.D: pages stay uncompressed while they fill, a full page is compressed afterwards
+under its page id, and new pages are counted in uncompressed storage until compression releases
+it.  The checks below restate those rules as invariants of the manager's state and run a random
+workload against a plain Python model of the same rules."""
+import random
+
+import pytest
+
+from tests import helpers as H
+
+
+@pytest.fixture(scope="module")
+def zf():
+    return H.zf_module()
+
+
+P = 16
+
+
+def test_admit_lists_every_page_for_an_uncompressed_first_write(zf):
+    kv = zf.KvManager(num_pages=10, num_raw_slots=10, page_size=P, max_requests=4, max_pages_per_req=8)
+    ids, nv, rs = kv.admit(0, 37)
+    assert ids == [0, 1, 2] and nv == [16, 16, 5] and rs == [0, 1, 2]
+    st = kv.stats()
+    assert (st["free_pages"], st["free_raw_slots"], st["pending_pages"], st["partial_pages"]) == (7, 7, 2, 1)
+    assert st["tokens"] == 37 and st["new_page_capacity"] == 7
+    table, lens = kv.export()
+    assert table[0, :4].tolist() == [0, 1, 2, -1] and lens.tolist() == [37, 0, 0, 0]
+    # the two full pages are reported compressed: their raw slots come back
+    pend, slots = kv.pending()
+    assert pend == [0, 1] and slots == [0, 1]
+    kv.reclaim(pend, [False, False])
+    st = kv.stats()
+    assert (st["free_raw_slots"], st["pending_pages"], st["compressed_pages"]) == (9, 0, 2)
+
+
+def test_append_fills_the_tail_then_opens_a_new_page(zf):
+    kv = zf.KvManager(num_pages=6, num_raw_slots=3, page_size=P, max_requests=2, max_pages_per_req=6)
+    kv.admit(0, 14)                                   # one partial page, raw slot 0
+    for expect_fill in (15, 16):
+        ids, nv, rs = kv.append([0])
+        assert ids == [0] and nv == [expect_fill] and rs == [0]
+    assert kv.stats()["pending_pages"] == 1 and kv.stats()["partial_pages"] == 0
+    ids, nv, rs = kv.append([0])                       # token 17 opens page 1 with a new raw slot
+    assert ids == [1] and nv == [1] and rs == [1]
+    kv.reclaim([0], [True])                            # page 0 stayed raw: keeps slot 0
+    st = kv.stats()
+    assert st["raw_full_pages"] == 1 and st["free_raw_slots"] == 1
+    kv.release(0)
+    st = kv.stats()
+    assert (st["free_pages"], st["free_raw_slots"], st["active_requests"], st["tokens"]) == (6, 3, 0, 0)
+
+
+def test_capacity_refusals_change_nothing(zf):
+    kv = zf.KvManager(num_pages=5, num_raw_slots=3, page_size=P, max_requests=3, max_pages_per_req=4)
+    kv.admit(0, 32)                                    # 2 ids, 2 raw slots (pending)
+    before = kv.stats()
+    with pytest.raises(zf.ZfError, match="page ids or raw slots"):
+        kv.admit(1, 40)                                # 3 pages but 1 raw slot free
+    assert kv.stats() == before and kv.export()[1][1] == 0
+    kv.admit(1, 16)                                    # exactly one page: fits
+    with pytest.raises(zf.ZfError, match="page ids or raw slots"):
+        kv.append([0, 1])                              # both open a page: 2 ids free, no raw slot
+    assert kv.stats()["tokens"] == 48
+    ids, _ = kv.pending()
+    kv.reclaim(ids, [False] * len(ids))                # compression releases uncompressed storage
+    ids, nv, rs = kv.append([0, 1])
+    assert nv == [1, 1] and len(set(rs)) == 2
+
+
+def test_invalid_calls_are_refused(zf):
+    kv = zf.KvManager(num_pages=4, num_raw_slots=4, page_size=P, max_requests=2, max_pages_per_req=2)
+    kv.admit(0, 5)
+    with pytest.raises(zf.ZfError):
+        kv.admit(0, 5)                                 # slot already active
+    with pytest.raises(zf.ZfError):
+        kv.admit(1, 33)                                # more pages than a request may hold
+    with pytest.raises(zf.ZfError):
+        kv.append([1])                                 # inactive request
+    with pytest.raises(zf.ZfError):
+        kv.append([0, 0])                              # the same request twice
+    with pytest.raises(zf.ZfError):
+        kv.reclaim([0], [False])                       # page 0 is partial, not pending
+    with pytest.raises(zf.ZfError):
+        kv.release(1)
+
+
+def test_plan_pages_counts_compressed_and_dense_storage(zf):
+    # one layer, 8 kv heads, 16-token pages: a dense page is 2 x 8 x 4 x 1024 B; a page id costs
+    # 2 x 8 x 4 x 784 B of slots + 8 directory entries
+    dense_page = 2 * 8 * 4 * 1024
+    comp_page = 2 * 8 * 4 * 784 + 8 * 4
+    pages, dense = zf.kv_plan_pages(1000 * dense_page, 8, 16, 100)
+    assert dense == 1000
+    assert pages == (1000 - 100) * dense_page // comp_page
+    assert 1.15 < pages / (dense - 100) < 1.31
+
+
+def test_random_workload_against_a_model(zf):
+    """Random admits, appends, reclaims and releases; after every call the manager's exported
+    table, lengths and counts match a plain model of the rules and no id or slot is held twice."""
+    rng = random.Random(5)
+    NP, NR, R, MP = 60, 24, 6, 12
+    kv = zf.KvManager(num_pages=NP, num_raw_slots=NR, page_size=P, max_requests=R, max_pages_per_req=MP)
+    model = {}                 # req -> dict(len, pages, tail_raw)
+    raw_kept = {}              # pid -> slot, full pages left raw
+    pending = {}               # pid -> slot
+
+    def held_slots():
+        s = [m["tail_raw"] for m in model.values() if m["tail_raw"] is not None]
+        return s + list(pending.values()) + list(raw_kept.values())
+
+    for step in range(600):
+        op = rng.random()
+        free_ids = NP - sum(len(m["pages"]) for m in model.values())
+        free_raw = NR - len(held_slots())
+        if op < 0.2 and len(model) < R:
+            req = rng.choice([q for q in range(R) if q not in model])
+            length = rng.randint(0, 70)
+            need = -(-length // P)
+            if need > MP:
+                continue
+            if need > min(free_ids, free_raw):
+                with pytest.raises(zf.ZfError, match="page ids or raw slots"):
+                    kv.admit(req, length)
+                continue
+            ids, nv, rs = kv.admit(req, length)
+            assert nv == [min(P, length - i * P) for i in range(need)]
+            m = {"len": length, "pages": ids, "tail_raw": None}
+            for pid, fill, slot in zip(ids, nv, rs):
+                if fill == P:
+                    pending[pid] = slot
+                else:
+                    m["tail_raw"] = slot
+            model[req] = m
+        elif op < 0.7 and model:
+            reqs = rng.sample(sorted(model), rng.randint(1, len(model)))
+            opening = [q for q in reqs if model[q]["len"] % P == 0]
+            if any(-(-model[q]["len"] // P) + 1 > MP for q in opening):
+                continue
+            if len(opening) > min(free_ids, free_raw):
+                with pytest.raises(zf.ZfError, match="page ids or raw slots"):
+                    kv.append(reqs)
+                continue
+            ids, nv, rs = kv.append(reqs)
+            for q, pid, fill, slot in zip(reqs, ids, nv, rs):
+                m = model[q]
+                if m["len"] % P == 0:
+                    assert pid not in m["pages"]
+                    m["pages"].append(pid)
+                else:
+                    assert slot == m["tail_raw"] and pid == m["pages"][-1]
+                m["len"] += 1
+                assert fill == m["len"] - (len(m["pages"]) - 1) * P
+                if fill == P:
+                    pending[pid] = slot
+                    m["tail_raw"] = None
+                else:
+                    m["tail_raw"] = slot
+        elif op < 0.85 and pending:
+            ids, slots = kv.pending()
+            assert dict(zip(ids, slots)) == pending
+            pick = rng.sample(ids, rng.randint(1, len(ids)))
+            kept = [rng.random() < 0.1 for _ in pick]
+            kv.reclaim(pick, kept)
+            for pid, k in zip(pick, kept):
+                slot = pending.pop(pid)
+                if k:
+                    raw_kept[pid] = slot
+        elif model:
+            req = rng.choice(sorted(model))
+            kv.release(req)
+            for pid in model.pop(req)["pages"]:
+                pending.pop(pid, None)
+                raw_kept.pop(pid, None)
+        # compare
+        table, lens = kv.export()
+        for q in range(R):
+            if q in model:
+                m = model[q]
+                assert lens[q] == m["len"]
+                row = table[q].tolist()
+                assert row[: len(m["pages"])] == m["pages"] and all(x == -1 for x in row[len(m["pages"]):])
+            else:
+                assert lens[q] == 0 and (table[q] == -1).all()
+        all_ids = [p for m in model.values() for p in m["pages"]]
+        assert len(all_ids) == len(set(all_ids))
+        slots = held_slots()
+        assert len(slots) == len(set(slots)) and all(0 <= s < NR for s in slots)
+        st = kv.stats()
+        assert st["free_pages"] == NP - len(all_ids) and st["free_raw_slots"] == NR - len(slots)
+        assert st["pending_pages"] == len(pending) and st["raw_full_pages"] == len(raw_kept)
+        assert st["tokens"] == sum(m["len"] for m in model.values())

@@ -35,6 +35,9 @@ struct zf_kv {
   std::vector<int32_t> held_raw;        // per page id: raw slot it holds while full, -1 if none
   std::vector<uint8_t> pending;         // per page id: full, raw slot held until the caller reclaims
   std::vector<uint8_t> kept;            // per page id: full and left raw by its encode
+  std::vector<int32_t> pending_ids;     // the pending page ids, unordered
+  std::vector<int32_t> pending_at;      // per page id: its index in pending_ids, -1 if not pending
+  int32_t kept_count = 0;
 };
 
 namespace {
@@ -49,10 +52,28 @@ int32_t take(std::vector<int32_t>& stack) {
   return v;
 }
 
+void set_pending(zf_kv* kv, int32_t pid, int32_t slot) {
+  kv->held_raw[pid] = slot;
+  kv->pending[pid] = 1;
+  kv->pending_at[pid] = static_cast<int32_t>(kv->pending_ids.size());
+  kv->pending_ids.push_back(pid);
+}
+
+void clear_pending(zf_kv* kv, int32_t pid) {
+  if (!kv->pending[pid]) return;
+  const int32_t at = kv->pending_at[pid], last = kv->pending_ids.back();
+  kv->pending_ids[at] = last;
+  kv->pending_at[last] = at;
+  kv->pending_ids.pop_back();
+  kv->pending_at[pid] = -1;
+  kv->pending[pid] = 0;
+}
+
 void give_back_raw(zf_kv* kv, int32_t pid) {
   if (kv->held_raw[pid] >= 0) kv->free_raw.push_back(kv->held_raw[pid]);
   kv->held_raw[pid] = -1;
-  kv->pending[pid] = 0;
+  clear_pending(kv, pid);
+  if (kv->kept[pid]) --kv->kept_count;
   kv->kept[pid] = 0;
 }
 
@@ -80,6 +101,7 @@ extern "C" zf_status zf_kv_create(int32_t num_pages, int32_t num_raw_slots, int3
   kv->held_raw.assign(num_pages, -1);
   kv->pending.assign(num_pages, 0);
   kv->kept.assign(num_pages, 0);
+  kv->pending_at.assign(num_pages, -1);
   *out = kv;
   return ZF_OK;
 }
@@ -106,8 +128,7 @@ extern "C" zf_status zf_kv_admit(zf_kv* kv, int32_t req, int32_t len, int32_t* p
     kv->owner[pid] = req;
     r.pages.push_back(pid);
     if (fill == kv->page_size) {
-      kv->held_raw[pid] = slot;
-      kv->pending[pid] = 1;
+      set_pending(kv, pid, slot);
     } else {
       r.tail_raw = slot;
     }
@@ -151,8 +172,7 @@ extern "C" zf_status zf_kv_append(zf_kv* kv, const int32_t* reqs, int32_t n, int
     n_valid[i] = fill;
     raw_slots[i] = r.tail_raw;
     if (fill == kv->page_size) {                            // full: compressed by this encode
-      kv->held_raw[pid] = r.tail_raw;
-      kv->pending[pid] = 1;
+      set_pending(kv, pid, r.tail_raw);
       r.tail_raw = -1;
     }
   }
@@ -162,17 +182,16 @@ extern "C" zf_status zf_kv_append(zf_kv* kv, const int32_t* reqs, int32_t n, int
 extern "C" zf_status zf_kv_pending(const zf_kv* kv, int32_t* page_ids, int32_t* raw_slots, int32_t capacity,
                                    int32_t* n) {
   if (!kv || !n || capacity < 0 || (capacity > 0 && (!page_ids || !raw_slots))) return ZF_ERR_INVALID_ARGUMENT;
-  int32_t k = 0;
-  for (int32_t pid = 0; pid < kv->num_pages; ++pid) {
-    if (!kv->pending[pid]) continue;
-    if (k < capacity) {
-      page_ids[k] = pid;
-      raw_slots[k] = kv->held_raw[pid];
-    }
-    ++k;
-  }
+  const int32_t k = static_cast<int32_t>(kv->pending_ids.size());
   *n = k;
-  return k <= capacity ? ZF_OK : ZF_ERR_INVALID_ARGUMENT;
+  if (k > capacity) return ZF_ERR_INVALID_ARGUMENT;
+  std::vector<int32_t> ids(kv->pending_ids);
+  std::sort(ids.begin(), ids.end());
+  for (int32_t i = 0; i < k; ++i) {
+    page_ids[i] = ids[i];
+    raw_slots[i] = kv->held_raw[ids[i]];
+  }
+  return ZF_OK;
 }
 
 extern "C" zf_status zf_kv_reclaim(zf_kv* kv, const int32_t* page_ids, const int32_t* kept_raw, int32_t n) {
@@ -186,8 +205,9 @@ extern "C" zf_status zf_kv_reclaim(zf_kv* kv, const int32_t* page_ids, const int
   for (int32_t i = 0; i < n; ++i) {
     const int32_t pid = page_ids[i];
     if (kept_raw[i]) {
-      kv->pending[pid] = 0;
+      clear_pending(kv, pid);
       kv->kept[pid] = 1;
+      ++kv->kept_count;
     } else {
       give_back_raw(kv, pid);
     }
@@ -231,12 +251,9 @@ extern "C" zf_status zf_kv_get_stats(const zf_kv* kv, zf_kv_stats* out) {
     s.tokens += r.len;
     if (r.tail_raw >= 0) ++s.partial_pages;
   }
-  int32_t owned = 0;
-  for (const zf_kv::Request& r : kv->reqs) owned += static_cast<int32_t>(r.pages.size());
-  for (int32_t pid = 0; pid < kv->num_pages; ++pid) {
-    if (kv->pending[pid]) ++s.pending_pages;
-    if (kv->kept[pid]) ++s.raw_full_pages;
-  }
+  const int32_t owned = kv->num_pages - s.free_pages;
+  s.pending_pages = static_cast<int32_t>(kv->pending_ids.size());
+  s.raw_full_pages = kv->kept_count;
   s.compressed_pages = owned - s.partial_pages - s.pending_pages - s.raw_full_pages;
   // new pages are written uncompressed first: each needs a page id and a raw slot
   s.new_page_capacity = std::min(s.free_pages, s.free_raw_slots);

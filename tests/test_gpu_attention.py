@@ -256,17 +256,20 @@ def test_back_to_back_calls_with_inputs_changed_between_them(zf):
     assert torch.equal(outs[0][0], outs[2][0]) and torch.equal(outs[0][1], outs[2][1])
 
 
+@pytest.mark.parametrize("tokens", [1, 4])
 @pytest.mark.parametrize("dense", [False, True])
 @pytest.mark.parametrize("change", ["lengths_and_table", "table_only", "nothing"])
-def test_inputs_written_by_the_preceding_grid_after_it_lets_the_call_start(zf, change, dense):
+def test_inputs_written_by_the_preceding_grid_after_it_lets_the_call_start(zf, change, dense, tokens):
     """A kernel ahead of the call lets it start at once and rewrites the page table (and lengths)
     about 200 us later: the call plans its first item from the old values while that kernel runs,
-    and must compute from the new ones (the plan is dropped when anything it read has changed)."""
+    and must compute from the new ones (the plan is dropped when anything it read has changed).
+    With four new tokens per request the same holds for zf_decode_attn_multi."""
     w = W(2, 32, 32, 16, 2048, pool="random", seed=29)
     layer = I.make_layer(w, seq_lens=[2048, 2048])
     gc = H.gpu_cache_from(layer, zf, force_raw=dense)
     dev = torch.device("cuda")
-    q = layer.q.to(dev)
+    q_host = I.make_multi_queries(w, tokens) if tokens > 1 else layer.q
+    q = q_host.to(dev)
     table_a, lens_a = layer.page_table.clone(), layer.seq_lens.clone()
     table_b, lens_b = table_a.clone(), lens_a.clone()
     if change != "nothing":
@@ -275,17 +278,20 @@ def test_inputs_written_by_the_preceding_grid_after_it_lets_the_call_start(zf, c
         lens_b = torch.tensor([1500, 77], dtype=lens_a.dtype)
     table_dev, lens_dev = table_a.to(dev), lens_a.to(dev)
     new_table, new_lens = table_b.to(dev), lens_b.to(dev)
-    ws = zf.new_workspace(zf.workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.page_size, w.max_pages))
+    ws = zf.new_workspace(zf.workspace_size_multi(w.batch, tokens, w.num_q_heads, w.num_kv_heads, w.page_size,
+                                                  w.max_pages))
     late_copy = H.late_writer()
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     assert late_copy(new_table.data_ptr(), table_dev.data_ptr(), table_dev.numel(), new_lens.data_ptr(),
                      lens_dev.data_ptr(), lens_dev.numel(), 200_000, stream.cuda_stream) == 0
-    o, l = zf.decode_attn(gc, q, table_dev, lens_dev, layer.scale, workspace=ws, dense=dense)
+    call = zf.decode_attn_multi if tokens > 1 else zf.decode_attn
+    o, l = call(gc, q, table_dev, lens_dev, layer.scale, workspace=ws, dense=dense)
     torch.cuda.synchronize()
     assert gc.status_word() == 0
     oc = H.oracle_cache_from(layer, O, force_raw=dense)
-    ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q), oc, table_b.numpy(), lens_b.numpy(), layer.scale)
+    ref = O.decode_attention_multi if tokens > 1 else O.decode_attention
+    ref_out, ref_lse = ref(H.np_bits(q_host), oc, table_b.numpy(), lens_b.numpy(), layer.scale)
     H.compare_attention(o, l, ref_out, ref_lse)
 
 

@@ -7,12 +7,17 @@
 //  * new pages must accept writes before they are compressed, so capacity for new pages is
 //    counted in uncompressed storage, and it grows back as compression releases that storage;
 //  * one logical page needs storage in every layer.
-// Here a page id names one compressed slot in every layer's cache, and a raw slot names one
-// uncompressed page in every layer's raw pool (every layer uses the same ids and slots).  Every
-// page being written holds a raw slot: the partial last page of a request for as long as it
-// fills, and a full page until the caller confirms that its encode compressed it (a page-head
-// whose blocks need more than six escapes stays in its raw slot for good).  Host code only; one
-// manager must not be used from two threads at once.
+// Here a page id names one compressed slot in every layer's cache.  Uncompressed pages live in
+// raw slots drawn from one pool that all layers share (every layer's cache points at the same raw
+// arrays): a page being written holds one raw slot per layer, and once its encodes have run each
+// layer gives its slot back on its own — so storage that compression frees in one layer is
+// reused by any layer, and a page left raw in one layer holds one slot, not one in every layer.
+// A partial last page holds its slots for as long as it fills; a full page holds them until the
+// caller reports, layer by layer, whether the encode compressed it (a page-head whose blocks need
+// more than six escapes stays in its raw slot for good).  With one layer, or with separate
+// per-layer raw pools addressed by the same slot index (a caller that reports a page raw when it
+// is raw in any layer), this is the same bookkeeping for every layer at once.  Host code only;
+// one manager must not be used from two threads at once.
 #include <algorithm>
 #include <cstdint>
 #include <new>
@@ -21,23 +26,24 @@
 #include "../../include/zf.h"
 
 struct zf_kv {
-  int32_t num_pages = 0, num_raw = 0, page_size = 0, max_requests = 0, max_pages = 0;
+  int32_t num_pages = 0, num_raw = 0, num_layers = 0, page_size = 0, max_requests = 0, max_pages = 0;
   std::vector<int32_t> free_pages;      // stacks of free ids / slots
   std::vector<int32_t> free_raw;
   struct Request {
     bool active = false;
     int32_t len = 0;
     std::vector<int32_t> pages;
-    int32_t tail_raw = -1;              // raw slot of the partial last page, -1 if the last is full
+    std::vector<int32_t> tail_raw;      // per layer, raw slot of the partial last page; empty if the last is full
   };
   std::vector<Request> reqs;
   std::vector<int32_t> owner;           // per page id: request holding it, -1 if free
-  std::vector<int32_t> held_raw;        // per page id: raw slot it holds while full, -1 if none
-  std::vector<uint8_t> pending;         // per page id: full, raw slot held until the caller reclaims
-  std::vector<uint8_t> kept;            // per page id: full and left raw by its encode
+  std::vector<int32_t> held_raw;        // [page id][layer]: raw slot a full page holds, -1 if none
+  std::vector<uint8_t> pending;         // per page id: full, raw slots held until the caller reclaims
+  std::vector<int32_t> kept;            // per page id: layers in which it is full and left raw
   std::vector<int32_t> pending_ids;     // the pending page ids, unordered
   std::vector<int32_t> pending_at;      // per page id: its index in pending_ids, -1 if not pending
-  int32_t kept_count = 0;
+  int32_t kept_pages = 0;               // full pages left raw in at least one layer
+  int64_t kept_slots = 0;               // raw slots those pages hold
 };
 
 namespace {
@@ -52,8 +58,11 @@ int32_t take(std::vector<int32_t>& stack) {
   return v;
 }
 
-void set_pending(zf_kv* kv, int32_t pid, int32_t slot) {
-  kv->held_raw[pid] = slot;
+int32_t* held(zf_kv* kv, int32_t pid) { return kv->held_raw.data() + static_cast<size_t>(pid) * kv->num_layers; }
+
+// a page that just became full: its per-layer raw slots are held until the caller reclaims them
+void set_pending(zf_kv* kv, int32_t pid, const std::vector<int32_t>& slots) {
+  std::copy(slots.begin(), slots.end(), held(kv, pid));
   kv->pending[pid] = 1;
   kv->pending_at[pid] = static_cast<int32_t>(kv->pending_ids.size());
   kv->pending_ids.push_back(pid);
@@ -70,26 +79,46 @@ void clear_pending(zf_kv* kv, int32_t pid) {
 }
 
 void give_back_raw(zf_kv* kv, int32_t pid) {
-  if (kv->held_raw[pid] >= 0) kv->free_raw.push_back(kv->held_raw[pid]);
-  kv->held_raw[pid] = -1;
+  int32_t* h = held(kv, pid);
+  for (int32_t l = 0; l < kv->num_layers; ++l) {
+    if (h[l] >= 0) kv->free_raw.push_back(h[l]);
+    h[l] = -1;
+  }
   clear_pending(kv, pid);
-  if (kv->kept[pid]) --kv->kept_count;
+  if (kv->kept[pid]) {
+    --kv->kept_pages;
+    kv->kept_slots -= kv->kept[pid];
+  }
   kv->kept[pid] = 0;
+}
+
+// a new page takes one raw slot per layer
+std::vector<int32_t> take_slots(zf_kv* kv) {
+  std::vector<int32_t> slots(kv->num_layers);
+  for (int32_t& v : slots) v = take(kv->free_raw);
+  return slots;
+}
+
+// pages that can be opened from the free pools: one id and num_layers raw slots each
+int32_t openable(const zf_kv* kv) {
+  return std::min(static_cast<int32_t>(kv->free_pages.size()),
+                  static_cast<int32_t>(kv->free_raw.size()) / kv->num_layers);
 }
 
 }  // namespace
 
-extern "C" zf_status zf_kv_create(int32_t num_pages, int32_t num_raw_slots, int32_t page_size, int32_t max_requests,
-                                  int32_t max_pages_per_req, zf_kv** out) {
+extern "C" zf_status zf_kv_create(int32_t num_pages, int32_t num_raw_slots, int32_t num_layers, int32_t page_size,
+                                  int32_t max_requests, int32_t max_pages_per_req, zf_kv** out) {
   if (!out) return ZF_ERR_INVALID_ARGUMENT;
   *out = nullptr;
-  if (num_pages < 1 || num_raw_slots < 1 || max_requests < 1 || max_pages_per_req < 1 ||
+  if (num_pages < 1 || num_layers < 1 || num_raw_slots < num_layers || max_requests < 1 || max_pages_per_req < 1 ||
       page_size < ZF_BLOCK_TOKENS || page_size % ZF_BLOCK_TOKENS || page_size > ZF_MAX_PAGE_SIZE)
     return ZF_ERR_INVALID_ARGUMENT;
   zf_kv* kv = new (std::nothrow) zf_kv;
   if (!kv) return ZF_ERR_UNSUPPORTED;
   kv->num_pages = num_pages;
   kv->num_raw = num_raw_slots;
+  kv->num_layers = num_layers;
   kv->page_size = page_size;
   kv->max_requests = max_requests;
   kv->max_pages = max_pages_per_req;
@@ -98,7 +127,7 @@ extern "C" zf_status zf_kv_create(int32_t num_pages, int32_t num_raw_slots, int3
   for (int32_t i = num_raw_slots - 1; i >= 0; --i) kv->free_raw.push_back(i);
   kv->reqs.resize(max_requests);
   kv->owner.assign(num_pages, -1);
-  kv->held_raw.assign(num_pages, -1);
+  kv->held_raw.assign(static_cast<size_t>(num_pages) * num_layers, -1);
   kv->pending.assign(num_pages, 0);
   kv->kept.assign(num_pages, 0);
   kv->pending_at.assign(num_pages, -1);
@@ -115,26 +144,26 @@ extern "C" zf_status zf_kv_admit(zf_kv* kv, int32_t req, int32_t len, int32_t* p
   const int32_t np = pages_for(kv, len);
   if (np > kv->max_pages) return ZF_ERR_INVALID_ARGUMENT;
   if (np > 0 && (!page_ids || !n_valid || !raw_slots)) return ZF_ERR_INVALID_ARGUMENT;
-  // every page is written uncompressed first: np ids and np raw slots
-  if (np > static_cast<int32_t>(kv->free_pages.size()) || np > static_cast<int32_t>(kv->free_raw.size()))
-    return ZF_ERR_CAPACITY;
+  // every page is written uncompressed first: np ids and np raw slots in every layer
+  if (np > openable(kv)) return ZF_ERR_CAPACITY;
   zf_kv::Request& r = kv->reqs[req];
   r = zf_kv::Request{};
   r.active = true;
   r.len = len;
   for (int32_t i = 0; i < np; ++i) {
-    const int32_t pid = take(kv->free_pages), slot = take(kv->free_raw);
+    const int32_t pid = take(kv->free_pages);
+    const std::vector<int32_t> slots = take_slots(kv);
     const int32_t fill = std::min(kv->page_size, len - i * kv->page_size);
     kv->owner[pid] = req;
     r.pages.push_back(pid);
     if (fill == kv->page_size) {
-      set_pending(kv, pid, slot);
+      set_pending(kv, pid, slots);
     } else {
-      r.tail_raw = slot;
+      r.tail_raw = slots;
     }
     page_ids[i] = pid;
     n_valid[i] = fill;
-    raw_slots[i] = slot;
+    for (int32_t l = 0; l < kv->num_layers; ++l) raw_slots[static_cast<size_t>(l) * np + i] = slots[l];
   }
   *n = np;
   return ZF_OK;
@@ -155,25 +184,24 @@ extern "C" zf_status zf_kv_append(zf_kv* kv, const int32_t* reqs, int32_t n, int
       ++need;
     }
   }
-  if (need > static_cast<int32_t>(kv->free_pages.size()) || need > static_cast<int32_t>(kv->free_raw.size()))
-    return ZF_ERR_CAPACITY;
+  if (need > openable(kv)) return ZF_ERR_CAPACITY;
   for (int32_t i = 0; i < n; ++i) {
     zf_kv::Request& r = kv->reqs[reqs[i]];
     if (r.len % kv->page_size == 0) {
       const int32_t pid = take(kv->free_pages);
       kv->owner[pid] = reqs[i];
       r.pages.push_back(pid);
-      r.tail_raw = take(kv->free_raw);
+      r.tail_raw = take_slots(kv);
     }
     ++r.len;
     const int32_t pid = r.pages.back();
     const int32_t fill = r.len - (static_cast<int32_t>(r.pages.size()) - 1) * kv->page_size;
     page_ids[i] = pid;
     n_valid[i] = fill;
-    raw_slots[i] = r.tail_raw;
+    for (int32_t l = 0; l < kv->num_layers; ++l) raw_slots[static_cast<size_t>(l) * n + i] = r.tail_raw[l];
     if (fill == kv->page_size) {                            // full: compressed by this encode
       set_pending(kv, pid, r.tail_raw);
-      r.tail_raw = -1;
+      r.tail_raw.clear();
     }
   }
   return ZF_OK;
@@ -189,7 +217,8 @@ extern "C" zf_status zf_kv_pending(const zf_kv* kv, int32_t* page_ids, int32_t* 
   std::sort(ids.begin(), ids.end());
   for (int32_t i = 0; i < k; ++i) {
     page_ids[i] = ids[i];
-    raw_slots[i] = kv->held_raw[ids[i]];
+    const int32_t* h = kv->held_raw.data() + static_cast<size_t>(ids[i]) * kv->num_layers;
+    for (int32_t l = 0; l < kv->num_layers; ++l) raw_slots[static_cast<size_t>(l) * k + i] = h[l];
   }
   return ZF_OK;
 }
@@ -204,12 +233,21 @@ extern "C" zf_status zf_kv_reclaim(zf_kv* kv, const int32_t* page_ids, const int
   }
   for (int32_t i = 0; i < n; ++i) {
     const int32_t pid = page_ids[i];
-    if (kept_raw[i]) {
-      clear_pending(kv, pid);
-      kv->kept[pid] = 1;
-      ++kv->kept_count;
-    } else {
-      give_back_raw(kv, pid);
+    int32_t* h = held(kv, pid);
+    int32_t keep = 0;
+    for (int32_t l = 0; l < kv->num_layers; ++l) {
+      if (kept_raw[static_cast<size_t>(l) * n + i]) {
+        ++keep;
+      } else {                                              // compressed in this layer: slot back to the pool
+        kv->free_raw.push_back(h[l]);
+        h[l] = -1;
+      }
+    }
+    clear_pending(kv, pid);
+    if (keep) {
+      kv->kept[pid] = keep;
+      ++kv->kept_pages;
+      kv->kept_slots += keep;
     }
   }
   return ZF_OK;
@@ -223,7 +261,7 @@ extern "C" zf_status zf_kv_release(zf_kv* kv, int32_t req) {
     kv->owner[pid] = -1;
     kv->free_pages.push_back(pid);
   }
-  if (r.tail_raw >= 0) kv->free_raw.push_back(r.tail_raw);
+  for (const int32_t slot : r.tail_raw) kv->free_raw.push_back(slot);
   r = zf_kv::Request{};
   return ZF_OK;
 }
@@ -249,14 +287,15 @@ extern "C" zf_status zf_kv_get_stats(const zf_kv* kv, zf_kv_stats* out) {
     if (!r.active) continue;
     ++s.active_requests;
     s.tokens += r.len;
-    if (r.tail_raw >= 0) ++s.partial_pages;
+    if (!r.tail_raw.empty()) ++s.partial_pages;
   }
   const int32_t owned = kv->num_pages - s.free_pages;
   s.pending_pages = static_cast<int32_t>(kv->pending_ids.size());
-  s.raw_full_pages = kv->kept_count;
+  s.raw_full_pages = kv->kept_pages;
+  s.raw_full_slots = static_cast<int32_t>(kv->kept_slots);
   s.compressed_pages = owned - s.partial_pages - s.pending_pages - s.raw_full_pages;
-  // new pages are written uncompressed first: each needs a page id and a raw slot
-  s.new_page_capacity = std::min(s.free_pages, s.free_raw_slots);
+  // new pages are written uncompressed first: each needs a page id and a raw slot in every layer
+  s.new_page_capacity = openable(kv);
   *out = s;
   return ZF_OK;
 }

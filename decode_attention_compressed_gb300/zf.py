@@ -40,6 +40,7 @@ class ZfKvStats(ctypes.Structure):
         ("tokens", ctypes.c_int64), ("free_pages", _c_int32), ("free_raw_slots", _c_int32),
         ("active_requests", _c_int32), ("partial_pages", _c_int32), ("pending_pages", _c_int32),
         ("raw_full_pages", _c_int32), ("compressed_pages", _c_int32), ("new_page_capacity", _c_int32),
+        ("raw_full_slots", _c_int32),
     ]
 
 
@@ -69,7 +70,7 @@ SIGNATURES = {
     "zf_dense_decode_attn_multi": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
                                               _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
                                               _c_void_p, _c_size_t, _c_void_p]),
-    "zf_kv_create": (_c_int32, [_c_int32, _c_int32, _c_int32, _c_int32, _c_int32, ctypes.POINTER(_c_void_p)]),
+    "zf_kv_create": (_c_int32, [_c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, ctypes.POINTER(_c_void_p)]),
     "zf_kv_destroy": (None, [_c_void_p]),
     "zf_kv_admit": (_c_int32, [_c_void_p, _c_int32, _c_int32, _P32, _P32, _P32, _P32]),
     "zf_kv_append": (_c_int32, [_c_void_p, _P32, _c_int32, _P32, _P32, _P32]),
@@ -128,22 +129,32 @@ class Cache:
     """One layer's paged cache in device memory, laid out as include/zf.h describes.
 
     k_comp/v_comp: [num_pages][Hkv][P/4 * 784] uint8; k_raw/v_raw: [num_raw][Hkv][P/4 * 512] int16
-    (BF16 bits); dir: [num_pages][Hkv] int32; status: one int32 device word.
+    (BF16 bits); dir: [num_pages][Hkv] int32; status: one int32 device word.  raw_pool=another
+    Cache makes this layer use that cache's raw arrays (one raw pool for all layers, as KvManager
+    with num_layers > 1 hands out slots).
     """
 
-    def __init__(self, num_pages, num_kv_heads, page_size, num_raw_slots, device="cuda", compressed=True):
+    def __init__(self, num_pages, num_kv_heads, page_size, num_raw_slots, device="cuda", compressed=True,
+                 raw_pool=None):
         nblk = page_size // 4
         self.num_pages, self.num_kv_heads, self.page_size = num_pages, num_kv_heads, page_size
         self.num_raw_slots = num_raw_slots
         dev = torch.device(device)
+        if raw_pool is not None:                   # share another cache's raw arrays (one pool for all layers)
+            if (raw_pool.num_kv_heads, raw_pool.page_size, raw_pool.num_raw_slots) != (num_kv_heads, page_size,
+                                                                                      num_raw_slots):
+                raise ValueError("a shared raw pool must match the kv heads, page size and raw slot count")
         if compressed:
             self.k_comp = torch.empty((num_pages, num_kv_heads, nblk * SLOT_BYTES), dtype=torch.uint8, device=dev)
             self.v_comp = torch.empty_like(self.k_comp)
         else:
             self.k_comp = self.v_comp = None       # dense cache: raw slots only (zf_dense_decode_attn)
         self.dir = torch.full((num_pages, num_kv_heads), DIR_INVALID, dtype=torch.int32, device=dev)
-        self.k_raw = torch.empty((num_raw_slots, num_kv_heads, nblk * 512), dtype=torch.int16, device=dev)
-        self.v_raw = torch.empty_like(self.k_raw)
+        if raw_pool is not None:
+            self.k_raw, self.v_raw = raw_pool.k_raw, raw_pool.v_raw
+        else:
+            self.k_raw = torch.empty((num_raw_slots, num_kv_heads, nblk * 512), dtype=torch.int16, device=dev)
+            self.v_raw = torch.empty_like(self.k_raw)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     @property
@@ -310,13 +321,15 @@ def _i32(values):
 
 
 class KvManager:
-    """zf_kv: host-side page manager (page ids and raw slots shared by all layers).  Each call
-    returns the encode list (page_ids, n_valid, raw_slots) that zf_encode_pages takes."""
+    """zf_kv: host-side page manager (page ids for all layers, one raw-slot pool shared by
+    num_layers layers).  admit/append return the encode list (page_ids, n_valid, raw_slots) with
+    raw_slots[l] the slot list of layer l's zf_encode_pages call."""
 
-    def __init__(self, num_pages, num_raw_slots, page_size, max_requests, max_pages_per_req):
+    def __init__(self, num_pages, num_raw_slots, page_size, max_requests, max_pages_per_req, num_layers=1):
         self.page_size, self.max_requests, self.max_pages = page_size, max_requests, max_pages_per_req
+        self.num_layers = num_layers
         h = _c_void_p()
-        _check("zf_kv_create", lib().zf_kv_create(num_pages, num_raw_slots, page_size, max_requests,
+        _check("zf_kv_create", lib().zf_kv_create(num_pages, num_raw_slots, num_layers, page_size, max_requests,
                                                    max_pages_per_req, ctypes.byref(h)))
         self._h = h
 
@@ -331,43 +344,59 @@ class KvManager:
         except Exception:
             pass
 
+    def _layers(self, flat, n):
+        return [list(flat[l * n:(l + 1) * n]) for l in range(self.num_layers)]
+
     def admit(self, req, length):
-        n_max = -(-length // self.page_size)
-        ids, nv, rs, n = (_c_int32 * max(n_max, 1))(), (_c_int32 * max(n_max, 1))(), (_c_int32 * max(n_max, 1))(), _c_int32()
+        n_max = max(-(-length // self.page_size), 1)
+        ids, nv, n = (_c_int32 * n_max)(), (_c_int32 * n_max)(), _c_int32()
+        rs = (_c_int32 * (n_max * self.num_layers))()
         _check("zf_kv_admit", lib().zf_kv_admit(self._h, req, length, ids, nv, rs, ctypes.byref(n)))
-        return list(ids[: n.value]), list(nv[: n.value]), list(rs[: n.value])
+        k = n.value
+        return list(ids[:k]), list(nv[:k]), self._layers(rs, k)
 
     def append(self, reqs):
         n = len(reqs)
-        ids, nv, rs = (_c_int32 * max(n, 1))(), (_c_int32 * max(n, 1))(), (_c_int32 * max(n, 1))()
+        ids, nv = (_c_int32 * max(n, 1))(), (_c_int32 * max(n, 1))()
+        rs = (_c_int32 * max(n * self.num_layers, 1))()
         _check("zf_kv_append", lib().zf_kv_append(self._h, _i32(reqs), n, ids, nv, rs))
-        return list(ids[:n]), list(nv[:n]), list(rs[:n])
+        return list(ids[:n]), list(nv[:n]), self._layers(rs, n)
 
     def pending(self):
+        """(page ids, raw slots per layer) of the full pages awaiting reclaim, ascending id."""
         n = _c_int32()
         code = lib().zf_kv_pending(self._h, None, None, 0, ctypes.byref(n))
         if code not in (0, -1):
             _check("zf_kv_pending", code)
         k = n.value
-        ids, rs = (_c_int32 * max(k, 1))(), (_c_int32 * max(k, 1))()
+        ids, rs = (_c_int32 * max(k, 1))(), (_c_int32 * max(k * self.num_layers, 1))()
         _check("zf_kv_pending", lib().zf_kv_pending(self._h, ids, rs, k, ctypes.byref(n)))
-        return list(ids[:k]), list(rs[:k])
+        return list(ids[:k]), self._layers(rs, k)
 
     def reclaim(self, page_ids, kept_raw):
-        _check("zf_kv_reclaim", lib().zf_kv_reclaim(self._h, _i32(page_ids), _i32([int(bool(x)) for x in kept_raw]),
-                                                    len(page_ids)))
+        """kept_raw[l][i]: page_ids[i] has a page-head stored raw in layer l (keeps that layer's slot)."""
+        n = len(page_ids)
+        if len(kept_raw) != self.num_layers or any(len(row) != n for row in kept_raw):
+            raise ValueError("kept_raw needs one row of len(page_ids) flags per layer")
+        flat = [int(bool(x)) for row in kept_raw for x in row]
+        _check("zf_kv_reclaim", lib().zf_kv_reclaim(self._h, _i32(page_ids), _i32(flat), n))
 
     def reclaim_from(self, caches):
-        """Reclaim every pending page from the directories of `caches` (one per layer): a page keeps
-        its raw slot if any page-head of it is stored raw in any of them."""
+        """Reclaim every pending page from the directories of `caches`.  With num_layers layers,
+        caches[l] is layer l (each layer keeps or returns its own slot); with num_layers == 1, any
+        number of caches addressed by the same slots (a page keeps its slot if it is raw in any)."""
         ids, _ = self.pending()
         if not ids:
             return 0
+        if self.num_layers > 1 and len(caches) != self.num_layers:
+            raise ValueError("one cache per layer")
         idx = torch.as_tensor(ids, dtype=torch.long)
-        kept = torch.zeros(len(ids), dtype=torch.bool)
-        for c in caches:
-            kept |= (c.dir.index_select(0, idx.to(c.dir.device)).cpu() >= 0).any(dim=1)
-        self.reclaim(ids, kept.tolist())
+        raw = [(c.dir.index_select(0, idx.to(c.dir.device)).cpu() >= 0).any(dim=1) for c in caches]
+        if self.num_layers == 1:
+            kept = [torch.stack(raw).any(dim=0).tolist()]
+        else:
+            kept = [r.tolist() for r in raw]
+        self.reclaim(ids, kept)
         return len(ids)
 
     def release(self, req):

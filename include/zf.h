@@ -97,7 +97,9 @@ typedef struct zf_cache {
   int32_t reserved;       /* must be 0 */
   uint8_t* k_comp;        /* [num_pages][num_kv_heads][page_size/4][784] */
   uint8_t* v_comp;
-  uint16_t* k_raw;        /* [num_raw_slots][num_kv_heads][page_size/4][512] */
+  uint16_t* k_raw;        /* [num_raw_slots][num_kv_heads][page_size/4][512]; several layers' caches
+                             may point at the same raw arrays (one pool, each slot written only by
+                             the encode it was listed for; see zf_kv) */
   uint16_t* v_raw;
   int32_t* dir;           /* [num_pages][num_kv_heads] */
   int32_t* status;        /* optional device word; ZF_DEV_* bits are OR-ed in; NULL = not reported */
@@ -268,14 +270,21 @@ zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t* q, int32_
  * compression (so capacity for them is counted in uncompressed storage) and capacity grows back as
  * compression releases that storage.  §II.C (Compression for Higher Serving Capacity): the
  * storage compression frees is what lets more requests in.
- * A page id names one compressed slot in every layer's cache, a raw slot one uncompressed page in
- * every layer's raw pool (all layers use the same ids and slots, sized alike).  Every page being
- * written holds a raw slot: a request's partial last page while it fills, a full page until the
- * caller reports, from the directory, whether its encode compressed it (zf_kv_reclaim): a page
- * whose page-heads all compressed returns its raw slot, one with any page-head left raw (more
- * than six escapes in a block) keeps it until its request is released.  The manager only does
- * the bookkeeping: the caller writes the listed pages with zf_encode_pages (whose page_ids,
- * n_valid and raw_slots arrays the calls below fill) and uploads the page table and lengths.
+ * A page id names one compressed slot in every layer's cache.  Raw slots come from one pool that
+ * all num_layers layers share (every layer's zf_cache points its k_raw / v_raw at the same arrays
+ * of num_raw_slots slots): a page being written holds one raw slot per layer — a request's partial
+ * last page while it fills, a full page until the caller reports, layer by layer, whether its
+ * encode compressed it (zf_kv_reclaim).  A layer whose page-heads of that page all compressed
+ * returns its slot to the pool, where any layer can take it (§III.D: storage released in one layer
+ * is reassigned to another once the reads of it have finished — here, once the caller has read
+ * the directory after the encode, and the slot is only written again by a later encode on the
+ * caller's stream); a layer with a page-head left raw (more than six escapes in a block) keeps its
+ * slot until the request is released.  With num_layers = 1 the same bookkeeping also serves
+ * per-layer raw pools addressed by one slot index (report a page raw when it is raw in any layer).
+ * Per-layer outputs and inputs are layer-major: entry (layer l, item i) of an n-item list is at
+ * l * n + i, so row l is the raw_slots array of layer l's zf_encode_pages call.  The manager only
+ * does the bookkeeping: the caller writes the listed pages with zf_encode_pages and uploads the
+ * page table and lengths.
  * Host code; not thread-safe; no GPU calls.
  * ------------------------------------------------------------------------------------------ */
 typedef struct zf_kv zf_kv;
@@ -287,39 +296,44 @@ typedef struct zf_kv_stats {
   int32_t active_requests;
   int32_t partial_pages;      /* last pages still filling (each holds a raw slot) */
   int32_t pending_pages;      /* full pages whose raw slot awaits zf_kv_reclaim */
-  int32_t raw_full_pages;     /* full pages left raw by their encode (raw slot held) */
-  int32_t compressed_pages;   /* full pages stored compressed (no raw slot) */
-  int32_t new_page_capacity;  /* pages that can be opened now: min(free ids, free raw slots) */
+  int32_t raw_full_pages;     /* full pages left raw in at least one layer */
+  int32_t compressed_pages;   /* full pages compressed in every layer (no raw slot) */
+  int32_t new_page_capacity;  /* pages that can be opened now: min(free ids, free raw slots / num_layers) */
+  int32_t raw_full_slots;     /* raw slots held by the raw_full_pages (one per layer left raw) */
 } zf_kv_stats;
 
-/* A manager for num_pages page ids and num_raw_slots raw slots, pages of page_size tokens, request
- * slots 0 .. max_requests-1 of at most max_pages_per_req pages each.  *out = NULL on error. */
-zf_status zf_kv_create(int32_t num_pages, int32_t num_raw_slots, int32_t page_size, int32_t max_requests,
-                       int32_t max_pages_per_req, zf_kv** out);
+/* A manager for num_pages page ids and a pool of num_raw_slots raw slots (>= num_layers) shared by
+ * num_layers layers, pages of page_size tokens, request slots 0 .. max_requests-1 of at most
+ * max_pages_per_req pages each.  *out = NULL on error. */
+zf_status zf_kv_create(int32_t num_pages, int32_t num_raw_slots, int32_t num_layers, int32_t page_size,
+                       int32_t max_requests, int32_t max_pages_per_req, zf_kv** out);
 void zf_kv_destroy(zf_kv* kv);
 
-/* Admit request slot `req` (inactive) with a prompt of `len` tokens: takes ceil(len / page_size)
- * page ids and as many raw slots (every page is written uncompressed first) and writes the
- * encode list for the prompt — page_ids / n_valid / raw_slots, *n entries — in page order.
- * ZF_ERR_CAPACITY when the pool cannot hold it. */
+/* Admit request slot `req` (inactive) with a prompt of `len` tokens: takes n = ceil(len /
+ * page_size) page ids and n raw slots per layer (every page is written uncompressed first) and
+ * writes the encode list for the prompt in page order — page_ids / n_valid [n], raw_slots
+ * [num_layers][n] — and *n = n.  ZF_ERR_CAPACITY when the pools cannot hold it. */
 zf_status zf_kv_admit(zf_kv* kv, int32_t req, int32_t len, int32_t* page_ids, int32_t* n_valid,
                       int32_t* raw_slots, int32_t* n);
 
 /* One new token for each of the n distinct active requests reqs[i]: entry i of the outputs is the
- * page that holds it (page id, tokens in it, raw slot) — one zf_encode_pages call writes them all.
- * A request whose last page is full opens a new page (id + raw slot) first; a page that becomes
- * full here is compressed by that encode and its raw slot is pending until zf_kv_reclaim.  All or
- * nothing: ZF_ERR_CAPACITY (or an invalid request) changes no request. */
+ * page that holds it (page_ids[i], tokens in it n_valid[i], its raw slot in layer l
+ * raw_slots[l * n + i]) — one zf_encode_pages call per layer writes them all.  A request whose
+ * last page is full opens a new page (an id + a raw slot per layer) first; a page that becomes
+ * full here is compressed by those encodes and its raw slots are pending until zf_kv_reclaim.
+ * All or nothing: ZF_ERR_CAPACITY (or an invalid request) changes no request. */
 zf_status zf_kv_append(zf_kv* kv, const int32_t* reqs, int32_t n, int32_t* page_ids, int32_t* n_valid,
                        int32_t* raw_slots);
 
-/* Full pages whose raw slot is pending, ascending page id: up to `capacity` (page id, raw slot)
- * pairs; *n = their total count (ZF_ERR_INVALID_ARGUMENT when it exceeds capacity). */
+/* Full pages whose raw slots are pending, ascending page id: *n = their count k; page_ids[i] and,
+ * per layer, raw_slots[l * k + i] (raw_slots holds num_layers * capacity entries).
+ * ZF_ERR_INVALID_ARGUMENT, with *n set, when k exceeds capacity. */
 zf_status zf_kv_pending(const zf_kv* kv, int32_t* page_ids, int32_t* raw_slots, int32_t capacity, int32_t* n);
 
-/* After the encodes of these pending pages have run: kept_raw[i] != 0 when any page-head of
- * page_ids[i], in any layer, is stored raw (directory entry >= 0); those keep their raw slot, the
- * others return it to the pool.  Every id must be pending, with no repeats. */
+/* After the encodes of these n pending pages have run: kept_raw[l * n + i] != 0 when any
+ * page-head of page_ids[i] is stored raw in layer l (directory entry >= 0); that layer keeps its
+ * raw slot, every other layer returns its slot to the shared pool.  Every id must be pending,
+ * with no repeats. */
 zf_status zf_kv_reclaim(zf_kv* kv, const int32_t* page_ids, const int32_t* kept_raw, int32_t n);
 
 /* Return request `req`'s page ids and raw slots to the pools. */
@@ -331,9 +345,10 @@ zf_status zf_kv_export(const zf_kv* kv, int32_t* page_table, int32_t* seq_lens);
 
 zf_status zf_kv_get_stats(const zf_kv* kv, zf_kv_stats* out);
 
-/* Sizing: page ids a layer's cache of bytes_per_layer holds next to num_raw_slots raw slots
- * (compressed K and V slots plus directory entries per page id), and the pages the same bytes
- * hold as a dense BF16 cache. */
+/* Sizing: page ids a layer's cache of bytes_per_layer holds next to num_raw_slots raw slots of
+ * its own (with one shared pool: its share, pool slots / layers), counting compressed K and V
+ * slots plus directory entries per page id, and the pages the same bytes hold as a dense BF16
+ * cache. */
 zf_status zf_kv_plan_pages(int64_t bytes_per_layer, int32_t num_kv_heads, int32_t page_size,
                            int32_t num_raw_slots, int32_t* num_pages, int32_t* dense_pages);
 

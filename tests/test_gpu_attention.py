@@ -360,57 +360,79 @@ def test_multi_token_full_size_sampled(zf):
 
 
 def test_decode_loop_through_the_page_manager(zf):
-    """A serving loop driven by zf_kv: three prompts admitted (their pages encoded as listed), 24
-    decode steps that each append one token per request (the listed tail pages re-encoded, raw
-    while partial, compressed when full), raw slots reclaimed from the directory after every
-    encode, one request released and another admitted mid-way; at several steps the attention over
-    the exported page table matches the float64 attention over each request's token stream."""
-    P, Hkv, Hq, D = 16, 2, 8, 128
+    """A serving loop driven by zf_kv over two layers whose caches share one raw-slot pool: three
+    prompts admitted (their pages encoded as listed, per layer), 24 decode steps that each append
+    one token per request (the listed tail pages re-encoded, raw while partial, compressed when
+    full), raw slots reclaimed layer by layer from the directories after every encode, one request
+    released and another admitted mid-way.  Layer 1's keys carry a spike every 24 tokens, so the
+    pages holding one stay raw in layer 1 only and their layer-0 slots go back to the pool for
+    either layer to reuse.  At several steps each layer's attention over the exported page table
+    matches the float64 attention over each request's token stream."""
+    P, Hkv, Hq, D, NL = 16, 2, 8, 128, 2
     dev = torch.device("cuda")
     gen = torch.Generator().manual_seed(61)
     max_len = 160
-    streams_k = [torch.randn(max_len, Hkv, D, generator=gen).mul(torch.exp(0.5 * torch.randn(D, generator=gen)))
-                 .to(torch.bfloat16).view(torch.int16) for _ in range(4)]
-    streams_v = [torch.randn(max_len, Hkv, D, generator=gen).to(torch.bfloat16).view(torch.int16) for _ in range(4)]
-    kv = zf.KvManager(num_pages=40, num_raw_slots=16, page_size=P, max_requests=4, max_pages_per_req=10)
-    cache = zf.Cache(40, Hkv, P, 16, device=dev)
+    streams_k, streams_v = [], []
+    for layer in range(NL):
+        ks, vs = [], []
+        for _ in range(4):
+            k = torch.randn(max_len, Hkv, D, generator=gen).mul(torch.exp(0.5 * torch.randn(D, generator=gen)))
+            if layer == 1:
+                k[7::24, 0, 5:13] *= 2.0 ** -30             # 8 escapes: that page-head stays raw
+            ks.append(k.to(torch.bfloat16).view(torch.int16))
+            vs.append(torch.randn(max_len, Hkv, D, generator=gen).to(torch.bfloat16).view(torch.int16))
+        streams_k.append(ks)
+        streams_v.append(vs)
+    num_raw = 20
+    kv = zf.KvManager(num_pages=40, num_raw_slots=num_raw, page_size=P, max_requests=4, max_pages_per_req=10,
+                      num_layers=NL)
+    caches = [zf.Cache(40, Hkv, P, num_raw, device=dev)]
+    caches.append(zf.Cache(40, Hkv, P, num_raw, device=dev, raw_pool=caches[0]))
     stream_of = {}
+    kept_seen = []
 
     def write(req, ids, nv, rs):
         s = stream_of[req]
-        pages_k = torch.zeros(len(ids), Hkv, P, D, dtype=torch.int16)
-        pages_v = torch.zeros_like(pages_k)
         length = int(kv.export()[1][req])
         first = -(-length // P) - len(ids)                   # index of the first listed page
-        for j in range(len(ids)):
-            lo = (first + j) * P
-            hi = lo + nv[j]
-            pages_k[j, :, : nv[j]] = streams_k[s][lo:hi].transpose(0, 1)
-            pages_v[j, :, : nv[j]] = streams_v[s][lo:hi].transpose(0, 1)
-        zf.encode_pages(cache, pages_k.to(dev), pages_v.to(dev), ids, nv, rs)
-        kv.reclaim_from([cache])
+        for layer in range(NL):
+            pages_k = torch.zeros(len(ids), Hkv, P, D, dtype=torch.int16)
+            pages_v = torch.zeros_like(pages_k)
+            for j in range(len(ids)):
+                lo = (first + j) * P
+                hi = lo + nv[j]
+                pages_k[j, :, : nv[j]] = streams_k[layer][s][lo:hi].transpose(0, 1)
+                pages_v[j, :, : nv[j]] = streams_v[layer][s][lo:hi].transpose(0, 1)
+            zf.encode_pages(caches[layer], pages_k.to(dev), pages_v.to(dev), ids, nv, rs[layer])
+
+    def reclaim():            # only once every page listed as pending has been encoded in every layer
+        kv.reclaim_from(caches)
+        st = kv.stats()
+        kept_seen.append((st["raw_full_pages"], st["raw_full_slots"]))
 
     def check():
         table, lens = kv.export()
-        q = torch.randn(4, Hq, D, generator=gen).to(torch.bfloat16).view(torch.int16)
-        out, lse = zf.decode_attn(cache, q.to(dev), table.to(dev), lens.to(dev), 0.125)
-        torch.cuda.synchronize()
-        assert cache.status_word() == 0
-        ref_out = np.zeros((4, Hq, D))
-        ref_lse = np.full((4, Hq), -math.inf)
-        for req, s in stream_of.items():
-            L = int(lens[req])
-            for h in range(Hq):
-                g = h // (Hq // Hkv)
-                ref_out[req, h], ref_lse[req, h], _ = O.attention_one(
-                    O.bf16_to_f64(H.np_bits(q[req, h])), O.bf16_to_f64(H.np_bits(streams_k[s][:L, g])),
-                    O.bf16_to_f64(H.np_bits(streams_v[s][:L, g])), 0.125)
-        H.compare_attention(out, lse, ref_out, ref_lse)
+        for layer in range(NL):
+            q = torch.randn(4, Hq, D, generator=gen).to(torch.bfloat16).view(torch.int16)
+            out, lse = zf.decode_attn(caches[layer], q.to(dev), table.to(dev), lens.to(dev), 0.125)
+            torch.cuda.synchronize()
+            assert caches[layer].status_word() == 0
+            ref_out = np.zeros((4, Hq, D))
+            ref_lse = np.full((4, Hq), -math.inf)
+            for req, s in stream_of.items():
+                L = int(lens[req])
+                for h in range(Hq):
+                    g = h // (Hq // Hkv)
+                    ref_out[req, h], ref_lse[req, h], _ = O.attention_one(
+                        O.bf16_to_f64(H.np_bits(q[req, h])), O.bf16_to_f64(H.np_bits(streams_k[layer][s][:L, g])),
+                        O.bf16_to_f64(H.np_bits(streams_v[layer][s][:L, g])), 0.125)
+            H.compare_attention(out, lse, ref_out, ref_lse)
 
     for req, length in ((0, 37), (1, 16), (2, 70)):
         stream_of[req] = req
         ids, nv, rs = kv.admit(req, length)
         write(req, ids, nv, rs)
+        reclaim()
     check()
     for step in range(24):
         if step == 10:                                       # request 1 leaves, request 3 arrives
@@ -419,11 +441,21 @@ def test_decode_loop_through_the_page_manager(zf):
             stream_of[3] = 3
             ids, nv, rs = kv.admit(3, 50)
             write(3, ids, nv, rs)
+            reclaim()
         reqs = sorted(stream_of)
         ids, nv, rs = kv.append(reqs)
-        for req, pid, fill, slot in zip(reqs, ids, nv, rs):
-            write(req, [pid], [fill], [slot])
+        for i, (req, pid, fill) in enumerate(zip(reqs, ids, nv)):
+            write(req, [pid], [fill], [[rs[layer][i]] for layer in range(NL)])
+        reclaim()
         if step % 6 == 5:
             check()
     st = kv.stats()
     assert st["pending_pages"] == 0 and st["tokens"] == int(kv.export()[1].sum())
+    # full pages with a spike stayed raw in layer 1 only: one kept slot each, none in layer 0
+    assert any(p > 0 for p, _ in kept_seen) and all(p == n for p, n in kept_seen), kept_seen
+    table, lens = kv.export()
+    full = [int(table[q, i]) for q in range(4) for i in range(int(lens[q]) // P)]
+    d0, d1 = caches[0].dir.cpu()[full], caches[1].dir.cpu()[full]
+    assert (d0 == zf.DIR_COMPRESSED).all()
+    raw_pages = int((d1 >= 0).any(dim=1).sum())
+    assert raw_pages > 0 and st["raw_full_pages"] == raw_pages == st["raw_full_slots"]

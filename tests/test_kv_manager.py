@@ -1,9 +1,10 @@
 """zf_kv, the host-side page manager (CPU only: bookkeeping, no GPU calls).
 
 ZipFusion §III.D: pages stay uncompressed while they fill, a full page is compressed afterwards
-under its page id, and new pages are counted in uncompressed storage until compression releases
-it.  The checks below restate those rules as invariants of the manager's state and run a random
-workload against a plain Python model of the same rules."""
+under its page id, new pages are counted in uncompressed storage until compression releases it,
+and storage released in one layer can be reassigned to another.  The checks below restate those
+rules as invariants of the manager's state and run a random workload against a plain Python model
+of the same rules, with one layer and with several layers sharing one raw-slot pool."""
 import random
 
 import pytest
@@ -22,7 +23,7 @@ P = 16
 def test_admit_lists_every_page_for_an_uncompressed_first_write(zf):
     kv = zf.KvManager(num_pages=10, num_raw_slots=10, page_size=P, max_requests=4, max_pages_per_req=8)
     ids, nv, rs = kv.admit(0, 37)
-    assert ids == [0, 1, 2] and nv == [16, 16, 5] and rs == [0, 1, 2]
+    assert ids == [0, 1, 2] and nv == [16, 16, 5] and rs == [[0, 1, 2]]
     st = kv.stats()
     assert (st["free_pages"], st["free_raw_slots"], st["pending_pages"], st["partial_pages"]) == (7, 7, 2, 1)
     assert st["tokens"] == 37 and st["new_page_capacity"] == 7
@@ -30,8 +31,8 @@ def test_admit_lists_every_page_for_an_uncompressed_first_write(zf):
     assert table[0, :4].tolist() == [0, 1, 2, -1] and lens.tolist() == [37, 0, 0, 0]
     # the two full pages are reported compressed: their raw slots come back
     pend, slots = kv.pending()
-    assert pend == [0, 1] and slots == [0, 1]
-    kv.reclaim(pend, [False, False])
+    assert pend == [0, 1] and slots == [[0, 1]]
+    kv.reclaim(pend, [[False, False]])
     st = kv.stats()
     assert (st["free_raw_slots"], st["pending_pages"], st["compressed_pages"]) == (9, 0, 2)
 
@@ -41,13 +42,13 @@ def test_append_fills_the_tail_then_opens_a_new_page(zf):
     kv.admit(0, 14)                                   # one partial page, raw slot 0
     for expect_fill in (15, 16):
         ids, nv, rs = kv.append([0])
-        assert ids == [0] and nv == [expect_fill] and rs == [0]
+        assert ids == [0] and nv == [expect_fill] and rs == [[0]]
     assert kv.stats()["pending_pages"] == 1 and kv.stats()["partial_pages"] == 0
     ids, nv, rs = kv.append([0])                       # token 17 opens page 1 with a new raw slot
-    assert ids == [1] and nv == [1] and rs == [1]
-    kv.reclaim([0], [True])                            # page 0 stayed raw: keeps slot 0
+    assert ids == [1] and nv == [1] and rs == [[1]]
+    kv.reclaim([0], [[True]])                          # page 0 stayed raw: keeps slot 0
     st = kv.stats()
-    assert st["raw_full_pages"] == 1 and st["free_raw_slots"] == 1
+    assert st["raw_full_pages"] == 1 and st["raw_full_slots"] == 1 and st["free_raw_slots"] == 1
     kv.release(0)
     st = kv.stats()
     assert (st["free_pages"], st["free_raw_slots"], st["active_requests"], st["tokens"]) == (6, 3, 0, 0)
@@ -65,9 +66,9 @@ def test_capacity_refusals_change_nothing(zf):
         kv.append([0, 1])                              # both open a page: 2 ids free, no raw slot
     assert kv.stats()["tokens"] == 48
     ids, _ = kv.pending()
-    kv.reclaim(ids, [False] * len(ids))                # compression releases uncompressed storage
+    kv.reclaim(ids, [[False] * len(ids)])              # compression releases uncompressed storage
     ids, nv, rs = kv.append([0, 1])
-    assert nv == [1, 1] and len(set(rs)) == 2
+    assert nv == [1, 1] and len(set(rs[0])) == 2
 
 
 def test_invalid_calls_are_refused(zf):
@@ -82,9 +83,45 @@ def test_invalid_calls_are_refused(zf):
     with pytest.raises(zf.ZfError):
         kv.append([0, 0])                              # the same request twice
     with pytest.raises(zf.ZfError):
-        kv.reclaim([0], [False])                       # page 0 is partial, not pending
+        kv.reclaim([0], [[False]])                     # page 0 is partial, not pending
     with pytest.raises(zf.ZfError):
         kv.release(1)
+
+
+def test_raw_slots_freed_in_one_layer_serve_another(zf):
+    """Three layers share a pool of 9 raw slots: a new page takes one slot per layer; after the
+    encodes, a layer that compressed the page returns its slot and a layer that left it raw keeps
+    only its own; the freed slots open new pages for every layer."""
+    kv = zf.KvManager(num_pages=10, num_raw_slots=9, page_size=P, max_requests=3, max_pages_per_req=6, num_layers=3)
+    ids, nv, rs = kv.admit(0, 40)                      # 3 pages x 3 layers: the whole pool
+    assert ids == [0, 1, 2] and nv == [16, 16, 8]
+    assert sorted(s for row in rs for s in row) == list(range(9)) and [len(row) for row in rs] == [3, 3, 3]
+    st = kv.stats()
+    assert (st["free_raw_slots"], st["new_page_capacity"], st["pending_pages"]) == (0, 0, 2)
+    with pytest.raises(zf.ZfError, match="page ids or raw slots"):
+        kv.admit(1, 1)
+    pend, slots = kv.pending()
+    assert pend == [0, 1] and slots == [[rs[l][0], rs[l][1]] for l in range(3)]
+    # page 0 stays raw in layer 2 only; page 1 compresses everywhere
+    kv.reclaim(pend, [[False, False], [False, False], [True, False]])
+    st = kv.stats()
+    assert (st["free_raw_slots"], st["raw_full_pages"], st["raw_full_slots"], st["compressed_pages"]) == (5, 1, 1, 1)
+    assert st["new_page_capacity"] == 1               # 5 slots: one page in all three layers
+    ids1, _, rs1 = kv.admit(1, 16)
+    freed = {rs[l][0] for l in range(2)} | {rs[l][1] for l in range(3)}
+    assert {row[0] for row in rs1} <= freed and len({row[0] for row in rs1}) == 3
+    kv.release(0)                                      # the kept slot and the tail's slots come back
+    st = kv.stats()
+    assert (st["free_raw_slots"], st["raw_full_pages"], st["raw_full_slots"]) == (6, 0, 0)
+
+
+def test_per_layer_lists_are_checked(zf):
+    kv = zf.KvManager(num_pages=4, num_raw_slots=4, page_size=P, max_requests=1, max_pages_per_req=4, num_layers=2)
+    kv.admit(0, 16)
+    with pytest.raises(ValueError):
+        kv.reclaim([0], [[False]])                     # one row per layer
+    with pytest.raises(zf.ZfError):
+        zf.KvManager(num_pages=4, num_raw_slots=1, page_size=P, max_requests=1, max_pages_per_req=4, num_layers=2)
 
 
 def test_plan_pages_counts_compressed_and_dense_storage(zf):
@@ -98,77 +135,85 @@ def test_plan_pages_counts_compressed_and_dense_storage(zf):
     assert 1.15 < pages / (dense - 100) < 1.31
 
 
-def test_random_workload_against_a_model(zf):
+@pytest.mark.parametrize("layers", [1, 3])
+def test_random_workload_against_a_model(zf, layers):
     """Random admits, appends, reclaims and releases; after every call the manager's exported
     table, lengths and counts match a plain model of the rules and no id or slot is held twice."""
-    rng = random.Random(5)
-    NP, NR, R, MP = 60, 24, 6, 12
-    kv = zf.KvManager(num_pages=NP, num_raw_slots=NR, page_size=P, max_requests=R, max_pages_per_req=MP)
-    model = {}                 # req -> dict(len, pages, tail_raw)
-    raw_kept = {}              # pid -> slot, full pages left raw
-    pending = {}               # pid -> slot
+    rng = random.Random(5 + layers)
+    NP, NR, R, MP = 60, 24 * layers, 6, 12
+    kv = zf.KvManager(num_pages=NP, num_raw_slots=NR, page_size=P, max_requests=R, max_pages_per_req=MP,
+                      num_layers=layers)
+    model = {}                 # req -> dict(len, pages, tail_raw: per-layer slots or None)
+    raw_kept = {}              # pid -> {layer: slot}, full pages left raw in some layers
+    pending = {}               # pid -> per-layer slots
 
     def held_slots():
-        s = [m["tail_raw"] for m in model.values() if m["tail_raw"] is not None]
-        return s + list(pending.values()) + list(raw_kept.values())
+        s = [x for m in model.values() if m["tail_raw"] is not None for x in m["tail_raw"]]
+        return s + [x for v in pending.values() for x in v] + [x for v in raw_kept.values() for x in v.values()]
+
+    def cols(rs, i):
+        return [rs[l][i] for l in range(layers)]
 
     for step in range(600):
         op = rng.random()
         free_ids = NP - sum(len(m["pages"]) for m in model.values())
         free_raw = NR - len(held_slots())
+        openable = min(free_ids, free_raw // layers)
         if op < 0.2 and len(model) < R:
             req = rng.choice([q for q in range(R) if q not in model])
             length = rng.randint(0, 70)
             need = -(-length // P)
             if need > MP:
                 continue
-            if need > min(free_ids, free_raw):
+            if need > openable:
                 with pytest.raises(zf.ZfError, match="page ids or raw slots"):
                     kv.admit(req, length)
                 continue
             ids, nv, rs = kv.admit(req, length)
-            assert nv == [min(P, length - i * P) for i in range(need)]
+            assert nv == [min(P, length - i * P) for i in range(need)] and len(rs) == layers
             m = {"len": length, "pages": ids, "tail_raw": None}
-            for pid, fill, slot in zip(ids, nv, rs):
+            for i, (pid, fill) in enumerate(zip(ids, nv)):
                 if fill == P:
-                    pending[pid] = slot
+                    pending[pid] = cols(rs, i)
                 else:
-                    m["tail_raw"] = slot
+                    m["tail_raw"] = cols(rs, i)
             model[req] = m
         elif op < 0.7 and model:
             reqs = rng.sample(sorted(model), rng.randint(1, len(model)))
             opening = [q for q in reqs if model[q]["len"] % P == 0]
             if any(-(-model[q]["len"] // P) + 1 > MP for q in opening):
                 continue
-            if len(opening) > min(free_ids, free_raw):
+            if len(opening) > openable:
                 with pytest.raises(zf.ZfError, match="page ids or raw slots"):
                     kv.append(reqs)
                 continue
             ids, nv, rs = kv.append(reqs)
-            for q, pid, fill, slot in zip(reqs, ids, nv, rs):
+            for i, (q, pid, fill) in enumerate(zip(reqs, ids, nv)):
                 m = model[q]
+                slots = cols(rs, i)
                 if m["len"] % P == 0:
                     assert pid not in m["pages"]
                     m["pages"].append(pid)
                 else:
-                    assert slot == m["tail_raw"] and pid == m["pages"][-1]
+                    assert slots == m["tail_raw"] and pid == m["pages"][-1]
                 m["len"] += 1
                 assert fill == m["len"] - (len(m["pages"]) - 1) * P
                 if fill == P:
-                    pending[pid] = slot
+                    pending[pid] = slots
                     m["tail_raw"] = None
                 else:
-                    m["tail_raw"] = slot
+                    m["tail_raw"] = slots
         elif op < 0.85 and pending:
             ids, slots = kv.pending()
-            assert dict(zip(ids, slots)) == pending
+            assert {pid: cols(slots, i) for i, pid in enumerate(ids)} == pending
             pick = rng.sample(ids, rng.randint(1, len(ids)))
-            kept = [rng.random() < 0.1 for _ in pick]
+            kept = [[rng.random() < 0.1 for _ in pick] for _ in range(layers)]
             kv.reclaim(pick, kept)
-            for pid, k in zip(pick, kept):
-                slot = pending.pop(pid)
-                if k:
-                    raw_kept[pid] = slot
+            for i, pid in enumerate(pick):
+                slots_p = pending.pop(pid)
+                keep = {l: slots_p[l] for l in range(layers) if kept[l][i]}
+                if keep:
+                    raw_kept[pid] = keep
         elif model:
             req = rng.choice(sorted(model))
             kv.release(req)
@@ -192,4 +237,6 @@ def test_random_workload_against_a_model(zf):
         st = kv.stats()
         assert st["free_pages"] == NP - len(all_ids) and st["free_raw_slots"] == NR - len(slots)
         assert st["pending_pages"] == len(pending) and st["raw_full_pages"] == len(raw_kept)
+        assert st["raw_full_slots"] == sum(len(v) for v in raw_kept.values())
+        assert st["new_page_capacity"] == min(NP - len(all_ids), (NR - len(slots)) // layers)
         assert st["tokens"] == sum(m["len"] for m in model.values())

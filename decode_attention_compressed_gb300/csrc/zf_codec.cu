@@ -1,4 +1,5 @@
-// zf_encode_pages and zf_decompress: page compression and its bit-exact inverse.
+// zf_encode_pages, zf_append_tokens and zf_decompress: page compression, token appends into
+// uncompressed pages, and the bit-exact inverse.
 //
 // ZipFusion §III.B (Lossless KV Cache Format, Fig. 2): a block is compressed when its exponents
 // fit [b, b+15], b = minimum exponent rounded down to even; each value keeps its low byte and a
@@ -19,6 +20,7 @@ namespace zf {
 
 constexpr int kCodecWarps = 8;
 constexpr int kCodecThreads = kCodecWarps * 32;
+static_assert(kCodecThreads == 2 * ZF_HEAD_DIM, "append_kernel: one thread per K and per V channel");
 
 struct CodecArgs {
   uint8_t* k_comp;
@@ -34,6 +36,7 @@ struct CodecArgs {
   const int32_t* page_ids;
   const int32_t* n_valid;
   const int32_t* raw_slots;
+  const int32_t* positions;  // append: token index within the page
   int32_t num_pages, hkv, page_size, num_raw, flags;
   int32_t raw_out;         // decompress: 1 = write the raw block layout of a dense cache
 };
@@ -42,6 +45,76 @@ struct CodecArgs {
 // channels 32*group + 16*(lane%2) .. +15 of a [P][128] page head.
 __device__ __forceinline__ size_t natural_offset(int tile, int group, int lane) {
   return static_cast<size_t>(16 * tile + (lane >> 1)) * ZF_HEAD_DIM + 32 * group + 16 * (lane & 1);
+}
+
+// One warp encodes one block.  u: this lane's 16 values at storage positions 16*lane .. +15
+// (two per word, low half first).  Writes the 784-byte slot, or sets *fail when the block needs
+// more than ZF_MAX_ESCAPES escapes.  Base: the minimum exponent rounded down to even when every
+// exponent fits [base, base+15], else the smallest even base whose window reaches the maximum
+// exponent, values below it becoming escapes.
+__device__ __forceinline__ void encode_block_lane(const uint32_t (&u)[8], uint8_t* slot, int lane, int* fail) {
+  uint32_t emin = 255, emax = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t e = ((u[j >> 1] >> (16 * (j & 1))) >> 7) & 0xFFu;
+    emin = min(emin, e);
+    emax = max(emax, e);
+  }
+  emin = __reduce_min_sync(0xFFFFFFFFu, emin);
+  emax = __reduce_max_sync(0xFFFFFFFFu, emax);
+  uint32_t base = emin & ~1u;
+  if (emax > base + 15) base = (emax - 14) & ~1u;
+
+  uint32_t code[16], lo[16], eh[16];
+  uint32_t esc_mask = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t v = (u[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+    const uint32_t e = (v >> 7) & 0xFFu;
+    lo[j] = v & 0xFFu;
+    eh[j] = e >> 1;
+    const bool esc = e < base;
+    esc_mask |= static_cast<uint32_t>(esc) << j;
+    code[j] = ((v >> 15) << 3) | (esc ? 0u : eh[j] - (base >> 1));
+  }
+  const uint32_t cnt = __popc(esc_mask);
+  uint32_t before = cnt;                       // inclusive scan over lanes
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, before, d);
+    if (lane >= d) before += t;
+  }
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, before, 31);
+  before -= cnt;
+  if (total > ZF_MAX_ESCAPES) {
+    if (lane == 0) atomicOr(fail, 1);
+    return;
+  }
+  uint4 lob;
+  lob.x = lo[0] | lo[1] << 8 | lo[2] << 16 | lo[3] << 24;
+  lob.y = lo[4] | lo[5] << 8 | lo[6] << 16 | lo[7] << 24;
+  lob.z = lo[8] | lo[9] << 8 | lo[10] << 16 | lo[11] << 24;
+  lob.w = lo[12] | lo[13] << 8 | lo[14] << 16 | lo[15] << 24;
+  *reinterpret_cast<uint4*>(slot + 16 * lane) = lob;
+  uint2 cw;
+  cw.x = (code[0] | code[4] << 4) | (code[1] | code[5] << 4) << 8 | (code[2] | code[6] << 4) << 16 |
+         (code[3] | code[7] << 4) << 24;
+  cw.y = (code[8] | code[12] << 4) | (code[9] | code[13] << 4) << 8 | (code[10] | code[14] << 4) << 16 |
+         (code[11] | code[15] << 4) << 24;
+  *reinterpret_cast<uint2*>(slot + 512 + 8 * lane) = cw;
+  uint16_t* escs = reinterpret_cast<uint16_t*>(slot + kEscapesAt);
+  if (lane < ZF_MAX_ESCAPES && static_cast<uint32_t>(lane) >= total) escs[lane] = 0;
+  uint32_t k = before;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (esc_mask & (1u << j)) {
+      escs[k] = static_cast<uint16_t>(((16 * lane + j) << 7) | eh[j]);
+      ++k;
+    }
+  }
+  if (lane == 0)
+    *reinterpret_cast<uint32_t*>(slot + kHeaderAt) =
+        (base >> 1) | (total << 8) | (static_cast<uint32_t>(ZF_FORMAT_VERSION) << 24);
 }
 
 __global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
@@ -81,20 +154,6 @@ __global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
     const uint4 x1 = *reinterpret_cast<const uint4*>(src + 8);
     const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 
-    // exponent range of the block
-    uint32_t emin = 255, emax = 0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t v = (w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-      const uint32_t e = (v >> 7) & 0xFFu;
-      emin = min(emin, e);
-      emax = max(emax, e);
-    }
-    emin = __reduce_min_sync(0xFFFFFFFFu, emin);
-    emax = __reduce_max_sync(0xFFFFFFFFu, emax);
-    uint32_t base = emin & ~1u;
-    if (emax > base + 15) base = (emax - 14) & ~1u;
-
     // scatter into storage order (this block's raw form)
     uint16_t* rblk = raw + blk * 512;
     const int tau = lane >> 1, g0 = 16 * (lane & 1);
@@ -109,57 +168,7 @@ __global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
     const uint4 y0 = *reinterpret_cast<const uint4*>(rblk + 16 * lane);
     const uint4 y1 = *reinterpret_cast<const uint4*>(rblk + 16 * lane + 8);
     const uint32_t u[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-    uint32_t code[16], lo[16], eh[16];
-    uint32_t esc_mask = 0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t v = (u[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-      const uint32_t e = (v >> 7) & 0xFFu;
-      lo[j] = v & 0xFFu;
-      eh[j] = e >> 1;
-      const bool esc = e < base;
-      esc_mask |= static_cast<uint32_t>(esc) << j;
-      code[j] = ((v >> 15) << 3) | (esc ? 0u : eh[j] - (base >> 1));
-    }
-    const uint32_t cnt = __popc(esc_mask);
-    uint32_t before = cnt;                       // inclusive scan over lanes
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, before, d);
-      if (lane >= d) before += t;
-    }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, before, 31);
-    before -= cnt;
-    if (total > ZF_MAX_ESCAPES) {
-      if (lane == 0) atomicOr(fail, 1);
-      continue;
-    }
-    uint8_t* slot = comp + blk * kSlotBytes;
-    uint4 lob;
-    lob.x = lo[0] | lo[1] << 8 | lo[2] << 16 | lo[3] << 24;
-    lob.y = lo[4] | lo[5] << 8 | lo[6] << 16 | lo[7] << 24;
-    lob.z = lo[8] | lo[9] << 8 | lo[10] << 16 | lo[11] << 24;
-    lob.w = lo[12] | lo[13] << 8 | lo[14] << 16 | lo[15] << 24;
-    *reinterpret_cast<uint4*>(slot + 16 * lane) = lob;
-    uint2 cw;
-    cw.x = (code[0] | code[4] << 4) | (code[1] | code[5] << 4) << 8 | (code[2] | code[6] << 4) << 16 |
-           (code[3] | code[7] << 4) << 24;
-    cw.y = (code[8] | code[12] << 4) | (code[9] | code[13] << 4) << 8 | (code[10] | code[14] << 4) << 16 |
-           (code[11] | code[15] << 4) << 24;
-    *reinterpret_cast<uint2*>(slot + 512 + 8 * lane) = cw;
-    uint16_t* escs = reinterpret_cast<uint16_t*>(slot + kEscapesAt);
-    if (lane < ZF_MAX_ESCAPES && static_cast<uint32_t>(lane) >= total) escs[lane] = 0;
-    uint32_t k = before;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (esc_mask & (1u << j)) {
-        escs[k] = static_cast<uint16_t>(((16 * lane + j) << 7) | eh[j]);
-        ++k;
-      }
-    }
-    if (lane == 0)
-      *reinterpret_cast<uint32_t*>(slot + kHeaderAt) =
-          (base >> 1) | (total << 8) | (static_cast<uint32_t>(ZF_FORMAT_VERSION) << 24);
+    encode_block_lane(u, comp + blk * kSlotBytes, lane, fail);
   }
   __syncthreads();
 
@@ -199,6 +208,80 @@ __global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
     else reinterpret_cast<uint4*>(dv)[t - n16] = val;
   }
   if (threadIdx.x == 0) a.dir[dir_at] = rs;
+}
+
+// Raw record index of storage position e of a block: 16-byte group 2*lane + half of the storage
+// order sits at group 32*half + lane of a raw block (the layout load_raw_lane reads).
+__device__ __forceinline__ int raw_position(int e) { return ((e >> 3) & 1) * 256 + (e >> 4) * 8 + (e & 7); }
+
+// One CTA appends one token to one (page, kv head) in its raw slot (ZipFusion §III.D: a page that
+// is still filling stays uncompressed, so a decode step writes its token in place).  Threads
+// 0-127 write the K channels, 128-255 the V channels, each to its block's raw position.  The
+// token that fills the page (position P-1) is followed by the page head's compression from the
+// slot: every warp encodes blocks from the raw record (a lane's 16 storage-order values are its
+// two 16-byte groups there), and the page goes to its compressed slot unless a block needs more
+// than ZF_MAX_ESCAPES escapes, in which case it stays in the raw slot.
+__global__ void __launch_bounds__(kCodecThreads) append_kernel(CodecArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int P = a.page_size;
+  const int nblk = P / 4;
+  uint8_t* comp = smem;                      // [2*nblk][784]
+  int* fail = reinterpret_cast<int*>(smem + 2 * nblk * kSlotBytes);
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pid = a.page_ids[i], pos = a.positions[i], rs = a.raw_slots[i];
+  if (pid < 0 || pid >= a.num_pages) {
+    if (threadIdx.x == 0) report(a.status, ZF_DEV_BAD_PAGE_ID);
+    return;
+  }
+  const size_t dir_at = static_cast<size_t>(pid) * a.hkv + h;
+  if (pos < 0 || pos >= P || rs < 0 || rs >= a.num_raw) {
+    if (threadIdx.x == 0) {
+      report(a.status, (pos < 0 || pos >= P) ? ZF_DEV_BAD_N_VALID : ZF_DEV_BAD_RAW_SLOT);
+      a.dir[dir_at] = ZF_DIR_INVALID;
+    }
+    return;
+  }
+  const size_t rec = static_cast<size_t>(nblk) * 512;            // uint16 per K (or V) record
+  uint16_t* rk = a.k_raw + (static_cast<size_t>(rs) * a.hkv + h) * rec;
+  uint16_t* rv = a.v_raw + (static_cast<size_t>(rs) * a.hkv + h) * rec;
+  {
+    const bool is_value = threadIdx.x >= ZF_HEAD_DIM;
+    const int c = threadIdx.x & (ZF_HEAD_DIM - 1);
+    const int bi = (pos >> 4) * 4 + (c >> 5);
+    const int at = bi * 512 + raw_position(block_position(is_value, pos & 15, c & 31));
+    const size_t from = (static_cast<size_t>(i) * a.hkv + h) * ZF_HEAD_DIM + c;
+    (is_value ? rv : rk)[at] = (is_value ? a.src_v : a.src_k)[from];
+  }
+  if (pos < P - 1) {
+    if (threadIdx.x == 0) a.dir[dir_at] = rs;
+    return;
+  }
+  if (threadIdx.x == 0) *fail = 0;
+  __syncthreads();                           // the token is in the slot for every warp of the CTA
+  for (int blk = warp; blk < 2 * nblk; blk += kCodecWarps) {
+    const bool is_value = blk >= nblk;
+    const int bi = is_value ? blk - nblk : blk;
+    const uint4* src = reinterpret_cast<const uint4*>((is_value ? rv : rk) + static_cast<size_t>(bi) * 512);
+    const uint4 y0 = src[lane], y1 = src[lane + 32];
+    const uint32_t u[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    encode_block_lane(u, comp + blk * kSlotBytes, lane, fail);
+  }
+  __syncthreads();
+  if (*fail) {
+    if (threadIdx.x == 0) a.dir[dir_at] = rs;
+    return;
+  }
+  const size_t crec = static_cast<size_t>(nblk) * kSlotBytes;
+  uint8_t* dk = a.k_comp + (static_cast<size_t>(pid) * a.hkv + h) * crec;
+  uint8_t* dv = a.v_comp + (static_cast<size_t>(pid) * a.hkv + h) * crec;
+  const int n16 = static_cast<int>(crec / 16);
+  for (int t = threadIdx.x; t < 2 * n16; t += kCodecThreads) {
+    const uint4 val = reinterpret_cast<const uint4*>(comp)[t];
+    if (t < n16) reinterpret_cast<uint4*>(dk)[t] = val;
+    else reinterpret_cast<uint4*>(dv)[t - n16] = val;
+  }
+  if (threadIdx.x == 0) a.dir[dir_at] = ZF_DIR_COMPRESSED;
 }
 
 __global__ void __launch_bounds__(kCodecThreads) decompress_kernel(CodecArgs a) {
@@ -296,6 +379,31 @@ extern "C" zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_
       cudaSuccess)
     return ZF_ERR_CUDA;
   encode_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
+}
+
+extern "C" zf_status zf_append_tokens(const zf_cache* cache, const uint16_t* k_tok, const uint16_t* v_tok,
+                                      const int32_t* page_ids, const int32_t* positions, const int32_t* raw_slots,
+                                      int32_t n, void* stream) {
+  zf_status st = check_cache(cache, /*need_comp=*/true, /*need_raw=*/true, /*need_dir=*/true);
+  if (st != ZF_OK) return st;
+  if (n < 0) return ZF_ERR_INVALID_ARGUMENT;
+  if (n == 0) return ZF_OK;
+  if (!k_tok || !v_tok || !page_ids || !positions || !raw_slots) return ZF_ERR_INVALID_ARGUMENT;
+  if (cache->num_kv_heads > 65535) return ZF_ERR_UNSUPPORTED;
+  CodecArgs a{};
+  a.k_comp = cache->k_comp; a.v_comp = cache->v_comp; a.k_raw = cache->k_raw; a.v_raw = cache->v_raw;
+  a.dir = cache->dir; a.status = cache->status;
+  a.src_k = k_tok; a.src_v = v_tok;
+  a.page_ids = page_ids; a.positions = positions; a.raw_slots = raw_slots;
+  a.num_pages = cache->num_pages; a.hkv = cache->num_kv_heads; a.page_size = cache->page_size;
+  a.num_raw = cache->num_raw_slots;
+  const int nblk = cache->page_size / 4;
+  const size_t smem = static_cast<size_t>(2 * nblk) * kSlotBytes + 16;
+  if (cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return ZF_ERR_CUDA;
+  append_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
 }
 

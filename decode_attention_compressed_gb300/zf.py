@@ -52,6 +52,8 @@ SIGNATURES = {
     "zf_page_head_bytes": (_c_size_t, [_c_int32, _c_int32]),
     "zf_encode_pages": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                    _c_void_p, _c_int32, _c_int32, _c_void_p]),
+    "zf_append_tokens": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                    _c_void_p, _c_int32, _c_void_p]),
     "zf_decompress": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p, _c_void_p]),
     "zf_decompress_to_raw": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p,
                                         _c_void_p]),
@@ -195,6 +197,21 @@ def encode_pages(cache: Cache, src_k, src_v, page_ids, n_valid, raw_slots=None, 
                                  ENCODE_FORCE_RAW if force_raw else 0, _stream(stream))
     _check("zf_encode_pages", code)
     return ids, nv, rs          # keep them alive until the stream has consumed them
+
+
+def append_tokens(cache: Cache, k_tok, v_tok, page_ids, positions, raw_slots, stream=None):
+    """zf_append_tokens: k_tok/v_tok [n][Hkv][128] int16 BF16 bits on the device; entry i is token
+    positions[i] of page page_ids[i], written into raw slot raw_slots[i] (the page is compressed
+    when that token fills it).  Returns the index tensors (keep them alive until the stream has
+    consumed them)."""
+    dev = cache.device
+    k_tok, v_tok = k_tok.contiguous(), v_tok.contiguous()
+    n = int(k_tok.shape[0])
+    ids, pos, rs = _dev_i32(page_ids, dev), _dev_i32(positions, dev), _dev_i32(raw_slots, dev)
+    d = cache.desc()
+    _check("zf_append_tokens", lib().zf_append_tokens(ctypes.byref(d), _ptr(k_tok), _ptr(v_tok), _ptr(ids), _ptr(pos),
+                                                       _ptr(rs), n, _stream(stream)))
+    return ids, pos, rs
 
 
 def decompress(cache: Cache, page_ids, stream=None):

@@ -134,6 +134,28 @@ zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_k, const ui
                           const int32_t* raw_slots, int32_t n, int32_t flags, void* stream);
 
 /*
+ * zf_append_tokens — write one new token into each of n uncompressed pages, in place.
+ * ZipFusion §III.D (KV Cache Management and Scheduling): a page that is still filling stays
+ * uncompressed so decoding appends its values directly; once full it is compressed under its
+ * page id.
+ *   k_tok, v_tok: [n][num_kv_heads][128] BF16: entry i is the token at index positions[i]
+ *                 (0..page_size-1) of page page_ids[i], written into raw slot raw_slots[i], which
+ *                 must already hold the page's earlier tokens (from earlier appends, or from
+ *                 zf_encode_pages with that slot and n_valid >= positions[i]).
+ *   page_ids:     [n] distinct ids in [0, num_pages); raw_slots: [n] in [0, num_raw_slots).
+ *   The directory entry of each page head becomes the raw slot; when positions[i] is
+ *   page_size - 1 the page head is then compressed from the slot into its compressed slot
+ *   (directory ZF_DIR_COMPRESSED), unless a block needs more than 6 escapes (it stays raw).
+ *   The result is bit-for-bit what zf_encode_pages writes for the page's tokens so far.  A bad
+ *   page id sets ZF_DEV_BAD_PAGE_ID; a bad position or raw slot sets ZF_DEV_BAD_N_VALID /
+ *   ZF_DEV_BAD_RAW_SLOT and makes the page's directory entries invalid.  Needs k_comp, v_comp,
+ *   k_raw, v_raw and dir; device pointers; n == 0 is a no-op.
+ */
+zf_status zf_append_tokens(const zf_cache* cache, const uint16_t* k_tok, const uint16_t* v_tok,
+                           const int32_t* page_ids, const int32_t* positions, const int32_t* raw_slots,
+                           int32_t n, void* stream);
+
+/*
  * zf_decompress — bit-exact inverse of zf_encode_pages, used for verification.
  *   page_ids: [n] ids; dst_k, dst_v: [n][num_kv_heads][page_size][128] BF16 in natural layout.
  *   A page head whose directory entry is invalid is written as zeros (and ZF_DEV_BAD_DIR set).

@@ -18,7 +18,8 @@ What it follows (the pages are summaries of three papers; the subject is ZipFusi
 * same page, §III.C (Attention over the Compressed KV Cache): keys and values are laid out for
   their operand roles in QK^T and PV; raw blocks need no reconstruction.
 * same page, §III.D (KV Cache Management and Scheduling): pages stay uncompressed while partially
-  filled; a full page is compressed later and keeps its page id.
+  filled, so decoding appends new tokens to them directly; a full page is compressed later and
+  keeps its page id.
 * same page, §IV.B (Attention Kernel Performance): attention over split chunks is finished by a
   split-result merge.
 
@@ -325,6 +326,43 @@ def encode_pages(cache: Cache, src_k, src_v, page_ids, n_valid, raw_slots, force
             else:
                 cache.dir[pid, h] = DIR_INVALID
                 cache.status |= ST_BAD_RAW_SLOT
+
+
+def append_tokens(cache: Cache, k_tok, v_tok, page_ids, positions, raw_slots):
+    """Append one token to each of n pages (ZipFusion §III.D: a page that is still filling stays
+    uncompressed, so a decode step writes its new token straight into it; a page that is full is
+    compressed under its page id).
+
+    k_tok/v_tok [n][Hkv][128] BF16 bits: entry i is token positions[i] of page page_ids[i].  Step 1
+    puts the token into the page's raw record in slot raw_slots[i] (which holds the page's earlier
+    tokens) and points the directory at that slot.  Step 2, only when the token is the page's last
+    (position P-1): the page head, now full, is encoded as encode_pages would encode it and goes
+    to its compressed slot, or stays in the raw slot if a block cannot be encoded.
+    """
+    P = cache.page_size
+    for i, pid in enumerate(page_ids):
+        pid, pos, slot = int(pid), int(positions[i]), int(raw_slots[i])
+        if not 0 <= pid < cache.num_pages:
+            cache.status |= ST_BAD_PAGE_ID
+            continue
+        if not 0 <= pos < P or not 0 <= slot < cache.num_raw:
+            cache.status |= ST_BAD_N_VALID if not 0 <= pos < P else ST_BAD_RAW_SLOT
+            cache.dir[pid, :] = DIR_INVALID
+            continue
+        for h in range(cache.num_kv_heads):
+            k, v = decode_page_head("raw", cache.k_raw[slot, h], cache.v_raw[slot, h], P)
+            k[pos] = k_tok[i, h]
+            v[pos] = v_tok[i, h]
+            _, rk, rv = encode_page_head(k, v, pos + 1, force_raw=True)
+            cache.k_raw[slot, h] = rk
+            cache.v_raw[slot, h] = rv
+            cache.dir[pid, h] = slot
+            if pos == P - 1:
+                kind, ck, cv = encode_page_head(k, v, P)
+                if kind == "comp":
+                    cache.k_comp[pid, h] = ck
+                    cache.v_comp[pid, h] = cv
+                    cache.dir[pid, h] = DIR_COMPRESSED
 
 
 def read_page_head(cache: Cache, pid: int, h: int):

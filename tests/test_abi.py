@@ -86,6 +86,22 @@ def test_decompress_rejects_bad_arguments(zf):
     assert f(ctypes.byref(d), 0x1000, 0, 0x2000, 0x3000, None) == 0
 
 
+def test_append_rejects_bad_arguments_before_launch(zf):
+    f = zf.lib().zf_append_tokens
+
+    def call(desc, n=1, tok=0x10000, ids=0x20000, pos=0x30000, slots=0x40000):
+        return f(ctypes.byref(desc) if desc is not None else None, tok, tok, ids, pos, slots, n, None)
+    assert call(None) == -1
+    assert call(_desc(zf, k_raw=None)) == -1                     # needs the raw pools
+    assert call(_desc(zf, k_comp=None)) == -1                    # and the compressed ones
+    assert call(_desc(zf, v_raw=0x4008)) == -1                   # misaligned raw pool
+    assert call(_desc(zf), tok=None) == -1
+    assert call(_desc(zf), pos=None) == -1
+    assert call(_desc(zf), slots=None) == -1
+    assert call(_desc(zf), n=-1) == -1
+    assert call(_desc(zf), n=0) == 0                             # nothing to do, nothing launched
+
+
 def _attn(zf, desc, batch=2, hq=8, max_pages=4, q=0x10000, out=0x20000, lse=0x30000, ws=0x40000, ws_bytes=1 << 20,
           dense=False, scale=0.1):
     f = zf.lib().zf_dense_decode_attn if dense else zf.lib().zf_decode_attn

@@ -361,10 +361,10 @@ def test_multi_token_full_size_sampled(zf):
 
 def test_decode_loop_through_the_page_manager(zf):
     """A serving loop driven by zf_kv over two layers whose caches share one raw-slot pool: three
-    prompts admitted (their pages encoded as listed, per layer), 24 decode steps that each append
-    one token per request (the listed tail pages re-encoded, raw while partial, compressed when
-    full), raw slots reclaimed layer by layer from the directories after every encode, one request
-    released and another admitted mid-way.  Layer 1's keys carry a spike every 24 tokens, so the
+    prompts admitted (their pages written by zf_encode_pages, per layer), 24 decode steps that each
+    append one token per request with zf_append_tokens (written in place into the raw tail page,
+    which is compressed when it fills), raw slots reclaimed layer by layer from the directories
+    after every step, one request released and another admitted mid-way.  Layer 1's keys carry a spike every 24 tokens, so the
     pages holding one stay raw in layer 1 only and their layer-0 slots go back to the pool for
     either layer to reuse.  At several steps each layer's attention over the exported page table
     matches the float64 attention over each request's token stream."""
@@ -444,8 +444,11 @@ def test_decode_loop_through_the_page_manager(zf):
             reclaim()
         reqs = sorted(stream_of)
         ids, nv, rs = kv.append(reqs)
-        for i, (req, pid, fill) in enumerate(zip(reqs, ids, nv)):
-            write(req, [pid], [fill], [[rs[layer][i]] for layer in range(NL)])
+        lens = kv.export()[1]
+        for layer in range(NL):             # the new token of each request, written in place
+            k_tok = torch.stack([streams_k[layer][stream_of[q]][int(lens[q]) - 1] for q in reqs])
+            v_tok = torch.stack([streams_v[layer][stream_of[q]][int(lens[q]) - 1] for q in reqs])
+            zf.append_tokens(caches[layer], k_tok.to(dev), v_tok.to(dev), ids, [f - 1 for f in nv], rs[layer])
         reclaim()
         if step % 6 == 5:
             check()

@@ -164,3 +164,65 @@ def test_decompress_to_raw_matches_a_raw_encode_and_attends(zf, name):
     ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q), oc, layer.page_table.numpy(), layer.seq_lens.numpy(),
                                           layer.scale)
     H.compare_attention(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_append_tokens_matches_oracle_bit_exactly(zf, P):
+    """zf_append_tokens against the oracle: pages filled one token per call (the adversarial pages
+    above plus two normal ones; two pages start as partial pages written by zf_encode_pages, the
+    rest from stale slot contents), compared bit for bit — every raw slot, the compressed slots the
+    directory points at, directory and status — at the first, middle and last token."""
+    rng = np.random.default_rng(200 + P)
+    hkv = 2
+    ak, av = adversarial_pages(seed=P, hkv=hkv, P=P)
+    nk = ((rng.standard_normal((2, hkv, P, 128)).astype(np.float32).view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
+    nvv = ((rng.standard_normal((2, hkv, P, 128)).astype(np.float32).view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
+    k = np.concatenate([ak, nk])
+    v = np.concatenate([av, nvv])
+    n = k.shape[0]
+    ids = [int(x) for x in rng.permutation(n + 2)[:n]]
+    slots = [int(x) for x in rng.permutation(n + 1)[:n]]
+    gc = zf.Cache(n + 2, hkv, P, n + 1)
+    oc = O.Cache(num_pages=n + 2, num_kv_heads=hkv, page_size=P, num_raw=n + 1)
+    oc.k_raw[:] = rng.integers(0, 1 << 16, oc.k_raw.shape, dtype=np.uint16)
+    oc.v_raw[:] = rng.integers(0, 1 << 16, oc.v_raw.shape, dtype=np.uint16)
+    gc.k_raw.copy_(torch.from_numpy(oc.k_raw.view(np.int16).reshape(gc.k_raw.shape)))
+    gc.v_raw.copy_(torch.from_numpy(oc.v_raw.view(np.int16).reshape(gc.v_raw.shape)))
+    kt = torch.from_numpy(k.view(np.int16).copy()).cuda()
+    vt = torch.from_numpy(v.view(np.int16).copy()).cuda()
+    start = {0: 3, n - 1: P // 2}                           # call index -> tokens already encoded
+    for i, t0 in start.items():
+        zf.encode_pages(gc, kt[i:i + 1], vt[i:i + 1], [ids[i]], [t0], [slots[i]])
+        O.encode_pages(oc, k[i:i + 1], v[i:i + 1], [ids[i]], [t0], [slots[i]])
+    for t in range(P):
+        sel = [i for i in range(n) if t >= start.get(i, 0)]
+        zf.append_tokens(gc, kt[sel, :, t], vt[sel, :, t], [ids[i] for i in sel], [t] * len(sel),
+                         [slots[i] for i in sel])
+        O.append_tokens(oc, k[sel][:, :, t], v[sel][:, :, t], [ids[i] for i in sel], [t] * len(sel),
+                        [slots[i] for i in sel])
+        if t in (0, P // 2, P - 1):
+            torch.cuda.synchronize()
+            H.assert_caches_equal(gc, oc)
+            assert (H.np_bits(gc.k_raw) == oc.k_raw.reshape(gc.k_raw.shape)).all()
+            assert (H.np_bits(gc.v_raw) == oc.v_raw.reshape(gc.v_raw.shape)).all()
+    assert (oc.dir[ids] == O.DIR_COMPRESSED).any() and (oc.dir[ids] >= 0).any()
+    dk, dv = zf.decompress(gc, ids)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, kt) and torch.equal(dv, vt)
+
+
+def test_append_tokens_reports_bad_entries(zf):
+    P, hkv = 16, 2
+    gc = zf.Cache(3, hkv, P, 2)
+    gc.k_raw.zero_()
+    gc.v_raw.zero_()
+    oc = O.Cache(num_pages=3, num_kv_heads=hkv, page_size=P, num_raw=2)
+    tok = np.arange(4 * hkv * 128, dtype=np.uint16).reshape(4, hkv, 128)
+    tt = torch.from_numpy(tok.view(np.int16).copy()).cuda()
+    ids, pos, slots = [0, 7, 1, 2], [0, 0, P, 5], [1, 0, 0, 2]   # good, bad id, bad position, bad slot
+    zf.append_tokens(gc, tt, tt, ids, pos, slots)
+    O.append_tokens(oc, tok, tok, ids, pos, slots)
+    torch.cuda.synchronize()
+    assert gc.status_word() == oc.status == (O.ST_BAD_PAGE_ID | O.ST_BAD_N_VALID | O.ST_BAD_RAW_SLOT)
+    H.assert_caches_equal(gc, oc)
+    assert (oc.dir[0] == 1).all() and (oc.dir[1:] == O.DIR_INVALID).all()

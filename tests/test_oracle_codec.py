@@ -323,3 +323,53 @@ def test_page_lifecycle(P):
     forced = O.Cache(num_pages=6, num_kv_heads=H, page_size=P, num_raw=6)
     O.encode_pages(forced, src_k, src_v, page_ids, [P] * 5, list(range(5)), force_raw=True)
     assert (forced.dir[page_ids] == np.arange(5)[:, None]).all()
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_appending_a_page_token_by_token_equals_encoding_it(P):
+    """ZipFusion §III.D: a page fills uncompressed, a token at a time, and is compressed once
+    full.  Appending its tokens one by one into a raw slot (starting from stale slot contents, or
+    from a partial page that encode_pages stored raw) must leave exactly what encode_pages leaves
+    for the same tokens: the first t tokens readable after t appends, and when full the same
+    compressed slots (or the same raw record, for a page that cannot be encoded)."""
+    rng = np.random.default_rng(100 + P)
+    H = 2
+    src_k = np.stack([np.stack([_page(rng, P, wide=(i == 2 and h == 0)) for h in range(H)]) for i in range(3)])
+    src_v = np.stack([np.stack([_page(rng, P) for h in range(H)]) for i in range(3)])
+    ref = O.Cache(num_pages=4, num_kv_heads=H, page_size=P, num_raw=3)
+    O.encode_pages(ref, src_k, src_v, [3, 0, 1], [P, P, P], [0, 1, 2])
+    app = O.Cache(num_pages=4, num_kv_heads=H, page_size=P, num_raw=3)
+    app.k_raw[:] = rng.integers(0, 1 << 16, app.k_raw.shape, dtype=np.uint16)   # stale slot contents
+    app.v_raw[:] = rng.integers(0, 1 << 16, app.v_raw.shape, dtype=np.uint16)
+    k_start = 5                                         # page 0 starts as a 5-token partial page
+    O.encode_pages(app, src_k[1:2], src_v[1:2], [0], [k_start], [1])
+    assert (app.dir[0] == 1).all()
+    for t in range(P):
+        sel = [i for i in range(3) if not (i == 1 and t < k_start)]
+        O.append_tokens(app, src_k[sel][:, :, t], src_v[sel][:, :, t], [[3, 0, 1][i] for i in sel], [t] * len(sel),
+                        [[0, 1, 2][i] for i in sel])
+        for i, pid in enumerate([3, 0, 1]):
+            kv = O.read_page_head(app, pid, 0)
+            assert (kv[0][: t + 1] == src_k[i, 0, : t + 1]).all() and (kv[1][: t + 1] == src_v[i, 0, : t + 1]).all()
+            if t < P - 1:
+                assert (app.dir[pid] == [0, 1, 2][i]).all()
+    assert app.status == 0
+    assert (app.dir == ref.dir).all()
+    assert app.dir[1, 0] == 2 and app.dir[3, 0] == O.DIR_COMPRESSED     # the wide page head stays raw
+    comp = ref.dir == O.DIR_COMPRESSED
+    assert (app.k_comp[comp] == ref.k_comp[comp]).all() and (app.v_comp[comp] == ref.v_comp[comp]).all()
+    assert (app.k_raw[2, 0] == ref.k_raw[2, 0]).all() and (app.v_raw[2, 0] == ref.v_raw[2, 0]).all()
+
+
+def test_append_errors():
+    P, H = 16, 2
+    c = O.Cache(num_pages=2, num_kv_heads=H, page_size=P, num_raw=1)
+    tok = np.zeros((1, H, 128), np.uint16)
+    O.append_tokens(c, tok, tok, [2], [0], [0])
+    assert c.status == O.ST_BAD_PAGE_ID and (c.dir == O.DIR_INVALID).all()
+    c.dir[:] = 0
+    O.append_tokens(c, tok, tok, [1], [P], [0])
+    assert c.status & O.ST_BAD_N_VALID and (c.dir[1] == O.DIR_INVALID).all() and (c.dir[0] == 0).all()
+    c.dir[:] = 0
+    O.append_tokens(c, tok, tok, [0], [3], [1])
+    assert c.status & O.ST_BAD_RAW_SLOT and (c.dir[0] == O.DIR_INVALID).all() and (c.dir[1] == 0).all()

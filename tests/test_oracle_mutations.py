@@ -109,3 +109,28 @@ def test_multi_token_off_by_one_is_caught(monkeypatch):
     real_multi = O.decode_attention_multi
     monkeypatch.setattr(O, "decode_attention_multi", bad_multi)
     _fails(TA.test_multi_token_identical_keys_give_mean_of_the_visible_values)
+
+
+def test_append_with_swapped_k_and_v_is_caught(monkeypatch):
+    real = O.append_tokens
+    monkeypatch.setattr(O, "append_tokens", lambda c, k, v, *rest: real(c, v, k, *rest))
+    _fails(TC.test_appending_a_page_token_by_token_equals_encoding_it, 16)
+
+
+def test_append_that_never_compresses_is_caught(monkeypatch):
+    real = O.encode_page_head
+    monkeypatch.setattr(O, "append_tokens", _append_without_step_2(real))
+    _fails(TC.test_appending_a_page_token_by_token_equals_encoding_it, 16)
+
+
+def _append_without_step_2(encode_page_head):
+    def bad(cache, k_tok, v_tok, page_ids, positions, raw_slots):
+        P = cache.page_size
+        for i, pid in enumerate(page_ids):
+            pos, slot = int(positions[i]), int(raw_slots[i])
+            for h in range(cache.num_kv_heads):
+                k, v = O.decode_page_head("raw", cache.k_raw[slot, h], cache.v_raw[slot, h], P)
+                k[pos], v[pos] = k_tok[i, h], v_tok[i, h]
+                _, cache.k_raw[slot, h], cache.v_raw[slot, h] = encode_page_head(k, v, pos + 1, force_raw=True)
+                cache.dir[int(pid), h] = slot
+    return bad

@@ -339,8 +339,9 @@ def _i32(values):
 
 class KvManager:
     """zf_kv: host-side page manager (page ids for all layers, one raw-slot pool shared by
-    num_layers layers).  admit/append return the encode list (page_ids, n_valid, raw_slots) with
-    raw_slots[l] the slot list of layer l's zf_encode_pages call."""
+    num_layers layers).  admit/append return the write list (page_ids, n_valid, raw_slots) with
+    raw_slots[l] the slot list of layer l's call: encode_pages for a prompt, append_tokens
+    (positions n_valid - 1) for a decode step."""
 
     def __init__(self, num_pages, num_raw_slots, page_size, max_requests, max_pages_per_req, num_layers=1):
         self.page_size, self.max_requests, self.max_pages = page_size, max_requests, max_pages_per_req

@@ -304,9 +304,10 @@ zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t* q, int32_
  * slot until the request is released.  With num_layers = 1 the same bookkeeping also serves
  * per-layer raw pools addressed by one slot index (report a page raw when it is raw in any layer).
  * Per-layer outputs and inputs are layer-major: entry (layer l, item i) of an n-item list is at
- * l * n + i, so row l is the raw_slots array of layer l's zf_encode_pages call.  The manager only
- * does the bookkeeping: the caller writes the listed pages with zf_encode_pages and uploads the
- * page table and lengths.
+ * l * n + i, so row l is the raw_slots array of layer l's zf_encode_pages / zf_append_tokens
+ * call.  The manager only does the bookkeeping: the caller writes the listed pages (a prompt with
+ * zf_encode_pages, a decode step's tokens with zf_append_tokens) and uploads the page table and
+ * lengths.
  * Host code; not thread-safe; no GPU calls.
  * ------------------------------------------------------------------------------------------ */
 typedef struct zf_kv zf_kv;
@@ -340,10 +341,11 @@ zf_status zf_kv_admit(zf_kv* kv, int32_t req, int32_t len, int32_t* page_ids, in
 
 /* One new token for each of the n distinct active requests reqs[i]: entry i of the outputs is the
  * page that holds it (page_ids[i], tokens in it n_valid[i], its raw slot in layer l
- * raw_slots[l * n + i]) — one zf_encode_pages call per layer writes them all.  A request whose
- * last page is full opens a new page (an id + a raw slot per layer) first; a page that becomes
- * full here is compressed by those encodes and its raw slots are pending until zf_kv_reclaim.
- * All or nothing: ZF_ERR_CAPACITY (or an invalid request) changes no request. */
+ * raw_slots[l * n + i]) — one zf_append_tokens call per layer (positions n_valid[i] - 1) writes
+ * them all.  A request whose last page is full opens a new page (an id + a raw slot per layer)
+ * first; a page that becomes full here is compressed by those calls and its raw slots are
+ * pending until zf_kv_reclaim.  All or nothing: ZF_ERR_CAPACITY (or an invalid request) changes
+ * no request. */
 zf_status zf_kv_append(zf_kv* kv, const int32_t* reqs, int32_t n, int32_t* page_ids, int32_t* n_valid,
                        int32_t* raw_slots);
 

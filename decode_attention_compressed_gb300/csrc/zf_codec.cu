@@ -1,5 +1,5 @@
-// zf_encode_pages, zf_append_tokens and zf_decompress: page compression, token appends into
-// uncompressed pages, and the bit-exact inverse.
+// zf_encode_pages, zf_append_tokens, zf_decompress and zf_validate_pages: page compression,
+// token appends into uncompressed pages, the bit-exact inverse, and a check of stored metadata.
 //
 // ZipFusion §III.B (Lossless KV Cache Format, Fig. 2): a block is compressed when its exponents
 // fit [b, b+15], b = minimum exponent rounded down to even; each value keeps its low byte and a
@@ -284,6 +284,78 @@ __global__ void __launch_bounds__(kCodecThreads) append_kernel(CodecArgs a) {
   if (threadIdx.x == 0) a.dir[dir_at] = ZF_DIR_COMPRESSED;
 }
 
+// Metadata check of one compressed slot (shared by the device validator and the host entry).
+// The header word is b/2 (bits 0-6) | escape count (bits 8-10) | format version (bits 24-31);
+// every other bit is zero, at most ZF_MAX_ESCAPES escapes are listed with strictly ascending
+// positions, and unused entries are 0.
+__host__ __device__ inline bool slot_header_ok(uint32_t header, const uint16_t (&esc)[ZF_MAX_ESCAPES]) {
+  const uint32_t n_esc = (header >> 8) & 0x7u;
+  if ((header >> 24) != ZF_FORMAT_VERSION || (header & 0x00FFF880u) != 0 || n_esc > ZF_MAX_ESCAPES)
+    return false;
+  int last = -1;
+  for (int k = 0; k < ZF_MAX_ESCAPES; ++k) {
+    if (static_cast<uint32_t>(k) < n_esc) {
+      const int p = esc[k] >> 7;
+      if (p <= last) return false;
+      last = p;
+    } else if (esc[k] != 0) {
+      return false;
+    }
+  }
+  return true;
+}
+
+// ... and every code's offset added to b/2 stays within 7 bits (the rebuild's additions carry
+// into no sign bit, ZipFusion §III.C), which can only fail when b/2 > 120.
+__host__ __device__ inline bool slot_ok(const uint8_t* slot) {
+  uint32_t header = 0;
+  for (int b = 0; b < 4; ++b) header |= static_cast<uint32_t>(slot[kHeaderAt + b]) << (8 * b);
+  uint16_t esc[ZF_MAX_ESCAPES];
+  for (int k = 0; k < ZF_MAX_ESCAPES; ++k)
+    esc[k] = static_cast<uint16_t>(slot[kEscapesAt + 2 * k] | slot[kEscapesAt + 2 * k + 1] << 8);
+  if (!slot_header_ok(header, esc)) return false;
+  const uint32_t half_base = header & 0x7Fu;
+  if (half_base > 120) {
+    for (int j = 0; j < 256; ++j) {
+      const uint32_t c = slot[512 + j];
+      if (half_base + (c & 7u) > 127 || half_base + ((c >> 4) & 7u) > 127) return false;
+    }
+  }
+  return true;
+}
+
+// One CTA per (page, kv head): thread t checks slot t of the page head's K and V records.
+__global__ void __launch_bounds__(kCodecThreads) validate_kernel(CodecArgs a, int32_t* bad) {
+  const int P = a.page_size;
+  const int nblk = P / 4;
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int pid = a.page_ids[i];
+  if (pid < 0 || pid >= a.num_pages) {
+    if (threadIdx.x == 0) {
+      report(a.status, ZF_DEV_BAD_PAGE_ID);
+      if (bad) bad[i] = 1;
+    }
+    return;
+  }
+  const int d = a.dir[static_cast<size_t>(pid) * a.hkv + h];
+  if (d != ZF_DIR_COMPRESSED) {
+    if (threadIdx.x == 0 && (d < 0 || d >= a.num_raw)) {
+      report(a.status, ZF_DEV_BAD_DIR);
+      if (bad) bad[i] = 1;
+    }
+    return;
+  }
+  for (int t = threadIdx.x; t < 2 * nblk; t += kCodecThreads) {
+    const bool is_value = t >= nblk;
+    const uint8_t* slot = (is_value ? a.v_comp : a.k_comp) +
+                          ((static_cast<size_t>(pid) * a.hkv + h) * nblk + (is_value ? t - nblk : t)) * kSlotBytes;
+    if (!slot_ok(slot)) {
+      report(a.status, ZF_DEV_BAD_SLOT);
+      if (bad) bad[i] = 1;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kCodecThreads) decompress_kernel(CodecArgs a) {
   __shared__ __align__(16) uint16_t stage[kCodecWarps][512];
   const int P = a.page_size;
@@ -406,6 +478,25 @@ extern "C" zf_status zf_append_tokens(const zf_cache* cache, const uint16_t* k_t
   append_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
 }
+
+extern "C" zf_status zf_validate_pages(const zf_cache* cache, const int32_t* page_ids, int32_t n, int32_t* bad,
+                                       void* stream) {
+  zf_status st = check_cache(cache, /*need_comp=*/true, /*need_raw=*/false, /*need_dir=*/true);
+  if (st != ZF_OK) return st;
+  if (n < 0) return ZF_ERR_INVALID_ARGUMENT;
+  if (n == 0) return ZF_OK;
+  if (!page_ids || (reinterpret_cast<uintptr_t>(bad) & 3u)) return ZF_ERR_INVALID_ARGUMENT;
+  if (cache->num_kv_heads > 65535) return ZF_ERR_UNSUPPORTED;
+  CodecArgs a{};
+  a.k_comp = cache->k_comp; a.v_comp = cache->v_comp; a.dir = cache->dir; a.status = cache->status;
+  a.page_ids = page_ids;
+  a.num_pages = cache->num_pages; a.hkv = cache->num_kv_heads; a.page_size = cache->page_size;
+  a.num_raw = cache->num_raw_slots;
+  validate_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, 0, static_cast<cudaStream_t>(stream)>>>(a, bad);
+  return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
+}
+
+extern "C" int32_t zf_slot_is_valid(const uint8_t* slot) { return slot && slot_ok(slot) ? 1 : 0; }
 
 static zf_status launch_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n, uint16_t* dst_k,
                                    uint16_t* dst_v, int raw_out, void* stream) {

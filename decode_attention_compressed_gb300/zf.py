@@ -21,7 +21,7 @@ DIR_COMPRESSED = -1
 DIR_INVALID = -2
 ENCODE_FORCE_RAW = 1
 DEV_BAD_PAGE_ID, DEV_BAD_RAW_SLOT, DEV_BAD_N_VALID = 0x1, 0x2, 0x4
-DEV_BAD_SEQ_LEN, DEV_BAD_DIR, DEV_TIMEOUT = 0x8, 0x10, 0x20
+DEV_BAD_SEQ_LEN, DEV_BAD_DIR, DEV_TIMEOUT, DEV_BAD_SLOT = 0x8, 0x10, 0x20, 0x40
 
 _c_int32, _c_void_p, _c_size_t, _c_float = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
 
@@ -54,6 +54,8 @@ SIGNATURES = {
                                    _c_void_p, _c_int32, _c_int32, _c_void_p]),
     "zf_append_tokens": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                     _c_void_p, _c_int32, _c_void_p]),
+    "zf_validate_pages": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p]),
+    "zf_slot_is_valid": (_c_int32, [_c_void_p]),
     "zf_decompress": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p, _c_void_p]),
     "zf_decompress_to_raw": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_void_p, _c_void_p,
                                         _c_void_p]),
@@ -212,6 +214,24 @@ def append_tokens(cache: Cache, k_tok, v_tok, page_ids, positions, raw_slots, st
     _check("zf_append_tokens", lib().zf_append_tokens(ctypes.byref(d), _ptr(k_tok), _ptr(v_tok), _ptr(ids), _ptr(pos),
                                                        _ptr(rs), n, _stream(stream)))
     return ids, pos, rs
+
+
+def validate_pages(cache: Cache, page_ids, stream=None):
+    """zf_validate_pages: an int32 device tensor, 1 for each listed page whose stored form has a
+    problem (the cache's status word says which kind)."""
+    dev = cache.device
+    ids = _dev_i32(page_ids, dev)
+    bad = torch.zeros(int(ids.numel()), dtype=torch.int32, device=dev)
+    d = cache.desc()
+    _check("zf_validate_pages", lib().zf_validate_pages(ctypes.byref(d), _ptr(ids), int(ids.numel()), _ptr(bad),
+                                                         _stream(stream)))
+    return bad
+
+
+def slot_is_valid(slot) -> bool:
+    """zf_slot_is_valid on one 784-byte compressed slot held in host memory (bytes or uint8 array)."""
+    buf = (ctypes.c_uint8 * SLOT_BYTES).from_buffer_copy(bytes(slot)[:SLOT_BYTES].ljust(SLOT_BYTES, b"\0"))
+    return bool(lib().zf_slot_is_valid(ctypes.addressof(buf)))
 
 
 def decompress(cache: Cache, page_ids, stream=None):

@@ -71,6 +71,7 @@ typedef int32_t zf_status;
 #define ZF_DEV_BAD_SEQ_LEN 0x8         /* seq_len outside [0, max_pages_per_req * page_size] */
 #define ZF_DEV_BAD_DIR 0x10            /* directory entry neither compressed nor a valid raw slot */
 #define ZF_DEV_TIMEOUT 0x20            /* a shared-memory pipeline wait gave up */
+#define ZF_DEV_BAD_SLOT 0x40           /* zf_validate_pages: a compressed slot's metadata is malformed */
 
 #define ZF_HEAD_DIM 128
 #define ZF_BLOCK_TOKENS 16
@@ -154,6 +155,25 @@ zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_k, const ui
 zf_status zf_append_tokens(const zf_cache* cache, const uint16_t* k_tok, const uint16_t* v_tok,
                            const int32_t* page_ids, const int32_t* positions, const int32_t* raw_slots,
                            int32_t n, void* stream);
+
+/*
+ * zf_validate_pages — check the stored form of n pages, for example after a cache was saved to a
+ * file and loaded again (its pools are plain bytes).  Per page head: the directory entry must be
+ * ZF_DIR_COMPRESSED or a raw slot in [0, num_raw_slots) (else ZF_DEV_BAD_DIR); every K and V
+ * slot of a compressed page head must pass zf_slot_is_valid (else ZF_DEV_BAD_SLOT).  Raw records
+ * hold plain BF16 values, where every bit pattern is valid.  Bad page ids set ZF_DEV_BAD_PAGE_ID.
+ *   page_ids: [n] device; bad: optional [n] device int32, set to 1 for each page with a problem
+ *   (entries of good pages are left as they are: zero it first).  Needs k_comp, v_comp and dir.
+ */
+zf_status zf_validate_pages(const zf_cache* cache, const int32_t* page_ids, int32_t n, int32_t* bad,
+                            void* stream);
+
+/* One 784-byte compressed slot in host memory: 1 when its metadata is well formed — format
+ * version 1, header bits 7 and 11-23 zero, at most 6 escapes, escape positions strictly
+ * ascending, unused escape entries zero, and base/2 + every code's 3-bit offset within 7 bits
+ * (the rebuild adds them without a carry, ZipFusion §III.C) — else 0.  The same test
+ * zf_validate_pages runs on the device. */
+int32_t zf_slot_is_valid(const uint8_t* slot);
 
 /*
  * zf_decompress — bit-exact inverse of zf_encode_pages, used for verification.

@@ -218,6 +218,10 @@ def decode_block(slot: np.ndarray, role: str) -> np.ndarray:
     lo = slot[LOW_AT:LOW_AT + 512].astype(np.int64)
     packed = slot[CODES_AT:CODES_AT + 256].astype(np.int64).reshape(64, 4)
     code = np.concatenate([packed & 0xF, packed >> 4], axis=1).ravel()
+    # ZipFusion §III.C: b/2 + offset is the 7-bit field exponent >> 1, rebuilt without a carry
+    # into the sign bit; a slot whose sum leaves 7 bits cannot come from any BF16 value
+    if half_base + int((code & 7).max()) > 127:
+        raise ValueError("exponent offset carries out of 7 bits")
     hi = ((code >> 3) << 7) | (half_base + (code & 7))
     for p, eh in esc:
         hi[p] = (hi[p] & 0x80) | eh

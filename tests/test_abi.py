@@ -102,6 +102,18 @@ def test_append_rejects_bad_arguments_before_launch(zf):
     assert call(_desc(zf), n=0) == 0                             # nothing to do, nothing launched
 
 
+def test_validate_rejects_bad_arguments_before_launch(zf):
+    f = zf.lib().zf_validate_pages
+    d = _desc(zf)
+    assert f(None, 0x1000, 1, 0x2000, None) == -1
+    assert f(ctypes.byref(_desc(zf, k_comp=None)), 0x1000, 1, 0x2000, None) == -1
+    assert f(ctypes.byref(d), None, 1, 0x2000, None) == -1
+    assert f(ctypes.byref(d), 0x1000, 1, 0x2002, None) == -1       # misaligned flag array
+    assert f(ctypes.byref(d), 0x1000, -1, 0x2000, None) == -1
+    assert f(ctypes.byref(d), 0x1000, 0, 0x2000, None) == 0
+    assert zf.lib().zf_slot_is_valid(None) == 0
+
+
 def _attn(zf, desc, batch=2, hq=8, max_pages=4, q=0x10000, out=0x20000, lse=0x30000, ws=0x40000, ws_bytes=1 << 20,
           dense=False, scale=0.1):
     f = zf.lib().zf_dense_decode_attn if dense else zf.lib().zf_decode_attn

@@ -226,3 +226,53 @@ def test_append_tokens_reports_bad_entries(zf):
     assert gc.status_word() == oc.status == (O.ST_BAD_PAGE_ID | O.ST_BAD_N_VALID | O.ST_BAD_RAW_SLOT)
     H.assert_caches_equal(gc, oc)
     assert (oc.dir[0] == 1).all() and (oc.dir[1:] == O.DIR_INVALID).all()
+
+
+def test_validate_pages_flags_exactly_the_damaged_pages(zf):
+    """zf_validate_pages after damage to stored metadata: random header / escape bytes of some
+    compressed slots, a code that would carry, a directory entry pointing past the raw slots, and
+    an id out of range.  The pages flagged are exactly those with a slot the oracle's decoder
+    rejects or a bad directory entry; the status word names the kinds."""
+    layer = I.make_layer(SMALL["llama3_8b_batched"])
+    gc = H.gpu_cache_from(layer, zf)
+    n = layer.num_pages
+    bad = zf.validate_pages(gc, list(range(n)) + [n + 5])
+    torch.cuda.synchronize()
+    assert bad[:n].sum().item() == 0 and bad[n].item() == 1 and gc.status_word() == zf.DEV_BAD_PAGE_ID
+    gc.status.zero_()
+    d = gc.dir.cpu().numpy()
+    comp, raw = np.argwhere(d == -1), np.argwhere(d >= 0)
+    assert len(comp) > 10 and len(raw) > 0
+    rng = np.random.default_rng(5)
+    nblk = gc.page_size // 4
+    for p, h in comp[rng.choice(len(comp), 8, replace=False)]:
+        pool = gc.k_comp if rng.integers(2) else gc.v_comp
+        at = int(rng.integers(nblk)) * 784 + int(rng.integers(768, 784))
+        pool[p, h, at] = int(rng.integers(256))
+    p, h = comp[rng.integers(len(comp))]
+    gc.k_comp[p, h, 768] = 127                             # b/2 = 127: any nonzero offset carries
+    gc.k_comp[p, h, 512] = 0x01
+    p, h = raw[0]
+    gc.dir[p, h] = gc.num_raw_slots + 3
+    bad = zf.validate_pages(gc, list(range(n)))
+    torch.cuda.synchronize()
+    kc, vc, dd = gc.k_comp.cpu().numpy(), gc.v_comp.cpu().numpy(), gc.dir.cpu().numpy()
+    want = np.zeros(n, np.int32)
+    kinds = 0
+    for pid in range(n):
+        for hh in range(gc.num_kv_heads):
+            e = dd[pid, hh]
+            if e == -1:
+                for rec in (kc[pid, hh], vc[pid, hh]):
+                    for b in range(nblk):
+                        try:
+                            O.decode_block(rec[b * 784:(b + 1) * 784], "k")
+                        except ValueError:
+                            want[pid] = 1
+                            kinds |= zf.DEV_BAD_SLOT
+            elif not 0 <= e < gc.num_raw_slots:
+                want[pid] = 1
+                kinds |= zf.DEV_BAD_DIR
+    assert want.sum() >= 3 and kinds == zf.DEV_BAD_SLOT | zf.DEV_BAD_DIR
+    assert (bad.cpu().numpy() == want).all()
+    assert gc.status_word() == kinds

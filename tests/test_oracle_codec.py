@@ -373,3 +373,19 @@ def test_append_errors():
     c.dir[:] = 0
     O.append_tokens(c, tok, tok, [0], [3], [1])
     assert c.status & O.ST_BAD_RAW_SLOT and (c.dir[0] == O.DIR_INVALID).all() and (c.dir[1] == 0).all()
+
+
+def test_offsets_that_would_carry_are_rejected():
+    """ZipFusion §III.C: high bytes are rebuilt by adding b/2 to 3-bit offsets with no carry into
+    the sign bit, so b/2 + offset <= 127 for every code.  Exponents {254, 255} give b/2 = 127 with
+    offset 0 only; a code with offset 1 there would carry and cannot come from any BF16 value."""
+    top = O.encode_block(np.full((16, 32), pattern(0, 255, 5), np.uint16), "k")
+    assert O.parse_header(top)[0] == 127
+    s = top.copy()
+    s[512 + 7] |= 0x10                                   # offset 1 in one high nibble
+    with pytest.raises(ValueError):
+        O.decode_block(s, "k")
+    low = O.encode_block(np.full((16, 32), pattern(1, 200, 5), np.uint16), "k")
+    s = low.copy()
+    s[512:768] = 0x77                                    # offset 7 everywhere: 100 + 7 fits
+    assert O.decode_block(s, "k").shape == (16, 32)

@@ -129,6 +129,45 @@ def _dev_i32(x, device):
     return torch.as_tensor(x, dtype=torch.int32, device=device).contiguous()
 
 
+_BITS16 = (torch.int16, torch.bfloat16)      # BF16 bit patterns, either view
+
+
+def _count(x) -> int:
+    return int(x.numel()) if isinstance(x, torch.Tensor) else len(x)
+
+
+def _arg(t, name, cache, dtypes, shape=None, min_rows=None):
+    """Checks the C ABI cannot make (it sees bare pointers): dtype, device, shape.  `shape` entries
+    of None match any size; min_rows bounds the first dimension from below."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {' or '.join(str(d) for d in dtypes)}")
+    if t.device != cache.device:
+        raise ValueError(f"{name} is on {t.device}, the cache on {cache.device}")
+    if shape is not None and (t.dim() != len(shape) or
+                              any(w is not None and h != w for h, w in zip(t.shape, shape))):
+        want = "[" + "][".join("*" if w is None else str(w) for w in shape) + "]"
+        raise ValueError(f"{name}: shape {list(t.shape)}, expected {want}")
+    if min_rows is not None and (t.dim() < 1 or t.shape[0] < min_rows):
+        raise ValueError(f"{name}: {t.shape[0] if t.dim() else 0} rows, at least {min_rows} needed")
+    return t.contiguous()
+
+
+def _result(t, name, cache, shape):
+    """An output the kernels write in place: float32, contiguous, exactly `shape`."""
+    _arg(t, name, cache, (torch.float32,), shape)
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (it is written in place)")
+    return t
+
+
+def _attn_args(cache, q, page_table, seq_lens, B):
+    page_table = _arg(page_table, "page_table", cache, (torch.int32,), (None, None), min_rows=B)
+    seq_lens = _arg(seq_lens, "seq_lens", cache, (torch.int32,), (None,), min_rows=B)
+    return page_table, seq_lens
+
+
 class Cache:
     """One layer's paged cache in device memory, laid out as include/zf.h describes.
 
@@ -189,8 +228,13 @@ class Cache:
 def encode_pages(cache: Cache, src_k, src_v, page_ids, n_valid, raw_slots=None, force_raw=False, stream=None):
     """Compress (or store raw) pages: src_k/src_v [n][Hkv][P][128] int16 BF16 bits on the device."""
     dev = cache.device
-    src_k, src_v = src_k.contiguous(), src_v.contiguous()
+    shape = (None, cache.num_kv_heads, cache.page_size, HEAD_DIM)
+    src_k = _arg(src_k, "src_k", cache, _BITS16, shape)
+    src_v = _arg(src_v, "src_v", cache, _BITS16, tuple(src_k.shape))
     n = int(src_k.shape[0])
+    for name, x in (("page_ids", page_ids), ("n_valid", n_valid), ("raw_slots", raw_slots)):
+        if x is not None and _count(x) != n:
+            raise ValueError(f"{name}: {_count(x)} entries for {n} pages")
     ids = _dev_i32(page_ids, dev)
     nv = _dev_i32(n_valid, dev)
     rs = _dev_i32(raw_slots, dev) if raw_slots is not None else _dev_i32([-1] * n, dev)
@@ -207,8 +251,12 @@ def append_tokens(cache: Cache, k_tok, v_tok, page_ids, positions, raw_slots, st
     when that token fills it).  Returns the index tensors (keep them alive until the stream has
     consumed them)."""
     dev = cache.device
-    k_tok, v_tok = k_tok.contiguous(), v_tok.contiguous()
+    k_tok = _arg(k_tok, "k_tok", cache, _BITS16, (None, cache.num_kv_heads, HEAD_DIM))
+    v_tok = _arg(v_tok, "v_tok", cache, _BITS16, tuple(k_tok.shape))
     n = int(k_tok.shape[0])
+    for name, x in (("page_ids", page_ids), ("positions", positions), ("raw_slots", raw_slots)):
+        if _count(x) != n:
+            raise ValueError(f"{name}: {_count(x)} entries for {n} tokens")
     ids, pos, rs = _dev_i32(page_ids, dev), _dev_i32(positions, dev), _dev_i32(raw_slots, dev)
     d = cache.desc()
     _check("zf_append_tokens", lib().zf_append_tokens(ctypes.byref(d), _ptr(k_tok), _ptr(v_tok), _ptr(ids), _ptr(pos),
@@ -274,14 +322,15 @@ def decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse
     """Decode attention over the cache.  q [B][Hq][128] int16 (BF16 bits), page_table [B][max_pages]
     int32, seq_lens [B] int32, all on the device.  Returns (out [B][Hq][128] f32, lse [B][Hq] f32).
     dense=True runs zf_dense_decode_attn on the raw pool (page id = raw slot)."""
+    q = _arg(q, "q", cache, _BITS16, (None, None, HEAD_DIM))
     B, Hq, _ = q.shape
+    page_table, seq_lens = _attn_args(cache, q, page_table, seq_lens, B)
     max_pages = int(page_table.shape[1])
     scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else scale
     dev = cache.device
-    if out is None:
-        out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=dev)
-    if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=dev) if out is None else \
+        _result(out, "out", cache, (B, Hq, HEAD_DIM))
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev) if lse is None else _result(lse, "lse", cache, (B, Hq))
     need = workspace_size(B, Hq, cache.num_kv_heads, cache.page_size, max_pages)
     if workspace is None:
         workspace = new_workspace(need, dev)
@@ -307,14 +356,16 @@ def decode_attn_multi(cache: Cache, q, page_table, seq_lens, scale=None, out=Non
     """zf_decode_attn_multi: T new tokens per request.  q [B][T][Hq][128] int16 (BF16 bits); token t
     of request b attends to positions 0 .. seq_lens[b] - T + t.  Returns (out [B][T][Hq][128] f32,
     lse [B][T][Hq] f32).  dense=True runs zf_dense_decode_attn_multi."""
+    q = _arg(q, "q", cache, _BITS16, (None, None, None, HEAD_DIM))
     B, T, Hq, _ = q.shape
+    page_table, seq_lens = _attn_args(cache, q, page_table, seq_lens, B)
     max_pages = int(page_table.shape[1])
     scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else scale
     dev = cache.device
-    if out is None:
-        out = torch.empty((B, T, Hq, HEAD_DIM), dtype=torch.float32, device=dev)
-    if lse is None:
-        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
+    out = torch.empty((B, T, Hq, HEAD_DIM), dtype=torch.float32, device=dev) if out is None else \
+        _result(out, "out", cache, (B, T, Hq, HEAD_DIM))
+    lse = torch.empty((B, T, Hq), dtype=torch.float32, device=dev) if lse is None else \
+        _result(lse, "lse", cache, (B, T, Hq))
     if workspace is None:
         workspace = new_workspace(workspace_size_multi(B, T, Hq, cache.num_kv_heads, cache.page_size, max_pages), dev)
     d = cache.desc()
@@ -334,13 +385,14 @@ def decode_attn_static(cache: Cache, q, page_table, seq_lens, scale=None, out=No
     """zf_decode_attn_static: the same attention without a caller-provided workspace, for callers
     that cannot allocate device memory (the library's 32 MiB static scratch array is used).
     Calls must not overlap on the GPU; the first call on a device must precede any stream capture."""
+    q = _arg(q, "q", cache, _BITS16, (None, None, HEAD_DIM))
     B, Hq, _ = q.shape
+    page_table, seq_lens = _attn_args(cache, q, page_table, seq_lens, B)
     scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else scale
     dev = cache.device
-    if out is None:
-        out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=dev)
-    if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=dev) if out is None else \
+        _result(out, "out", cache, (B, Hq, HEAD_DIM))
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev) if lse is None else _result(lse, "lse", cache, (B, Hq))
     d = cache.desc()
     code = lib().zf_decode_attn_static(ctypes.byref(d), _ptr(q), B, Hq, _ptr(page_table), int(page_table.shape[1]),
                                        _ptr(seq_lens), scale, _ptr(out), _ptr(lse), _stream(stream))

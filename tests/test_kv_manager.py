@@ -240,3 +240,78 @@ def test_random_workload_against_a_model(zf, layers):
         assert st["raw_full_slots"] == sum(len(v) for v in raw_kept.values())
         assert st["new_page_capacity"] == min(NP - len(all_ids), (NR - len(slots)) // layers)
         assert st["tokens"] == sum(m["len"] for m in model.values())
+
+
+def test_serving_loop_on_the_oracle_with_one_raw_pool(zf):
+    """The manager's protocol end to end on the oracle's caches: two layers whose caches share one
+    raw pool (the same arrays), prompts written with encode_pages, decode steps with append_tokens,
+    raw slots reclaimed layer by layer from the directories after every step, a request released
+    and another admitted mid-way.  Layer 1's keys carry blocks that cannot be encoded (eight tiny
+    values in a 512-value block), so some pages stay raw there only.  After every step each
+    layer's pages hold every request's tokens bit for bit — a slot handed from one layer to the
+    other never overwrites live data."""
+    import numpy as np
+    from oracle import zf_oracle as O
+
+    Hkv, NL, max_len = 2, 2, 120
+    rng = np.random.default_rng(3)
+
+    def stream(spiky):
+        x = rng.standard_normal((max_len, Hkv, 128)).astype(np.float32)
+        if spiky:
+            x[7::24, 0, 5:13] *= 2.0 ** -30
+        return ((x.view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
+
+    sk = [[stream(l == 1) for _ in range(4)] for l in range(NL)]
+    sv = [[stream(False) for _ in range(4)] for l in range(NL)]
+    kv = zf.KvManager(num_pages=30, num_raw_slots=14, page_size=P, max_requests=4, max_pages_per_req=8, num_layers=NL)
+    caches = [O.Cache(num_pages=30, num_kv_heads=Hkv, page_size=P, num_raw=14) for _ in range(NL)]
+    caches[1].k_raw, caches[1].v_raw = caches[0].k_raw, caches[0].v_raw
+    stream_of = {}
+
+    def reclaim():
+        ids, _ = kv.pending()
+        if ids:
+            kv.reclaim(ids, [[bool((c.dir[pid] >= 0).any()) for pid in ids] for c in caches])
+
+    def admit(req, length):
+        stream_of[req] = req
+        ids, nv, rs = kv.admit(req, length)
+        for l in range(NL):
+            src_k = np.zeros((len(ids), Hkv, P, 128), np.uint16)
+            src_v = np.zeros_like(src_k)
+            for j, fill in enumerate(nv):
+                src_k[j, :, :fill] = sk[l][req][j * P:j * P + fill].transpose(1, 0, 2)
+                src_v[j, :, :fill] = sv[l][req][j * P:j * P + fill].transpose(1, 0, 2)
+            O.encode_pages(caches[l], src_k, src_v, ids, nv, rs[l])
+        reclaim()
+
+    def check():
+        table, lens = kv.export()
+        for l in range(NL):
+            for req, s in stream_of.items():
+                L = int(lens[req])
+                K, V = O.gather_sequence(caches[l], table[req].numpy(), L)
+                assert (K == sk[l][s][:L]).all() and (V == sv[l][s][:L]).all(), (l, req)
+            assert caches[l].status == 0
+
+    for req, length in ((0, 37), (1, 16), (2, 50)):
+        admit(req, length)
+    check()
+    for step in range(30):
+        if step == 12:
+            kv.release(1)
+            del stream_of[1]
+            admit(3, 21)
+        reqs = sorted(stream_of)
+        ids, nv, rs = kv.append(reqs)
+        lens = kv.export()[1]
+        for l in range(NL):
+            k_tok = np.stack([sk[l][stream_of[q]][int(lens[q]) - 1] for q in reqs])
+            v_tok = np.stack([sv[l][stream_of[q]][int(lens[q]) - 1] for q in reqs])
+            O.append_tokens(caches[l], k_tok, v_tok, ids, [f - 1 for f in nv], rs[l])
+        reclaim()
+        check()
+    st = kv.stats()
+    assert st["pending_pages"] == 0 and st["raw_full_pages"] > 0
+    assert st["raw_full_slots"] == st["raw_full_pages"]          # kept in layer 1 only

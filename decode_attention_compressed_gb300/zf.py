@@ -493,11 +493,12 @@ class KvManager:
         _check("zf_kv_release", lib().zf_kv_release(self._h, req))
 
     def export(self):
-        table = (_c_int32 * (self.max_requests * self.max_pages))()
-        lens = (_c_int32 * self.max_requests)()
-        _check("zf_kv_export", lib().zf_kv_export(self._h, table, lens))
-        t = torch.tensor(list(table), dtype=torch.int32).reshape(self.max_requests, self.max_pages)
-        return t, torch.tensor(list(lens), dtype=torch.int32)
+        """(page_table [max_requests][max_pages_per_req], seq_lens [max_requests]) int32 CPU tensors."""
+        table = torch.empty((self.max_requests, self.max_pages), dtype=torch.int32)
+        lens = torch.empty(self.max_requests, dtype=torch.int32)
+        _check("zf_kv_export", lib().zf_kv_export(self._h, ctypes.cast(table.data_ptr(), _P32),
+                                                   ctypes.cast(lens.data_ptr(), _P32)))
+        return table, lens
 
     def stats(self) -> dict:
         st = ZfKvStats()

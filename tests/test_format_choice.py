@@ -1,0 +1,63 @@
+"""Why the format is not tighter (CPU only): the byte counts behind the choice of a 4-bit code
+with up to six escapes over narrower codes.  On the workloads' K and V distributions, two tighter
+families are counted block by block — a 3-bit code (sign + 2-bit exponent offset, a window of 8
+exponents) with room for E escapes, and bases per 32-value group (16 tokens x 2 channels) with a
+k-bit offset — each block costing its low bytes, packed codes, group bases, a 4-byte header and 2
+bytes per escape slot, rounded up to 16 bytes, or 1024 bytes raw when its escapes overflow.  None
+saves more than 2% of the present format's bytes on K and V together, which does not pay for a
+second rebuild path; the present format's count is checked against the encoder itself."""
+import numpy as np
+import pytest
+
+from decode_attention_compressed_gb300 import inputs as I
+from oracle import zf_oracle as O
+
+
+def _blocks(pages):
+    """[n][H][P][128] BF16 bits -> [blocks][16 tokens][32 channels]."""
+    n, H, P, D = pages.shape
+    return pages.reshape(n, H, P // 16, 16, 4, 32).transpose(0, 1, 2, 4, 3, 5).reshape(-1, 16, 32)
+
+
+def _round16(x):
+    return (x + 15) // 16 * 16
+
+
+def _window_cost(blocks, offset_bits, esc_slots, groups=1):
+    """Mean bytes per block for a code of sign + offset_bits with a window anchored at the top
+    exponent of each value group: the whole block, or 16 groups of 16 tokens x 2 channels (the
+    workloads scale K per channel).  Values below their group's window escape."""
+    eh = ((blocks >> 7) & 0xFF).astype(np.int64) >> 1                 # [blocks][16 tokens][32 channels]
+    if groups == 1:
+        eh = eh.reshape(len(blocks), 1, 512)
+    else:
+        eh = eh.reshape(len(blocks), 16, 16, 2).transpose(0, 2, 1, 3).reshape(len(blocks), 16, 32)
+    top = eh.max(axis=2, keepdims=True)
+    base = np.maximum(top - ((1 << offset_bits) - 1), 0)
+    esc = (eh < base).sum(axis=(1, 2))
+    payload = _round16(512 + 512 * (1 + offset_bits) // 8 + (groups if groups > 1 else 0) + 4 + 2 * esc_slots)
+    return np.where(esc > esc_slots, 1024, payload).mean()
+
+
+def _present_cost(blocks):
+    """Bytes per block of the present format, from the oracle encoder."""
+    sizes = [O.SLOT_BYTES if O.encode_block(b, "k") is not None else O.RAW_BLOCK_BYTES for b in blocks]
+    return float(np.mean(sizes))
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_batched", "qwen2_7b_maxbatch", "llama7b_mha_8192"])
+def test_no_tighter_variant_saves_more_than_two_percent(name):
+    w = I.scaled(I.WORKLOADS[name], batch=1, ctx=1024, ctx_min=1024, layers=1)
+    lay = I.make_layer(w, seq_lens=[1024])
+    kb = _blocks(lay.k_pages.numpy().view(np.uint16))
+    vb = _blocks(lay.v_pages.numpy().view(np.uint16))
+    both = np.concatenate([kb, vb])
+    present = _present_cost(both)
+    # the counting model reproduces the present format (4-bit code: 3-bit offset, six escapes)
+    assert _window_cost(both, 3, 6) == pytest.approx(present)
+    assert present <= 0.77 * 1024
+    variants = {f"3-bit code, {e} escapes": _window_cost(both, 2, e) for e in (8, 12, 16, 24)}
+    variants.update({f"group bases, {k}-bit offsets, {e} escapes": _window_cost(both, k, e, 16)
+                     for k, e in ((2, 8), (2, 16), (2, 24))})
+    best = min(variants.values())
+    assert best >= 0.98 * present, {k: round(v / present, 4) for k, v in variants.items()}

@@ -163,3 +163,17 @@ def test_multi_token_attention_rejects_bad_token_counts(zf, dense):
     assert call(2, hq=7) == -1                                       # heads still a multiple of kv heads
     assert zf.lib().zf_decode_attn_multi_workspace_size(1, 0, 8, 2, 16, 4) == 0
     assert zf.lib().zf_decode_attn_multi_workspace_size(1, 2, 7, 2, 16, 4) == 0
+
+
+def test_product_path_never_touches_the_oracle():
+    """The library and its binding neither import nor read anything under oracle/ (the oracle is
+    test infrastructure; a product path through it would be a CPU fallback)."""
+    pkg = os.path.join(ROOT, "decode_attention_compressed_gb300")
+    offenders = []
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                if re.search(r"^\s*(from|import)\s+oracle\b|zf_oracle|[\"']oracle[/\"']", text, flags=re.M):
+                    offenders.append(f)
+    assert offenders == []

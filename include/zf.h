@@ -11,7 +11,8 @@
  *
  * General rules for every call below
  *  - All tensor pointers are DEVICE pointers owned by the caller; the library never allocates,
- *    frees or keeps them.  All arrays are dense, row-major, and 16-byte aligned.
+ *    frees or keeps them.  All arrays are dense, row-major, and 16-byte aligned.  (The host-side
+ *    page manager zf_kv_* and zf_slot_is_valid work on host memory instead.)
  *  - BF16 values are passed as their 16-bit patterns (uint16_t).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call only enqueues
  *    work on `stream` and returns; results are ready when the stream reaches that point.

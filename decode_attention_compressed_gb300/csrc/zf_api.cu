@@ -13,6 +13,7 @@ extern "C" const char* zf_status_string(zf_status status) {
     case ZF_ERR_CUDA: return "CUDA runtime error";
     case ZF_ERR_STATIC_WORKSPACE_EXCEEDED: return "sizes need more scratch than the library's static workspace";
     case ZF_ERR_CAPACITY: return "not enough free page ids or raw slots";
+    case ZF_ERR_STATIC_WORKSPACE_UNAVAILABLE: return "no device memory left to load the library's static workspace";
     default: return "unknown status";
   }
 }

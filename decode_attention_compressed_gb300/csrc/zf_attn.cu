@@ -1389,26 +1389,24 @@ extern "C" zf_status zf_dense_decode_attn_multi(const zf_cache* cache, const uin
 // zf_decode_attn_static: the same attention for callers that cannot allocate device memory.
 // Its split-KV scratch is this file-scope device array (held by every GPU that loads the library
 // until exit).  Host code must not pass `g_static_workspace` itself to a kernel: on the host the
-// name is only a stand-in, so the device address is looked up once per device below.
+// name is only a stand-in, so the device address is looked up with the caller's device current.
 static __device__ __align__(256) unsigned char g_static_workspace[ZF_STATIC_WORKSPACE_BYTES];
 
 namespace {
-constexpr int kStaticMaxDevices = 64;
-std::mutex g_static_mutex;
-void* g_static_address[kStaticMaxDevices] = {};
-
-// Address of g_static_workspace on the current device (looked up on the first call per device).
+// Address of g_static_workspace in the current context.  Looked up on every call rather than
+// cached per device ordinal: after a device reset, or with another context of the same device
+// made current, a cached address would name memory that context does not map.  Once the module
+// is loaded the lookup allocates nothing; the first lookup in a context may load it (lazy module
+// loading), which is when the array is reserved.
 zf_status static_workspace_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ZF_ERR_CUDA;
-  if (dev < 0 || dev >= kStaticMaxDevices) return ZF_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (!g_static_address[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return ZF_ERR_CUDA;
-    g_static_address[dev] = p;
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+  if (e == cudaErrorMemoryAllocation) {
+    (void)cudaGetLastError();          // not sticky: clear it for the caller's next call
+    return ZF_ERR_STATIC_WORKSPACE_UNAVAILABLE;
   }
-  *out = g_static_address[dev];
+  if (e != cudaSuccess || !p) return ZF_ERR_CUDA;
+  *out = p;
   return ZF_OK;
 }
 }  // namespace

@@ -500,7 +500,9 @@ extern "C" int32_t zf_slot_is_valid(const uint8_t* slot) { return slot && slot_o
 
 static zf_status launch_decompress(const zf_cache* cache, const int32_t* page_ids, int32_t n, uint16_t* dst_k,
                                    uint16_t* dst_v, int raw_out, void* stream) {
-  zf_status st = check_cache(cache, /*need_comp=*/false, /*need_raw=*/false, /*need_dir=*/true);
+  // the directory may name any compressed slot or raw slot, so every pool the descriptor sizes
+  // must be present (a NULL pool would otherwise be read on the device)
+  zf_status st = check_cache(cache, /*need_comp=*/true, /*need_raw=*/true, /*need_dir=*/true);
   if (st != ZF_OK) return st;
   if (n < 0) return ZF_ERR_INVALID_ARGUMENT;
   if (n == 0) return ZF_OK;

@@ -379,6 +379,7 @@ def decode_attn_multi(cache: Cache, q, page_table, seq_lens, scale=None, out=Non
 
 STATIC_WORKSPACE_BYTES = 32 << 20
 ERR_STATIC_WORKSPACE_EXCEEDED = -5
+ERR_STATIC_WORKSPACE_UNAVAILABLE = -7
 
 
 def decode_attn_static(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse=None, stream=None):

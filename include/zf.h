@@ -21,8 +21,11 @@
  *    a page that needed raw storage but got none, a pipeline wait that gave up) never fault:
  *    the offending page is skipped and a bit is OR-ed into the optional device status word
  *    zf_cache.status (ZF_DEV_* below), which the caller may read after synchronising.
- *  - The library keeps no global state; concurrent calls on different streams are safe as long
- *    as they do not write the same memory.
+ *  - Concurrent calls on different streams are safe as long as they do not write the same memory.
+ *    The library's only global state is (a) the scratch array of zf_decode_attn_static (below),
+ *    which that entry point's calls share, and (b) a per-device record, behind a mutex, of the
+ *    shared-memory limits already raised for its kernels.  Every other entry point works only
+ *    on the memory it is given.
  *
  * Data layout of one layer's cache (head_dim is fixed at 128, page_size P is a multiple of 16):
  *  - A BLOCK is 16 consecutive tokens x 32 consecutive channels of one (page, kv head, K|V):
@@ -64,6 +67,8 @@ typedef int32_t zf_status;
 #define ZF_ERR_CUDA (-4)               /* a CUDA runtime call failed (launch or attribute) */
 #define ZF_ERR_STATIC_WORKSPACE_EXCEEDED (-5) /* zf_decode_attn_static: sizes need more than ZF_STATIC_WORKSPACE_BYTES */
 #define ZF_ERR_CAPACITY (-6)           /* zf_kv: not enough free page ids or raw slots; nothing changed */
+#define ZF_ERR_STATIC_WORKSPACE_UNAVAILABLE (-7) /* zf_decode_attn_static: the device had no memory left to
+                                                    load the library's scratch array (see that call) */
 
 /* Bits of the device status word (zf_cache.status). */
 #define ZF_DEV_BAD_PAGE_ID 0x1         /* page id outside [0, num_pages) */
@@ -293,12 +298,22 @@ zf_status zf_dense_decode_attn_multi(const zf_cache* cache, const uint16_t* q, i
  *   - Sizes whose split-KV partials need more than ZF_STATIC_WORKSPACE_BYTES (see
  *     zf_decode_attn_workspace_size) are rejected with ZF_ERR_STATIC_WORKSPACE_EXCEEDED before
  *     anything is launched.
- *   - The first call on a device looks up that device's address of the array (with that device
- *     current); make that first call before any stream capture.
+ *   - When the array comes into being: CUDA loads the library's device code into a context lazily
+ *     by default (CUDA_MODULE_LOADING=LAZY), and the array is reserved when the module holding
+ *     it is loaded — at the first libzf attention call in that context, which may be the first
+ *     zf_decode_attn_static call itself.  That first call can therefore reserve the 32 MiB and
+ *     synchronise.  A caller that cannot allocate later should make one call (any shape) at
+ *     initialisation, before its engine takes the rest of device memory and before any stream
+ *     capture.  If the device has no memory left to load it, the call returns
+ *     ZF_ERR_STATIC_WORKSPACE_UNAVAILABLE and launches nothing.
+ *   - Every call looks up the array's address in the current context (cheap once the module is
+ *     loaded, and it allocates nothing), so it stays correct after a device reset or with another
+ *     context of the device current.
  *   - All calls share the one array and it keeps the previous call's contents (nothing in it has
  *     to start at zero).  Calls that overlap on the GPU (other streams, other threads) race on it:
  *     serialise them.
- *   Results are identical to zf_decode_attn's for the same inputs.
+ *   Results are bit-for-bit those of zf_decode_attn for the same inputs (same kernels, same work
+ *   split; only the scratch memory differs).
  */
 #define ZF_STATIC_WORKSPACE_BYTES (32u << 20)
 zf_status zf_decode_attn_static(const zf_cache* cache, const uint16_t* q, int32_t batch,

@@ -38,6 +38,7 @@ def test_status_strings(zf):
     assert zf.status_string(0) == "ok"
     assert zf.status_string(-1) == "invalid argument"
     assert zf.status_string(-3) == "workspace too small"
+    assert zf.status_string(-7).startswith("no device memory left")
     assert zf.status_string(12345) == "unknown status"
 
 
@@ -84,6 +85,12 @@ def test_decompress_rejects_bad_arguments(zf):
     assert f(ctypes.byref(d), None, 1, 0x2000, 0x3000, None) == -1
     assert f(ctypes.byref(d), 0x1000, 1, 0x2001, 0x3000, None) == -1
     assert f(ctypes.byref(d), 0x1000, 0, 0x2000, 0x3000, None) == 0
+    # every pool the descriptor sizes must be present: the directory may point into any of them
+    for pool in ("k_comp", "v_comp", "k_raw", "v_raw", "dir"):
+        bad = _desc(zf, **{pool: None})
+        for g in (zf.lib().zf_decompress, zf.lib().zf_decompress_to_raw):
+            assert g(ctypes.byref(bad), 0x1000, 1, 0x2000, 0x3000, None) == -1, pool
+    assert zf.lib().zf_decompress_to_raw(ctypes.byref(d), 0x1000, 1, 0x2000, 0x3008, None) == -1
 
 
 def test_append_rejects_bad_arguments_before_launch(zf):

@@ -134,3 +134,20 @@ def _append_without_step_2(encode_page_head):
                 _, cache.k_raw[slot, h], cache.v_raw[slot, h] = encode_page_head(k, v, pos + 1, force_raw=True)
                 cache.dir[int(pid), h] = slot
     return bad
+
+
+def test_sign_dropping_bf16_widening_is_caught(monkeypatch):
+    """A widening that loses the sign bit passes every attention pin (both sides of each go through
+    it); the BF16 pins catch it."""
+    import tests.test_oracle_bf16 as TB
+    real = O.bf16_to_f64
+    monkeypatch.setattr(O, "bf16_to_f64", lambda x: real(np.asarray(x, dtype=np.uint16) & np.uint16(0x7FFF)))
+    _fails(TB.test_hand_listed_patterns)
+    _fails(TB.test_every_pattern_matches_an_independent_field_decode)
+
+
+def test_bf16_widening_with_a_shifted_exponent_is_caught(monkeypatch):
+    import tests.test_oracle_bf16 as TB
+    real = O.bf16_to_f64
+    monkeypatch.setattr(O, "bf16_to_f64", lambda x: real(x) * 2.0)
+    _fails(TB.test_hand_listed_patterns)

@@ -53,8 +53,9 @@ class Workload:
         return -(-self.ctx // self.page_size)
 
 
-# The five decode configurations (tiny, LLaMA-7B MHA, Llama-3-8B batched, Qwen2-7B max batch,
-# long context).  Config 1 is one workload per context length.
+# The decode configurations (tiny, LLaMA-7B MHA, Llama-3-8B batched, Qwen2-7B max batch, long
+# context, and the batch-64 shape of the pages' kernel figure).  LLaMA-7B MHA is one workload per
+# context length.
 WORKLOADS = {
     "tiny": Workload("tiny", 1, 32, 8, 16, 512, seed=0,
                      note="batch 1, 32/8 heads, ctx 512, page 16, pages in order"),
@@ -71,6 +72,12 @@ WORKLOADS = {
                                        "2% (token, head) one-channel x50 spikes"),
     "long_ctx": Workload("long_ctx", 4, 32, 8, 64, 131072, pool="random", seed=4,
                          note="batch 4, 32/8 heads, ctx 131072, page 64, random pool"),
+    # the shape the ZipFusion attention-kernel figure (§IV.B, Fig. 4) times: an 8B model with 32
+    # query and 8 kv heads, batch 64, contexts 2048 and 8192, 16-token pages
+    "batch64_gqa4_2048": Workload("batch64_gqa4_2048", 64, 32, 8, 16, 2048, pool="random", seed=5,
+                                  note="batch 64, 32/8 heads, ctx 2048, page 16, random pool"),
+    "batch64_gqa4_8192": Workload("batch64_gqa4_8192", 64, 32, 8, 16, 8192, pool="random", seed=6,
+                                  note="batch 64, 32/8 heads, ctx 8192, page 16, random pool"),
 }
 
 

@@ -103,3 +103,47 @@ def _batch_shard(rank, world):
 
 def test_replicas_on_disjoint_requests_reproduce_the_full_batch():
     assert run_ranks(_batch_shard) == [True, True]
+
+
+STUB = """
+import json, sys
+import torch
+import torch.distributed as dist
+dist.init_process_group("gloo")
+r, w = dist.get_rank(), dist.get_world_size()
+t = torch.tensor([10.0 + r])
+dist.all_reduce(t, op=dist.ReduceOp.MAX)
+if r == 0:
+    print(json.dumps({"world": w, "max": float(t.item()), "args": sys.argv[1:]}), flush=True)
+dist.destroy_process_group()
+"""
+
+
+def test_launcher_starts_one_rank_per_gpu(tmp_path):
+    """bench.py --gpus N run without torchrun starts N ranks itself (torch.distributed.run on
+    127.0.0.1); here the ranks are gloo processes running a stand-in script."""
+    import json
+    stub = tmp_path / "stub.py"
+    stub.write_text(STUB)
+    res = bench.launch_ranks(2, ["--steps", "3"], script=str(stub), capture_output=True)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = [x for x in res.stdout.splitlines() if x.startswith("{")][-1]
+    got = json.loads(line)
+    assert got == {"world": 2, "max": 11.0, "args": ["--steps", "3"]}
+
+
+def test_main_hands_gpus_above_one_to_the_launcher(monkeypatch):
+    seen = {}
+
+    class Done:
+        returncode = 0
+
+    def fake(n, argv, script=None, capture_output=False):
+        seen["n"], seen["argv"] = n, list(argv)
+        return Done()
+    monkeypatch.setattr(bench, "launch_ranks", fake)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr("sys.argv", ["bench.py", "--gpus", "4", "--steps", "5"])
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert e.value.code == 0 and seen == {"n": 4, "argv": ["--gpus", "4", "--steps", "5"]}

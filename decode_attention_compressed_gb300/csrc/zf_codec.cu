@@ -7,9 +7,9 @@
 // is wider (window anchored at the maximum exponent).  ZipFusion §III.D: partial pages stay raw;
 // full pages are compressed under their page id.
 //
-// One CTA encodes one (page, kv head): each warp classifies and encodes whole blocks into shared
-// memory, then the CTA decides compressed vs raw for the page head and writes it out with
-// coalesced 16-byte stores.
+// One CTA encodes one (page, kv head): each warp classifies and encodes whole blocks straight into
+// the page's compressed slot (coalesced 16-byte stores); a page head with a block that cannot be
+// compressed is then written to its raw slot instead.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -47,145 +47,208 @@ __device__ __forceinline__ size_t natural_offset(int tile, int group, int lane) 
   return static_cast<size_t>(16 * tile + (lane >> 1)) * ZF_HEAD_DIM + 32 * group + 16 * (lane & 1);
 }
 
+struct uint4x2 {
+  uint4 a, b;
+};
+
 // One warp encodes one block.  u: this lane's 16 values at storage positions 16*lane .. +15
 // (two per word, low half first).  Writes the 784-byte slot, or sets *fail when the block needs
 // more than ZF_MAX_ESCAPES escapes.  Base: the minimum exponent rounded down to even when every
 // exponent fits [base, base+15], else the smallest even base whose window reaches the maximum
 // exponent, values below it becoming escapes.
-__device__ __forceinline__ void encode_block_lane(const uint32_t (&u)[8], uint8_t* slot, int lane, int* fail) {
-  uint32_t emin = 255, emax = 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t e = ((u[j >> 1] >> (16 * (j & 1))) >> 7) & 0xFFu;
-    emin = min(emin, e);
-    emax = max(emax, e);
-  }
-  emin = __reduce_min_sync(0xFFFFFFFFu, emin);
-  emax = __reduce_max_sync(0xFFFFFFFFu, emax);
-  uint32_t base = emin & ~1u;
-  if (emax > base + 15) base = (emax - 14) & ~1u;
+//
+// Four values per 32-bit operation: with h = sign << 7 | exponent >> 1 (a value's high byte) and
+// eh = h & 0x7F, the rule reads base/2 = min eh when max eh <= min eh + 7, else max eh - 7; a value
+// is an escape when eh < base/2, and its code is sign << 3 | (eh - base/2) (offset 0 for escapes).
+__device__ __forceinline__ uint32_t byte_signs(uint32_t x) {
+  uint32_t r;       // prmt with the sign-replicate selector bit: byte i = 0xFF if bit 7 of byte i is set
+  asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(r) : "r"(x));
+  return r;
+}
 
-  uint32_t code[16], lo[16], eh[16];
-  uint32_t esc_mask = 0;
+__device__ __forceinline__ void encode_block_lane(const uint32_t (&u)[8], uint8_t* slot, int lane, int* fail) {
+  uint32_t eh[4], lo4[4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t v = (u[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-    const uint32_t e = (v >> 7) & 0xFFu;
-    lo[j] = v & 0xFFu;
-    eh[j] = e >> 1;
-    const bool esc = e < base;
-    esc_mask |= static_cast<uint32_t>(esc) << j;
-    code[j] = ((v >> 15) << 3) | (esc ? 0u : eh[j] - (base >> 1));
+  for (int k = 0; k < 4; ++k) {            // values 4k .. 4k+3: word 2k holds 4k, 4k+1
+    eh[k] = __byte_perm(u[2 * k], u[2 * k + 1], 0x7531);    // high bytes
+    lo4[k] = __byte_perm(u[2 * k], u[2 * k + 1], 0x6420);   // low bytes, stored as they are
   }
-  const uint32_t cnt = __popc(esc_mask);
-  uint32_t before = cnt;                       // inclusive scan over lanes
+  // min and max of the 16 exponent>>1 fields, two per 16-bit lane
+  uint32_t f[8];
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, before, d);
-    if (lane >= d) before += t;
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = eh[k] & 0x007F007Fu;
+    f[2 * k + 1] = (eh[k] >> 8) & 0x007F007Fu;
   }
-  const uint32_t total = __shfl_sync(0xFFFFFFFFu, before, 31);
-  before -= cnt;
+  uint32_t mn = __vimin3_u16x2(__vimin3_u16x2(f[0], f[1], f[2]), __vimin3_u16x2(f[3], f[4], f[5]),
+                               __vimin3_u16x2(f[6], f[7], f[7]));
+  uint32_t mx = __vimax3_u16x2(__vimax3_u16x2(f[0], f[1], f[2]), __vimax3_u16x2(f[3], f[4], f[5]),
+                               __vimax3_u16x2(f[6], f[7], f[7]));
+  mn = __reduce_min_sync(0xFFFFFFFFu, min(mn & 0xFFFFu, mn >> 16));
+  mx = __reduce_max_sync(0xFFFFFFFFu, max(mx & 0xFFFFu, mx >> 16));
+  const uint32_t half_base = mx > mn + 7 ? mx - 7 : mn;
+  const uint32_t hb4 = half_base * 0x01010101u;
+  // per byte: d = 0x80 + eh - base/2 (no borrow crosses a byte: eh, base/2 <= 127), bit 7 set
+  // exactly when the value is not an escape
+  uint32_t code[4], esc[4], cnt = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t d = (eh[k] | 0x80808080u) - hb4;
+    const uint32_t keep = byte_signs(d);                        // 0xFF per non-escape byte
+    esc[k] = ~d & 0x80808080u;
+    code[k] = (d & keep & 0x07070707u) | ((eh[k] >> 4) & 0x08080808u);
+    cnt += __popc(esc[k]);
+  }
+  const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, cnt);
   if (total > ZF_MAX_ESCAPES) {
     if (lane == 0) atomicOr(fail, 1);
     return;
   }
-  uint4 lob;
-  lob.x = lo[0] | lo[1] << 8 | lo[2] << 16 | lo[3] << 24;
-  lob.y = lo[4] | lo[5] << 8 | lo[6] << 16 | lo[7] << 24;
-  lob.z = lo[8] | lo[9] << 8 | lo[10] << 16 | lo[11] << 24;
-  lob.w = lo[12] | lo[13] << 8 | lo[14] << 16 | lo[15] << 24;
-  *reinterpret_cast<uint4*>(slot + 16 * lane) = lob;
-  uint2 cw;
-  cw.x = (code[0] | code[4] << 4) | (code[1] | code[5] << 4) << 8 | (code[2] | code[6] << 4) << 16 |
-         (code[3] | code[7] << 4) << 24;
-  cw.y = (code[8] | code[12] << 4) | (code[9] | code[13] << 4) << 8 | (code[10] | code[14] << 4) << 16 |
-         (code[11] | code[15] << 4) << 24;
-  *reinterpret_cast<uint2*>(slot + 512 + 8 * lane) = cw;
+  *reinterpret_cast<uint4*>(slot + 16 * lane) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+  // byte m of a code word = code of value m | code of value m + 4 << 4
+  *reinterpret_cast<uint2*>(slot + 512 + 8 * lane) = make_uint2(code[0] | code[1] << 4, code[2] | code[3] << 4);
   uint16_t* escs = reinterpret_cast<uint16_t*>(slot + kEscapesAt);
   if (lane < ZF_MAX_ESCAPES && static_cast<uint32_t>(lane) >= total) escs[lane] = 0;
-  uint32_t k = before;
+  if (total > 0) {
+    uint32_t before = cnt;                   // inclusive scan over lanes, then exclusive
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (esc_mask & (1u << j)) {
-      escs[k] = static_cast<uint16_t>(((16 * lane + j) << 7) | eh[j]);
-      ++k;
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, before, d);
+      if (lane >= d) before += t;
+    }
+    uint32_t k = before - cnt;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (esc[j >> 2] & (0x80u << (8 * (j & 3)))) {     // entry: position << 7 | exponent >> 1
+        escs[k++] = static_cast<uint16_t>(((16 * lane + j) << 7) | ((eh[j >> 2] >> (8 * (j & 3))) & 0x7Fu));
+      }
     }
   }
   if (lane == 0)
     *reinterpret_cast<uint32_t*>(slot + kHeaderAt) =
-        (base >> 1) | (total << 8) | (static_cast<uint32_t>(ZF_FORMAT_VERSION) << 24);
+        half_base | (total << 8) | (static_cast<uint32_t>(ZF_FORMAT_VERSION) << 24);
 }
 
-__global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
+// This lane's 16 source values of block `bi` (tile bi/4, channel group bi%4) of a [P][128] page
+// head in natural layout: token lane/2, channels 16*(lane%2) .. +15 of the group.
+__device__ __forceinline__ uint4x2 load_block_lane(const uint16_t* src_head, int bi, int lane) {
+  const uint16_t* p = src_head + natural_offset(bi >> 2, bi & 3, lane);
+  uint4x2 x;
+  x.a = *reinterpret_cast<const uint4*>(p);
+  x.b = *reinterpret_cast<const uint4*>(p + 8);
+  return x;
+}
+
+// Rows of a warp's staging block: 16 tokens x 32 channels, rows padded to 80 bytes so that the
+// eight 16-byte rows one ldmatrix phase reads fall in distinct banks.
+constexpr int kStageRowBytes = 80;
+constexpr int kStageBytes = 16 * kStageRowBytes;
+
+// A lane's natural-layout values -> the warp's stage -> the lane's own 16 storage positions
+// (16*lane .. +15, two per word).  The storage order is the m16n8k16 A-operand register order of
+// each 16x16 half, so ldmatrix delivers it: for keys the A operand is the block itself (rows
+// tokens), for values its transpose (rows channels), read with .trans.
+__device__ __forceinline__ void to_storage_order(const uint4x2& x, bool is_value, uint8_t* stage, int lane,
+                                                 uint32_t (&u)[8]) {
+  uint8_t* row = stage + (lane >> 1) * kStageRowBytes + 32 * (lane & 1);
+  *reinterpret_cast<uint4*>(row) = x.a;
+  *reinterpret_cast<uint4*>(row + 16) = x.b;
+  __syncwarp();
+  // matrix q = lane / 8 of the four, row lane % 8 of it.  Keys: q selects (tokens +8 for q odd,
+  // channels +8 for q >= 2); values: (channels +8 for q odd, tokens +8 for q >= 2).
+  const int q = lane >> 3, r = lane & 7;
+  const int tok = r + 8 * (is_value ? (q >> 1) : (q & 1));
+  const int ch = 8 * (is_value ? (q & 1) : (q >> 1));
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint8_t* p = stage + tok * kStageRowBytes + 2 * (16 * half + ch);
+    if (is_value) ldmatrix_x4_trans(p, u[4 * half], u[4 * half + 1], u[4 * half + 2], u[4 * half + 3]);
+    else ldmatrix_x4(p, u[4 * half], u[4 * half + 1], u[4 * half + 2], u[4 * half + 3]);
+  }
+  __syncwarp();                                  // the stage is rewritten by the next block
+}
+
+// One CTA per (page, kv head) with W warps: warp w takes blocks w, w + W, ... of the page head's K
+// blocks then V blocks, kEncodeBatch at a time.  The source address does not depend on the
+// page id, so the first batch of loads is issued before the page id and fill count are read.  A
+// full page is encoded straight into its compressed slot; if any block needs more than
+// ZF_MAX_ESCAPES escapes, the page head is then written raw instead (the compressed slot's
+// contents are unused while the directory names the raw slot).  Partial and forced-raw pages go
+// to the raw slot directly.  Launched with programmatic stream serialisation: it waits for the
+// preceding grid before reading anything, and lets the next grid launch at once.
+// Two blocks in flight per warp and 8 warps per CTA (measured on GB300 against 2, 4 and 16
+// warps, and against loading the next pair while encoding this one: 8 warps without that was
+// fastest); at most 64 registers so that four CTAs fit an SM.
+constexpr int kEncodeBatch = 2;
+constexpr int kEncodeWarps = 8;
+__global__ void __launch_bounds__(kEncodeWarps * 32, 4) encode_kernel(CodecArgs a) {
+  __shared__ __align__(16) uint8_t stage[kEncodeWarps][kStageBytes];
+  __shared__ int fail;
+  wait_prior_grid();
+  allow_next_grid();
   const int P = a.page_size;
   const int nblk = P / 4;                    // blocks per K (or V) page head
-  uint8_t* comp = smem;                      // [2*nblk][784]
-  uint16_t* raw = reinterpret_cast<uint16_t*>(smem + 2 * nblk * kSlotBytes);   // [2*nblk][512]
-  int* fail = reinterpret_cast<int*>(raw + 2 * nblk * 512);
-
+  const int nb = 2 * nblk;
   const int i = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kStep = kEncodeWarps * kEncodeBatch;
+  const size_t head_elems = static_cast<size_t>(P) * ZF_HEAD_DIM;
+  const uint16_t* src_k = a.src_k + (static_cast<size_t>(i) * a.hkv + h) * head_elems;
+  const uint16_t* src_v = a.src_v + (static_cast<size_t>(i) * a.hkv + h) * head_elems;
+  uint4x2 x[kEncodeBatch];
+  auto load = [&](int b0) {
+#pragma unroll
+    for (int k = 0; k < kEncodeBatch; ++k) {
+      const int blk = b0 + k * kEncodeWarps;
+      if (blk < nb) x[k] = load_block_lane(blk >= nblk ? src_v : src_k, blk >= nblk ? blk - nblk : blk, lane);
+    }
+  };
+  // walk the warp's blocks a batch at a time: fn(block, values) for each; batch 0 is already in x
+  auto walk = [&](auto&& fn) {
+    for (int b0 = warp; b0 < nb; b0 += kStep) {
+      if (b0 != warp) load(b0);
+#pragma unroll
+      for (int k = 0; k < kEncodeBatch; ++k) {
+        const int blk = b0 + k * kEncodeWarps;
+        if (blk < nb) fn(blk, x[k]);
+      }
+    }
+  };
+  load(warp);
+  if (threadIdx.x == 0) fail = 0;
   const int pid = a.page_ids[i];
   const int nv = a.n_valid[i];
   if (pid < 0 || pid >= a.num_pages) {
     if (threadIdx.x == 0) report(a.status, ZF_DEV_BAD_PAGE_ID);
     return;
   }
+  const size_t dir_at = static_cast<size_t>(pid) * a.hkv + h;
   if (nv < 0 || nv > P) {
     if (threadIdx.x == 0) {
       report(a.status, ZF_DEV_BAD_N_VALID);
-      a.dir[static_cast<size_t>(pid) * a.hkv + h] = ZF_DIR_INVALID;
+      a.dir[dir_at] = ZF_DIR_INVALID;
     }
     return;
   }
-  if (threadIdx.x == 0) *fail = 0;
-  __syncthreads();
-
-  const size_t head_elems = static_cast<size_t>(P) * ZF_HEAD_DIM;
-  for (int blk = warp; blk < 2 * nblk; blk += kCodecWarps) {
-    const bool is_value = blk >= nblk;
-    const int bi = is_value ? blk - nblk : blk;
-    const int tile = bi >> 2, group = bi & 3;
-    const uint16_t* src = (is_value ? a.src_v : a.src_k) + (static_cast<size_t>(i) * a.hkv + h) * head_elems +
-                          natural_offset(tile, group, lane);
-    const uint4 x0 = *reinterpret_cast<const uint4*>(src);
-    const uint4 x1 = *reinterpret_cast<const uint4*>(src + 8);
-    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-
-    // scatter into storage order (this block's raw form)
-    uint16_t* rblk = raw + blk * 512;
-    const int tau = lane >> 1, g0 = 16 * (lane & 1);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint16_t v = static_cast<uint16_t>((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-      rblk[block_position(is_value, tau, g0 + j)] = v;
-    }
-    __syncwarp();
-
-    // this lane now owns storage positions 16*lane .. 16*lane+15
-    const uint4 y0 = *reinterpret_cast<const uint4*>(rblk + 16 * lane);
-    const uint4 y1 = *reinterpret_cast<const uint4*>(rblk + 16 * lane + 8);
-    const uint32_t u[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-    encode_block_lane(u, comp + blk * kSlotBytes, lane, fail);
-  }
-  __syncthreads();
-
-  const bool store_raw = (a.flags & ZF_ENCODE_FORCE_RAW) || nv < P || *fail;
-  const size_t dir_at = static_cast<size_t>(pid) * a.hkv + h;
-  if (!store_raw) {
+  uint8_t* my_stage = stage[warp];
+  __syncthreads();                           // `fail` is initialised
+  if (!((a.flags & ZF_ENCODE_FORCE_RAW) || nv < P)) {
     const size_t rec = static_cast<size_t>(nblk) * kSlotBytes;     // bytes per K (or V) record
-    uint8_t* dk = a.k_comp + (static_cast<size_t>(pid) * a.hkv + h) * rec;
-    uint8_t* dv = a.v_comp + (static_cast<size_t>(pid) * a.hkv + h) * rec;
-    const int n16 = static_cast<int>(rec / 16);
-    for (int t = threadIdx.x; t < 2 * n16; t += kCodecThreads) {
-      const uint4 val = reinterpret_cast<const uint4*>(comp)[t];
-      if (t < n16) reinterpret_cast<uint4*>(dk)[t] = val;
-      else reinterpret_cast<uint4*>(dv)[t - n16] = val;
+    uint8_t* dk = a.k_comp + dir_at * rec;
+    uint8_t* dv = a.v_comp + dir_at * rec;
+    walk([&](int blk, const uint4x2& v) {
+      const bool is_value = blk >= nblk;
+      const int bi = is_value ? blk - nblk : blk;
+      uint32_t u[8];
+      to_storage_order(v, is_value, my_stage, lane, u);
+      encode_block_lane(u, (is_value ? dv : dk) + static_cast<size_t>(bi) * kSlotBytes, lane, &fail);
+    });
+    __syncthreads();
+    if (!fail) {
+      if (threadIdx.x == 0) a.dir[dir_at] = ZF_DIR_COMPRESSED;
+      return;
     }
-    if (threadIdx.x == 0) a.dir[dir_at] = ZF_DIR_COMPRESSED;
-    return;
+    load(warp);                              // a block overflowed its escapes: the page head goes raw
   }
   const int rs = a.raw_slots ? a.raw_slots[i] : -1;
   if (rs < 0 || rs >= a.num_raw) {
@@ -195,18 +258,20 @@ __global__ void __launch_bounds__(kCodecThreads) encode_kernel(CodecArgs a) {
     }
     return;
   }
-  const size_t rec = static_cast<size_t>(nblk) * 512;            // uint16 per K (or V) record
-  uint16_t* dk = a.k_raw + (static_cast<size_t>(rs) * a.hkv + h) * rec;
-  uint16_t* dv = a.v_raw + (static_cast<size_t>(rs) * a.hkv + h) * rec;
-  const int n16 = static_cast<int>(rec / 8);
-  for (int t = threadIdx.x; t < 2 * n16; t += kCodecThreads) {
-    // shared memory holds blocks in storage order (16-byte group 2*lane + half); raw blocks are
-    // half-major (group 32*half + lane)
-    const int blk = t >> 6, within = t & 63;
-    const uint4 val = reinterpret_cast<const uint4*>(raw)[blk * 64 + 2 * (within & 31) + (within >> 5)];
-    if (t < n16) reinterpret_cast<uint4*>(dk)[t] = val;
-    else reinterpret_cast<uint4*>(dv)[t - n16] = val;
-  }
+  const size_t rrec = static_cast<size_t>(nblk) * 512;             // uint16 per K (or V) record
+  uint16_t* rk = a.k_raw + (static_cast<size_t>(rs) * a.hkv + h) * rrec;
+  uint16_t* rv = a.v_raw + (static_cast<size_t>(rs) * a.hkv + h) * rrec;
+  walk([&](int blk, const uint4x2& v) {
+    const bool is_value = blk >= nblk;
+    const int bi = is_value ? blk - nblk : blk;
+    uint32_t u[8];
+    to_storage_order(v, is_value, my_stage, lane, u);
+    // raw blocks are half-major: the lane's storage positions 16*lane + 8*half + r sit at
+    // 256*half + 8*lane + r
+    uint8_t* dst = reinterpret_cast<uint8_t*>((is_value ? rv : rk) + static_cast<size_t>(bi) * 512);
+    *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(u[0], u[1], u[2], u[3]);
+    *reinterpret_cast<uint4*>(dst + 512 + 16 * lane) = make_uint4(u[4], u[5], u[6], u[7]);
+  });
   if (threadIdx.x == 0) a.dir[dir_at] = rs;
 }
 
@@ -445,13 +510,19 @@ extern "C" zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_
   a.page_ids = page_ids; a.n_valid = n_valid; a.raw_slots = raw_slots;
   a.num_pages = cache->num_pages; a.hkv = cache->num_kv_heads; a.page_size = cache->page_size;
   a.num_raw = cache->num_raw_slots; a.flags = flags;
-  const int nblk = cache->page_size / 4;
-  const size_t smem = static_cast<size_t>(2 * nblk) * (kSlotBytes + 1024) + 16;
-  if (cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return ZF_ERR_CUDA;
-  encode_kernel<<<dim3(n, cache->num_kv_heads), kCodecThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
-  return cudaGetLastError() == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
+  // programmatic stream serialisation: the grid may launch while its predecessor drains and waits
+  // for it (griddepcontrol.wait) before reading anything
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n, cache->num_kv_heads);
+  cfg.blockDim = dim3(32 * kEncodeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, encode_kernel, a) == cudaSuccess ? ZF_OK : ZF_ERR_CUDA;
 }
 
 extern "C" zf_status zf_append_tokens(const zf_cache* cache, const uint16_t* k_tok, const uint16_t* v_tok,

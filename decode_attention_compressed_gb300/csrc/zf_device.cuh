@@ -130,6 +130,24 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
   return y;
 }
 
+// Four 8x8 16-bit matrices from shared memory, lane l supplying the address of row l % 8 of
+// matrix l / 8; lane l receives elements (l / 4, 2(l % 4) .. +1) of each matrix (transposed with
+// .trans), one 32-bit register per matrix.
+__device__ __forceinline__ void ldmatrix_x4(const void* row, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_addr(row))
+               : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(const void* row, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_addr(row))
+               : "memory");
+}
+
 // 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); ex2(-inf) = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -133,8 +133,11 @@ size_t zf_page_head_bytes(int32_t page_size, int32_t compressed);
  *                 n_valid are stored as given).  Otherwise the page goes to its compressed slot.
  *   raw_slots:    [n] raw slot per page, or -1 when none is available (a page that then needs
  *                 raw storage gets ZF_DIR_INVALID and ZF_DEV_BAD_RAW_SLOT).
- *   Writes k_comp/v_comp or k_raw/v_raw and dir[page_ids[i]][*].  All pointers are device
- *   pointers; n == 0 is a no-op.  The source must not alias the cache.
+ *   Writes k_comp/v_comp or k_raw/v_raw and dir[page_ids[i]][*].  A full page head that ends up
+ *   raw (a block with more than 6 escapes) may also have had its compressed slot overwritten;
+ *   that slot is not read while the directory names the raw slot.  All pointers are device
+ *   pointers; n == 0 is a no-op.  The source must not alias the cache.  Launched with
+ *   programmatic stream serialisation (it waits for the preceding kernel before reading).
  */
 zf_status zf_encode_pages(const zf_cache* cache, const uint16_t* src_k, const uint16_t* src_v,
                           const int32_t* page_ids, const int32_t* n_valid,

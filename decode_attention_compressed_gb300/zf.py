@@ -71,6 +71,9 @@ SIGNATURES = {
     "zf_decode_attn_multi": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
                                         _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p, _c_void_p,
                                         _c_size_t, _c_void_p]),
+    "zf_decode_attn_multi_kernel": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
+                                               _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
+                                               _c_void_p, _c_size_t, _c_int32, _c_void_p]),
     "zf_dense_decode_attn_multi": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
                                               _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
                                               _c_void_p, _c_size_t, _c_void_p]),
@@ -317,11 +320,30 @@ def new_workspace(nbytes, device="cuda"):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
+# attention kernels of zf_decode_attn_multi_kernel
+KERNELS = {"auto": 0, "warp_mma": 1, "tcgen05": 2}
+
+
+def _kernel_code(kernel, dense):
+    if kernel not in KERNELS:
+        raise ValueError(f"kernel must be one of {sorted(KERNELS)}")
+    if dense and kernel != "auto":
+        raise ValueError("the dense comparator has one kernel (warp MMA)")
+    return KERNELS[kernel]
+
+
 def decode_attn(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse=None, workspace=None,
-                stream=None, dense=False):
+                stream=None, dense=False, kernel="auto"):
     """Decode attention over the cache.  q [B][Hq][128] int16 (BF16 bits), page_table [B][max_pages]
     int32, seq_lens [B] int32, all on the device.  Returns (out [B][Hq][128] f32, lse [B][Hq] f32).
-    dense=True runs zf_dense_decode_attn on the raw pool (page id = raw slot)."""
+    dense=True runs zf_dense_decode_attn on the raw pool (page id = raw slot).  kernel: "auto"
+    (zf_decode_attn), or "warp_mma" / "tcgen05" (zf_decode_attn_multi_kernel with one new token)."""
+    code = _kernel_code(kernel, dense)
+    if code:
+        o, l = decode_attn_multi(cache, q[:, None], page_table, seq_lens, scale,
+                                 out=None if out is None else out[:, None], lse=None if lse is None else lse[:, None],
+                                 workspace=workspace, stream=stream, kernel=kernel)
+        return o[:, 0], l[:, 0]
     q = _arg(q, "q", cache, _BITS16, (None, None, HEAD_DIM))
     B, Hq, _ = q.shape
     page_table, seq_lens = _attn_args(cache, q, page_table, seq_lens, B)
@@ -352,10 +374,12 @@ def workspace_size_multi(batch, tokens, num_q_heads, num_kv_heads, page_size, ma
 
 
 def decode_attn_multi(cache: Cache, q, page_table, seq_lens, scale=None, out=None, lse=None, workspace=None,
-                      stream=None, dense=False):
+                      stream=None, dense=False, kernel="auto"):
     """zf_decode_attn_multi: T new tokens per request.  q [B][T][Hq][128] int16 (BF16 bits); token t
     of request b attends to positions 0 .. seq_lens[b] - T + t.  Returns (out [B][T][Hq][128] f32,
-    lse [B][T][Hq] f32).  dense=True runs zf_dense_decode_attn_multi."""
+    lse [B][T][Hq] f32).  dense=True runs zf_dense_decode_attn_multi.  kernel: "auto", "warp_mma" or
+    "tcgen05" (zf_decode_attn_multi_kernel)."""
+    code = _kernel_code(kernel, dense)
     q = _arg(q, "q", cache, _BITS16, (None, None, None, HEAD_DIM))
     B, T, Hq, _ = q.shape
     page_table, seq_lens = _attn_args(cache, q, page_table, seq_lens, B)
@@ -369,11 +393,15 @@ def decode_attn_multi(cache: Cache, q, page_table, seq_lens, scale=None, out=Non
     if workspace is None:
         workspace = new_workspace(workspace_size_multi(B, T, Hq, cache.num_kv_heads, cache.page_size, max_pages), dev)
     d = cache.desc()
-    name = "zf_dense_decode_attn_multi" if dense else "zf_decode_attn_multi"
-    code = getattr(lib(), name)(ctypes.byref(d), _ptr(q), B, T, Hq, _ptr(page_table), max_pages, _ptr(seq_lens),
-                                scale, _ptr(out), _ptr(lse), _ptr(workspace),
-                                workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(name, code)
+    args = (ctypes.byref(d), _ptr(q), B, T, Hq, _ptr(page_table), max_pages, _ptr(seq_lens), scale, _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size())
+    if code:
+        name = "zf_decode_attn_multi_kernel"
+        status = lib().zf_decode_attn_multi_kernel(*args, code, _stream(stream))
+    else:
+        name = "zf_dense_decode_attn_multi" if dense else "zf_decode_attn_multi"
+        status = getattr(lib(), name)(*args, _stream(stream))
+    _check(name, status)
     return out, lse
 
 

@@ -267,6 +267,33 @@ zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t
                                const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Kernels zf_decode_attn_multi_kernel can be asked for. */
+#define ZF_KERNEL_AUTO 0       /* what zf_decode_attn and zf_decode_attn_multi run (below) */
+#define ZF_KERNEL_WARP_MMA 1   /* warp-level MMA, 8 query columns per pass over a kv head's tiles */
+#define ZF_KERNEL_TCGEN05 2    /* 5th-generation tensor cores, up to 32 columns per pass */
+
+/*
+ * zf_decode_attn_multi_kernel — zf_decode_attn_multi with the attention kernel chosen by `kernel`.
+ * ZipFusion §III.C: the compressed blocks are rebuilt into exact BF16 operands right before the
+ * tensor-core instructions.  The columns of a kv head are its query heads x new tokens
+ * ((num_q_heads / num_kv_heads) x T).
+ *  - ZF_KERNEL_WARP_MMA rebuilds each block in registers straight into warp-MMA (m16n8k16)
+ *    fragments: 8 columns per pass, so a kv head's K/V tiles are read once per 8 columns.
+ *  - ZF_KERNEL_TCGEN05 rebuilds each 16-token tile into shared-memory operands of tcgen05.mma
+ *    (M = 128 tokens or channels, N = 16 or 32 columns) whose scores and output accumulate in
+ *    tensor memory: up to 32 columns per pass, so tiles are read once per 32 columns.  Its shared
+ *    memory holds the request lengths: batch above about 3000 returns ZF_ERR_UNSUPPORTED.
+ *  - ZF_KERNEL_AUTO (what zf_decode_attn / zf_decode_attn_multi do) takes ZF_KERNEL_TCGEN05 when
+ *    a kv head has more than 8 columns and the batch fits, else ZF_KERNEL_WARP_MMA.
+ *   Both give the same results within floating-point rounding (different summation order).
+ *   Workspace: zf_decode_attn_multi_workspace_size covers every kernel.  Other arguments as for
+ *   zf_decode_attn_multi.  Returns ZF_ERR_INVALID_ARGUMENT for an unknown `kernel`.
+ */
+zf_status zf_decode_attn_multi_kernel(const zf_cache* cache, const uint16_t* q, int32_t batch, int32_t tokens,
+                                      int32_t num_q_heads, const int32_t* page_table, int32_t max_pages_per_req,
+                                      const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, int32_t kernel, void* stream);
+
 /*
  * zf_dense_decode_attn — the same decode attention over an uncompressed BF16 paged cache: page
  * id p of the page table is read from raw slot p of cache->k_raw / cache->v_raw (raw block

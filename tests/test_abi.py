@@ -172,6 +172,16 @@ def test_multi_token_attention_rejects_bad_token_counts(zf, dense):
     assert zf.lib().zf_decode_attn_multi_workspace_size(1, 2, 7, 2, 16, 4) == 0
 
 
+def test_kernel_choice_is_checked(zf):
+    """zf_decode_attn_multi_kernel rejects an unknown kernel before anything is launched."""
+    f = zf.lib().zf_decode_attn_multi_kernel
+    d = _desc(zf)
+    for bad in (-1, 3, 99):
+        assert f(ctypes.byref(d), 0x1000, 1, 1, 4, 0x2000, 4, 0x3000, 0.1, 0x4000, 0x5000, 0x6000, 1 << 20, bad,
+                 None) == -1
+    assert zf.KERNELS == {"auto": 0, "warp_mma": 1, "tcgen05": 2}
+
+
 def test_product_path_never_touches_the_oracle():
     """The library and its binding neither import nor read anything under oracle/ (the oracle is
     test infrastructure; a product path through it would be a CPU fallback)."""

@@ -77,6 +77,15 @@ def test_small_cases(zf, name):
     out, lse = _run(zf, layer, gc)
     H.compare_attention(out, lse, ref_out, ref_lse)
     assert gc.status_word() == 0
+    # each compressed kernel on its own, whichever the call would pick (the tensor-memory kernel
+    # also for a single column per kv head: one of 16 MMA columns used)
+    dev = torch.device("cuda")
+    for kernel in ("warp_mma", "tcgen05"):
+        o, l = zf.decode_attn(gc, layer.q.to(dev), layer.page_table.to(dev), layer.seq_lens.to(dev), layer.scale,
+                              kernel=kernel)
+        torch.cuda.synchronize()
+        H.compare_attention(o, l, ref_out, ref_lse)
+        assert gc.status_word() == 0, kernel
     dc = H.gpu_cache_from(layer, zf, force_raw=True)
     dout, dlse = _run(zf, layer, dc, dense=True)
     H.compare_attention(dout, dlse, ref_out, ref_lse)
@@ -99,13 +108,18 @@ def test_mixed_raw_and_compressed_pages(zf):
     H.compare_attention(out, lse, ref_out, ref_lse)
 
 
-def test_deterministic(zf):
-    w, lens = CASES["gqa7_spikes"]
-    layer = I.make_layer(w, seq_lens=lens)
-    gc = H.gpu_cache_from(layer, zf)
-    a = _run(zf, layer, gc)
-    b = _run(zf, layer, gc)
-    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+@pytest.mark.parametrize("kernel", ["warp_mma", "tcgen05"])
+def test_deterministic(zf, kernel):
+    for name in ("gqa7_spikes", "balanced_two_slices"):
+        w, lens = CASES[name]
+        layer = I.make_layer(w, seq_lens=lens)
+        gc = H.gpu_cache_from(layer, zf)
+        dev = torch.device("cuda")
+        args = (gc, layer.q.to(dev), layer.page_table.to(dev), layer.seq_lens.to(dev), layer.scale)
+        a = zf.decode_attn(*args, kernel=kernel)
+        b = zf.decode_attn(*args, kernel=kernel)
+        torch.cuda.synchronize()
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
 def test_one_workspace_across_calls_of_different_shapes(zf):
@@ -306,19 +320,26 @@ MULTI_CASES = {
     "page64_t8": (W(2, 4, 4, 64, 400, pool="random", seed=45), [400, 129], 8),
     "tokens_that_see_nothing": (W(3, 4, 2, 16, 10, seed=46), [3, 1, 10], 4),
     "one_token": (W(2, 8, 2, 16, 100, seed=47), [100, 31], 1),
+    # 32 columns per kv head (GQA 16 x 2 tokens): one tensor-memory pass, four warp-MMA passes
+    "gqa16_t2": (W(3, 32, 2, 16, 700, pool="random", seed=48), [700, 129, 5], 2),
+    # 16 columns from MHA x 16 tokens, 64-token pages, ragged
+    "mha_t16_page64": (W(2, 2, 2, 64, 530, pool="random", seed=49), [530, 200], 16),
+    # 40 columns: a 32-column slice and an 8-column slice
+    "gqa20_t2_two_slices": (W(2, 40, 2, 16, 300, pool="random", seed=50), [300, 250], 2),
 }
 
 
-@pytest.mark.parametrize("dense", [False, True])
+@pytest.mark.parametrize("kernel", ["auto", "warp_mma", "tcgen05", "dense"])
 @pytest.mark.parametrize("name", sorted(MULTI_CASES))
-def test_multi_token_cases(zf, name, dense):
+def test_multi_token_cases(zf, name, kernel):
     w, lens, T = MULTI_CASES[name]
+    dense = kernel == "dense"
     layer = I.make_layer(w, seq_lens=lens)
     gc = H.gpu_cache_from(layer, zf, force_raw=dense)
     q = I.make_multi_queries(w, T)
     dev = torch.device("cuda")
     out, lse = zf.decode_attn_multi(gc, q.to(dev), layer.page_table.to(dev), layer.seq_lens.to(dev), layer.scale,
-                                    dense=dense)
+                                    dense=dense, kernel="auto" if dense else kernel)
     torch.cuda.synchronize()
     assert gc.status_word() == 0
     oc = H.oracle_cache_from(layer, O, force_raw=dense)
@@ -327,7 +348,8 @@ def test_multi_token_cases(zf, name, dense):
     H.compare_attention(out, lse, ref_out, ref_lse)
     if T == 1:   # the same bits as the single-token entry point
         o1, l1 = zf.decode_attn(gc, q[:, 0].contiguous().to(dev), layer.page_table.to(dev),
-                                layer.seq_lens.to(dev), layer.scale, dense=dense)
+                                layer.seq_lens.to(dev), layer.scale, dense=dense,
+                                kernel="auto" if dense else kernel)
         torch.cuda.synchronize()
         assert torch.equal(o1, out[:, 0]) and torch.equal(l1, lse[:, 0])
 
@@ -354,6 +376,45 @@ def test_multi_token_full_size_sampled(zf):
         pages = torch.as_tensor(table[b, : -(-L // w.page_size)], dtype=torch.long, device="cuda")
         K = H.np_bits(layer.k_pages[pages, h].reshape(-1, 128))[:L]
         V = H.np_bits(layer.v_pages[pages, h].reshape(-1, 128))[:L]
+        ref_out[b, t, h], ref_lse[b, t, h], _ = O.attention_one(O.bf16_to_f64(qn[b, t, h]), O.bf16_to_f64(K),
+                                                                O.bf16_to_f64(V), layer.scale)
+    H.compare_attention(out, lse, ref_out, ref_lse, pairs=picks)
+
+
+def test_tcgen05_full_size_sampled_two_tokens(zf):
+    """Two new tokens per request on the Qwen2-7B max-batch shape (GQA 7: 14 columns per kv head),
+    one layer in the benchmark's launch configuration: the tensor-memory kernel (what the call
+    picks) on sampled (request, token, head) outputs against float64 attention, and every output
+    against the warp-MMA kernel."""
+    w = I.WORKLOADS["qwen2_7b_maxbatch"]
+    T = 2
+    layer = I.make_layer(w, layer=0, device="cuda")
+    npg = layer.num_pages
+    gc = zf.Cache(npg, w.num_kv_heads, w.page_size, npg)
+    zf.encode_pages(gc, layer.k_pages, layer.v_pages, list(range(npg)), layer.n_valid, list(range(npg)))
+    q = I.make_multi_queries(w, T, device="cuda")
+    ws = zf.new_workspace(zf.workspace_size_multi(w.batch, T, w.num_q_heads, w.num_kv_heads, w.page_size,
+                                                  w.max_pages))
+    out, lse = zf.decode_attn_multi(gc, q, layer.page_table, layer.seq_lens, layer.scale, workspace=ws)
+    mo, ml = zf.decode_attn_multi(gc, q, layer.page_table, layer.seq_lens, layer.scale, workspace=ws,
+                                  kernel="warp_mma")
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    d = (out - mo).abs()
+    assert float(d.max()) <= 2 * H.MAX_ABS and float(d.mean()) <= H.MEAN_ABS
+    assert float((lse - ml).abs().max()) <= 2 * H.LSE_ABS
+    rng = np.random.default_rng(7)
+    picks = sorted({(int(rng.integers(w.batch)), t, int(rng.integers(w.num_q_heads))) for t in range(T) for _ in range(24)}
+                   | {(0, 0, 0), (w.batch - 1, T - 1, w.num_q_heads - 1)})
+    qn, table, lens = H.np_bits(q), layer.page_table.cpu().numpy(), layer.seq_lens.cpu().numpy()
+    ref_out = np.zeros(tuple(out.shape))
+    ref_lse = np.full(tuple(lse.shape), -math.inf)
+    for b, t, h in picks:
+        L = int(lens[b]) - T + t + 1
+        pages = torch.as_tensor(table[b, : -(-L // w.page_size)], dtype=torch.long, device="cuda")
+        g = h // w.group
+        K = H.np_bits(layer.k_pages[pages, g].reshape(-1, 128))[:L]
+        V = H.np_bits(layer.v_pages[pages, g].reshape(-1, 128))[:L]
         ref_out[b, t, h], ref_lse[b, t, h], _ = O.attention_one(O.bf16_to_f64(qn[b, t, h]), O.bf16_to_f64(K),
                                                                 O.bf16_to_f64(V), layer.scale)
     H.compare_attention(out, lse, ref_out, ref_lse, pairs=picks)

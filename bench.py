@@ -339,9 +339,10 @@ class Workbench:
     workspace, and the decode step over them (CUDA graph, or eager for the long-context step whose
     appends change pointers every step)."""
 
-    def __init__(self, zf, I, w, device, tokens=1, world=1, local_rank=0, max_steps=0):
+    def __init__(self, zf, I, w, device, tokens=1, world=1, local_rank=0, max_steps=0, kernel="auto"):
         import torch
         self.zf, self.I, self.w, self.device, self.T = zf, I, w, device, tokens
+        self.kernel = kernel            # compressed attention kernel: auto, warp_mma or tcgen05
         self.world, self.local_rank = world, local_rank
         if tokens > 1 and w.name == "long_ctx":
             raise SystemExit("--tokens > 1 is not combined with the long-context append step")
@@ -364,12 +365,13 @@ class Workbench:
 
     # ---- the step
     def attn(self, cache, q, table, lens, scale, out, lse, dense=False):
+        kernel = "auto" if dense else self.kernel
         if self.T > 1:
             self.zf.decode_attn_multi(cache, q, table, lens, scale, out=out, lse=lse, workspace=self.workspace,
-                                      dense=dense)
+                                      dense=dense, kernel=kernel)
         else:
             self.zf.decode_attn(cache, q, table, lens, scale, out=out, lse=lse, workspace=self.workspace,
-                                dense=dense)
+                                dense=dense, kernel=kernel)
 
     def step(self, dense=False, events=None, reencode=False):
         if self.append is not None:
@@ -670,7 +672,7 @@ def run_gpu(args, rank, world, local_rank):
     max_steps = 4 * (args.steps + args.warmup) + 64
     if w.name == "long_ctx":
         max_steps = max(max_steps, 2 * math.ceil(MIN_TIMED_MS / 0.2) + 64)
-    wb = Workbench(zf, I, w, device, T, world, local_rank, max_steps)
+    wb = Workbench(zf, I, w, device, T, world, local_rank, max_steps, kernel=args.kernel)
     layers = wb.layers
     L = len(layers)
     use_graph = wb.append is None           # the append step changes pointers every step: eager
@@ -731,7 +733,7 @@ def run_gpu(args, rank, world, local_rank):
         vs_baseline=None, dtype="bf16", data="synthetic (seeded, distributions of the workload)",
         config={"workload": w.name, "note": w.note, "batch": w.batch, "q_heads": w.num_q_heads,
                 "kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": w.page_size, "ctx": w.ctx,
-                "layers_per_step": w.layers, "new_tokens_per_request": T,
+                "layers_per_step": w.layers, "new_tokens_per_request": T, "kernel": args.kernel,
                 "parallelism": "replicas" if world > 1 else "single",
                 "l2": f"no flush: {comp_bytes / 1e9:.2f} GB of compressed KV read per step "
                       f"(> {L2_BYTES / 2**20:.0f} MiB L2)"},
@@ -939,6 +941,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="measure only the headline workload (no per_config object)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "warp_mma", "tcgen05"],
+                    help="compressed attention kernel (zf_decode_attn_multi_kernel)")
     ap.add_argument("--tokens", type=int, default=1,
                     help="new tokens per request per call (speculative verification; zf_decode_attn_multi)")
     ap.add_argument("--layers", type=int, default=None,

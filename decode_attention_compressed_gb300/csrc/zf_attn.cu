@@ -711,14 +711,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
   if (lane == 0) a.lse[row] = (M + fast_log2(lsum)) * kLn2;
 }
 
-// Which kernel a compressed call runs: ZF_KERNEL_AUTO takes the tensor-memory kernel when a kv
-// head has more query columns (query heads per kv head x new tokens) than one warp-MMA tile holds
-// and the request lengths fit its shared memory.  Returns whether it is the tensor-memory kernel,
-// or -1 when the requested kernel cannot run these sizes.
+// Which kernel a compressed call runs.  ZF_KERNEL_AUTO runs the warp-MMA kernel: on GB300 it is
+// the faster one on every shape measured, also where it reads a kv head's tiles twice or four
+// times (GQA-7 with 2 or 4 new tokens: 502 against 616 us, 988 against 1209 us per call).
+// Returns whether it is the tensor-memory kernel, or -1 when that kernel cannot run these sizes.
 static int pick_tc(int32_t kernel, int batch, int hq, int hkv) {
-  if (kernel == ZF_KERNEL_WARP_MMA) return 0;
+  (void)hq;
+  (void)hkv;
   if (kernel == ZF_KERNEL_TCGEN05) return attention_tc_fits(batch) ? 1 : -1;
-  return hq / hkv > kHeadsPerSlice && attention_tc_fits(batch) ? 1 : 0;
+  return 0;
 }
 
 static Plan compressed_plan(bool tc, int batch, int hq, int hkv, int page_size, int max_pages, int num_sms) {

@@ -33,7 +33,7 @@ constexpr int kWarpStages = 2;
 constexpr int kTileCompBytes = 4 * kSlotBytes;      // 3136: one 16-token tile of K (or V), compressed
 constexpr int kTileRawBytes = 4 * kRawBlockBytes;   // 4096
 constexpr int kHeadsPerSlice = 8;                   // MMA n of the warp-MMA kernel
-constexpr int kTcMaxCols = 32;                      // MMA n of the tensor-memory kernel (16 or 32)
+constexpr int kTcMaxCols = 16;                      // MMA n of the tensor-memory kernel
 constexpr int kMaxItemTiles = 512;                  // 16-token tiles per work item (metadata buffer size)
 constexpr int kMaxItemPages = 256;                  // pages per work item (page-table loads per lane: /32)
 // q rows in shared memory: channel words permuted so that lane (gi, ti) finds the four B-fragment

@@ -10,24 +10,25 @@
 // operations right before the tensor-core instructions; raw blocks need no rebuild.  §IV.B: split
 // chunks are combined by a split-result merge.
 //
-// One CTA per SM, 14 warps:
-//  * warps 0-7 (rebuild): warp r takes tile r of every 128-token group of an item (16 tokens of
-//    one kv head); it copies its tiles HBM -> its two private stages with 1-D bulk copies (the next
-//    tile in flight while it works on this one), rebuilds the tile's K rows into the K operand
-//    (A of S^T = K Q^T: 128 tokens x 128 channels) and its V^T columns into the V operand (A of
-//    O^T = V^T P^T: 128 channels x 128 tokens), K-major core-matrix layout, straight from the
-//    m16n8k16 fragment registers the rebuild produces (one conflict-free 32-bit store per lane
-//    fills one 8 x 16-byte core matrix);
-//  * warps 8-11 (softmax warpgroup; warp w reads TMEM lanes 32(w%4)..): S^T comes out of tensor
+// One CTA per SM, 22 warps:
+//  * warps 0-7 rebuild K, warps 8-15 rebuild V: warp r (mod 8) takes tile slot r of every
+//    128-token group of an item (16 tokens of one kv head).  It copies its half of the tile HBM ->
+//    its two private stages with 1-D bulk copies (the next in flight while it works on this one)
+//    and rebuilds it into the K operand (A of S^T = K Q^T: 128 tokens x 128 channels) or the V
+//    operand (A of O^T = V^T P^T: 128 channels x 128 tokens), K-major core-matrix layout, straight
+//    from the m16n8k16 fragment registers the rebuild produces (one conflict-free 32-bit store per
+//    lane fills one 8 x 16-byte core matrix).  K and V warps wait only for the MMA that last read
+//    their own operand, so the keys of the next group are rebuilt while this group's softmax runs;
+//  * warps 16-19 (softmax warpgroup; warp w reads TMEM lanes 32(w%4)..): S^T comes out of tensor
 //    memory in the m16n8 accumulator layout, the online softmax runs in the log2 domain with one
 //    running max per column shared by the warpgroup (raised only when a score exceeds it by more
-//    than 8, after a warpgroup vote; the output in tensor memory is then rescaled in place), and
-//    P^T (BF16 high part + BF16 remainder) is transposed with movmatrix into the P operand; at the
-//    end of an item it divides O^T by the column sums and writes the output or the partial;
-//  * warp 12 (MMA): allocates tensor memory and one lane issues the MMAs: per group 8 x
-//    (M128 N{16,32} K16) for S^T into one of two TMEM score buffers, then 2 x 8 for O^T += V^T P^T
-//    (high and low parts), signalling completion through tcgen05.commit on mbarriers;
-//  * warp 13 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
+//    than 8, after a warpgroup vote; the output in tensor memory is then rescaled in place), P^T
+//    (BF16 high part + BF16 remainder) is transposed with movmatrix into the P operand, and the
+//    warpgroup's first thread issues O^T += V^T P^T (2 x 8 MMAs) into tensor memory; at the end of
+//    an item it divides O^T by the column sums and writes the output or the partial;
+//  * warp 20 (QK): allocates tensor memory; one lane issues S^T = K Q^T (8 x M128 N{16,32} K16)
+//    into one of two TMEM score buffers per group, completion signalled by tcgen05.commit;
+//  * warp 21 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
 //    item ahead: resolves the pages through the page table and the directory and stages the
 //    item's query rows as the B operand of S^T.
 // Every wait is bounded (2 s); a wait that gives up sets ZF_DEV_TIMEOUT and the CTA winds down
@@ -41,50 +42,58 @@
 namespace zf {
 namespace {
 
-constexpr int kRebuildWarps = 8;
-constexpr int kSoftmaxWarp0 = 8;                  // warps 8..11: TMEM lane quadrants 0..3
-constexpr int kMmaWarp = 12;
-constexpr int kMetaWarp = 13;
-constexpr int kTcWarps = 14;
+constexpr int kHalfWarps = 8;                     // warps per half: 8 rebuild K rows, 8 rebuild V^T columns
+constexpr int kRebuildWarps = 2 * kHalfWarps;
+constexpr int kSoftmaxWarp0 = 16;                 // warps 16..19: TMEM lane quadrants 0..3
+constexpr int kQkWarp = 20;
+constexpr int kMetaWarp = 21;
+constexpr int kTcWarps = 22;
 constexpr int kTcThreads = kTcWarps * 32;
-constexpr int kTcStageBytes = Cfg<true>::kStageBytes;   // one compressed K + V tile (a raw tile: K, then V)
-constexpr int kTcVOffset = Cfg<true>::kVOffset;
+constexpr int kHalfStageBytes = kTileCompBytes;   // one compressed K (or V) half tile; a raw half: 3 + 1 blocks
 constexpr int kOpBytes = 128 * 128 * 2;           // one 128 x 128 BF16 operand
 constexpr int kCoreRow = 2048;                    // bytes between core-matrix rows along M/N (16 along K)
-constexpr uint32_t kTmemCols = 128;               // two score buffers + the output, <= 32 columns each
+// Tensor memory: two score buffers (kCols columns each) and the output at columns 0 .. 3 kCols,
+// and two K operands (128 tokens x 128 channels as BF16 pairs: 64 columns each) from column 128.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemK = 128;
 constexpr int kSoftmaxBarrier = 1;                // named barrier of the softmax warpgroup
 
 // Barriers (mbarrier index in the shared array).
+// Copy stages per rebuild warp: the V warps' copies are the ones the PV products wait for, so
+// they run three deep; the K warps' two.
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
+constexpr int kNumStages = kHalfWarps * (kKStages + kVStages);
+
 enum : int {
-  kBarStage = 0,                // 2 per rebuild warp: its tile copies
-  kBarItemFull = 16,            // [2] the metadata warp published an item
-  kBarItemEmpty = 18,           // [2] rebuild + softmax warps are done with it
-  kBarQFull = 20,               // [2] the item's query operand is staged
-  kBarKFull = 22,               // the 8 rebuild warps wrote a group's K operand
-  kBarVFull = 23,               // ... and its V operand
-  kBarKFree = 24,               // S^T = K Q^T of a group completed (commit)
-  kBarVFree = 25,               // O^T += V^T P^T of a group completed (commit): V and P operands free
-  kBarSFull = 26,               // [2] scores of a group in TMEM buffer (commit)
-  kBarSFree = 28,               // [2] the softmax warpgroup read that score buffer
-  kBarPFull = 30,               // the softmax warpgroup wrote a group's P operand
-  kBarOFree = 31,               // the softmax warpgroup read an item's output from TMEM
-  kBarDrain = 32,               // end of the CTA: every MMA issued has completed
-  kNumBars = 33,
+  kBarStage = 0,                // one per copy stage of the rebuild warps (K warps first)
+  kBarItemFull = kNumStages,    // [2] the metadata warp published an item
+  kBarItemEmpty = kBarItemFull + 2,   // [2] rebuild + softmax warps are done with it
+  kBarQFull = kBarItemEmpty + 2,      // [2] the item's query operand is staged
+  kBarKFull = kBarQFull + 2,          // [2] the 8 K warps wrote a group's K operand (per K buffer)
+  kBarVFull = kBarKFull + 2,          // [2] the 8 V warps wrote a group's V operand (per V buffer)
+  kBarKFree = kBarVFull + 2,          // [2] S^T = K Q^T of a group completed, per K buffer (commit)
+  kBarSFull = kBarKFree + 2,          // [2] scores of a group in TMEM buffer (commit)
+  kBarSFree = kBarSFull + 2,          // [2] the softmax warpgroup read that score buffer
+  kBarPFull = kBarSFree + 2,          // [2] the softmax warpgroup wrote a group's P operand (per P buffer)
+  kBarPvDone = kBarPFull + 2,         // [2] O^T += V^T P^T of a group completed, per V / P buffer (commit)
+  kBarOFree = kBarPvDone + 2,         // the softmax warpgroup read an item's output from tensor memory
+  kBarDrain = kBarOFree + 1,          // end of the CTA: every MMA issued has completed
+  kNumBars = kBarDrain + 1,
 };
 
 struct TcLayout {
-  size_t kop, vop, pop, qop, stages, meta, desc, bars, misc, red, prefix, lens, total;
+  size_t vop, pop, qop, stages, meta, desc, bars, misc, red, prefix, lens, total;
 };
 
 template <int kCols>
 __host__ __device__ inline TcLayout tc_layout(int batch) {
   TcLayout s;
   size_t at = 0;
-  s.kop = at; at += kOpBytes;
-  s.vop = at; at += kOpBytes;
-  s.pop = at; at += 2 * kCols * 256;              // P^T: high part, then low part (kCols x 128 BF16 each)
+  s.vop = at; at += 2 * kOpBytes;                 // two V operands (groups alternate)
+  s.pop = at; at += 4 * kCols * 256;              // P^T, two buffers: high part, then low part (kCols x 128 BF16 each)
   s.qop = at; at += 2 * kCols * 256;              // Q of two items (kCols x 128 BF16 each)
-  s.stages = at; at += static_cast<size_t>(kRebuildWarps) * kWarpStages * kTcStageBytes;
+  s.stages = at; at += static_cast<size_t>(kNumStages) * kHalfStageBytes;
   s.meta = at; at += 2 * kMaxItemTiles * 4;
   s.desc = at; at += 2 * 64;
   s.bars = at; at += kNumBars * 8;
@@ -121,64 +130,104 @@ __device__ __forceinline__ bool wg_any(bool v) {
   return r != 0;
 }
 
-// K rows of tile p (tokens 16p .. 16p+15 of the group) into the K operand.  Register i of a half
-// of a lane's fragment (rows g = lane/4 (+8 for i odd), columns 2(lane%4) (+8 for i >= 2)) is core
-// matrix (m-block 2p + (i & 1), k-block 4j + 2h + (i >> 1)) of channel group j, half h.
-__device__ __forceinline__ void write_k_tile(const uint8_t* st, bool comp, uint8_t* kop, int p, int lane) {
-  uint8_t* base = kop + (2 * p) * kCoreRow + (lane >> 2) * 16 + (lane & 3) * 4;
-  uint32_t hdr[4] = {0u, 0u, 0u, 0u};
-  bool fast = false;
-  if (comp) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) hdr[j] = *reinterpret_cast<const uint32_t*>(st + j * kSlotBytes + kHeaderAt);
-    fast = ((hdr[0] | hdr[1] | hdr[2] | hdr[3]) & kHeaderEscMask) == 0;
+// Start the copy of the K (is_v false) or V half of tile u of an item into `stage`: a compressed
+// half (3136 bytes) whole, a raw half's first three blocks (its fourth is fetched once those are
+// used, see fetch_raw_block3).  Returns the tile's kind (nothing is armed for an invalid one).
+__device__ __forceinline__ int issue_half(const AttnArgs& a, const ItemDesc& d, const int* meta, int u, bool is_v,
+                                          uint8_t* stage, uint64_t* bar, int lane, uint64_t policy) {
+  const int m = meta[u];
+  const int kind = m & 3;
+  const size_t head = static_cast<size_t>(m >> 5) * a.hkv + d.g;
+  const int t = (m >> 2) & 7;
+  if (lane == 0) {
+    if (kind == kKindComp) {
+      mbar_arrive_expect_tx(bar, kTileCompBytes);
+      bulk_copy_g2s(stage, (is_v ? a.v_comp : a.k_comp) + head * a.comp_head_bytes + static_cast<size_t>(t) * kTileCompBytes,
+                    kTileCompBytes, bar, policy);
+    } else if (kind == kKindRaw) {
+      mbar_arrive_expect_tx(bar, 3 * kRawBlockBytes);
+      bulk_copy_g2s(stage, (is_v ? a.v_raw : a.k_raw) + head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes,
+                    3 * kRawBlockBytes, bar, policy);
+    }
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t ka[8];
-    if (fast) rebuild_lane_noesc(st + j * kSlotBytes, lane, __byte_perm(hdr[j], 0u, 0x0000u), ka);
-    else if (comp) rebuild_lane(st + j * kSlotBytes, lane, ka);
-    else load_raw_lane(st + j * kRawBlockBytes, lane, ka);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint32_t*>(base + (i & 1) * kCoreRow + (4 * j + 2 * h + (i >> 1)) * 128) = ka[4 * h + i];
+  return kind;
+}
+
+// The fourth block of a raw half of tile u, into the start of `stage` (its first three blocks
+// have been used).
+__device__ __forceinline__ void fetch_raw_block3(const AttnArgs& a, const ItemDesc& d, const int* meta, int u,
+                                                 bool is_v, uint8_t* stage, uint64_t* bar, int lane, uint64_t policy) {
+  const int m = meta[u];
+  const size_t head = static_cast<size_t>(m >> 5) * a.hkv + d.g;
+  const int t = (m >> 2) & 7;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, kRawBlockBytes);
+    bulk_copy_g2s(stage, (is_v ? a.v_raw : a.k_raw) + head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes +
+                             3 * kRawBlockBytes,
+                  kRawBlockBytes, bar, policy);
   }
 }
 
-// V^T columns of tile p (tokens 16p ..) into the V operand; values of tokens at or past ntok are
-// zeroed (they may hold anything).  Register i of a half (V^T rows = channels g (+8 for i odd),
-// columns = tokens 2(lane%4) (+8 for i >= 2)) is core matrix (m-block 4j + 2h + (i & 1), k-block
-// 2p + (i >> 1)).
-__device__ __forceinline__ void write_v_tile(const uint8_t* st, bool comp, int ntok, uint8_t* vop, int p, int lane) {
-  const int ti = lane & 3;
-  uint8_t* base = vop + (2 * p) * 128 + (lane >> 2) * 16 + ti * 4;
-  uint32_t keep_a = 0xFFFFFFFFu, keep_b = 0xFFFFFFFFu;
-  if (ntok < 16) {
-    keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
-    keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
-  }
-  uint32_t hdr[4] = {0u, 0u, 0u, 0u};
-  bool fast = false;
-  if (comp) {
+// Fragment registers -> operand.  K (A of S^T = K Q^T, rows = tokens) goes to tensor memory:
+// the rows of tile slot p are TMEM lanes 16p .. 16p+15 and the 128 channels are 64 columns of BF16
+// pairs, in a channel order permuted within each 16-channel span (element 4c + m of a span holds
+// channel {2c, 2c+1, 2c+8, 2c+9}[m]; the query operand uses the same order, which leaves q.k
+// unchanged).  That order is the one tcgen05.st.16x256b takes from the m16n8k16 fragments: a
+// thread's registers for span 2j + h are {a0a1, a4a5, a2a3, a6a7} of half h of channel group j.
+// V^T (A of O^T = V^T P^T, rows = channels) goes to shared memory: register i of half h of channel
+// group j (rows g = lane/4 (+8 for i odd), columns 2(lane%4) (+8 for i >= 2)) is core matrix
+// (m-block 4j + 2h + (i & 1), k-block 2p + (i >> 1)); values of tokens at or past the context's end
+// are zeroed by keep_a / keep_b.
+__device__ __forceinline__ void store_k_block(const uint32_t (&ka)[8], int j, uint32_t k_tmem) {
+  const uint32_t r[8] = {ka[0], ka[2], ka[1], ka[3], ka[4], ka[6], ka[5], ka[7]};
+  tmem_st_16x256b_x2(k_tmem + 16 * j, r);
+}
+__device__ __forceinline__ void store_v_block(const uint32_t (&va)[8], int j, uint8_t* vop, int p, int lane,
+                                              uint32_t keep_a, uint32_t keep_b) {
+  uint8_t* base = vop + (2 * p) * 128 + (lane >> 2) * 16 + (lane & 3) * 4;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<uint32_t*>(base + (4 * j + 2 * h + (i & 1)) * kCoreRow + (i >> 1) * 128) =
+          va[4 * h + i] & ((i >> 1) ? keep_b : keep_a);
+}
+
+// One half tile (K or V, 4 blocks) from its stage into its operand.  kind: compressed or raw (a raw
+// half holds its first three blocks; fetch3() brings the fourth into the start of the stage and
+// returns false when its wait gave up).  Returns false only then.
+template <bool kV, typename Fetch3>
+__device__ __forceinline__ bool rebuild_half(const uint8_t* st, int kind, uint32_t keep_a, uint32_t keep_b, uint8_t* vop_g,
+                                             int p, uint32_t k_tmem, int lane, Fetch3&& fetch3) {
+  auto put = [&](const uint32_t (&x)[8], int j) {
+    if constexpr (kV) store_v_block(x, j, vop_g, p, lane, keep_a, keep_b);
+    else store_k_block(x, j, k_tmem);
+  };
+  if (kind == kKindComp) {
+    uint32_t hdr[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) hdr[j] = *reinterpret_cast<const uint32_t*>(st + j * kSlotBytes + kHeaderAt);
-    fast = ((hdr[0] | hdr[1] | hdr[2] | hdr[3]) & kHeaderEscMask) == 0;
+    const bool escapes = ((hdr[0] | hdr[1] | hdr[2] | hdr[3]) & kHeaderEscMask) != 0;
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+      uint32_t x[8];
+      if (escapes) rebuild_lane(st + j * kSlotBytes, lane, x);
+      else rebuild_lane_noesc(st + j * kSlotBytes, lane, __byte_perm(hdr[j], 0u, 0x0000u), x);
+      put(x, j);
+    }
+    return true;
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t va[8];
-    if (fast) rebuild_lane_noesc(st + j * kSlotBytes, lane, __byte_perm(hdr[j], 0u, 0x0000u), va);
-    else if (comp) rebuild_lane(st + j * kSlotBytes, lane, va);
-    else load_raw_lane(st + j * kRawBlockBytes, lane, va);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint32_t*>(base + (4 * j + 2 * h + (i & 1)) * kCoreRow + (i >> 1) * 128) =
-            va[4 * h + i] & ((i >> 1) ? keep_b : keep_a);
+#pragma unroll 1
+  for (int j = 0; j < 3; ++j) {
+    uint32_t x[8];
+    load_raw_lane(st + j * kRawBlockBytes, lane, x);
+    put(x, j);
   }
+  if (!fetch3()) return false;
+  uint32_t x[8];
+  load_raw_lane(st, lane, x);
+  put(x, 3);
+  return true;
 }
 
 // Zero V^T columns of tile slot p (a group with fewer than 8 tiles, or a page that could not be
@@ -193,18 +242,26 @@ __device__ __forceinline__ void zero_v_tile(uint8_t* vop, int p, int lane) {
 }
 
 // The item's query rows as the B operand of S^T = K Q^T (column n = query head d.h0 + n, K-major:
-// core matrix (n / 8, channel / 8)); columns past d.nh are zero.
+// core matrix (n / 8, k / 8)); columns past d.nh are zero.  K index k holds channel
+// 16 (k / 16) + {2c, 2c+1, 2c+8, 2c+9}[k % 4], c = (k % 16) / 4: the order of the K operand.
 template <int kCols>
 __device__ __forceinline__ void stage_q(const AttnArgs& a, const ItemDesc& d, uint8_t* qb, int lane) {
-#pragma unroll 4
-  for (int it = 0; it < kCols / 2; ++it) {
-    const int n = 2 * it + (lane >> 4), ck = lane & 15;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 2
+  for (int it = 0; it < kCols / 4; ++it) {
+    // lane: column n, 16-channel span sp (two 16-byte chunks of the operand)
+    const int n = 4 * it + (lane >> 3), sp = lane & 7;
+    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
     if (n < d.nh) {
       const size_t row = query_row(d.b, d.h0 + n, a.tokens, a.hq);
-      v = *reinterpret_cast<const uint4*>(a.q + row * ZF_HEAD_DIM + 8 * ck);
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + row * ZF_HEAD_DIM + 16 * sp);
+      lo = src[0];      // channel pairs 0..3 of the span
+      hi = src[1];      // channel pairs 4..7
     }
-    *reinterpret_cast<uint4*>(qb + (n >> 3) * kCoreRow + ck * 128 + (n & 7) * 16) = v;
+    // chunk 0: pairs (0,1) (8,9) (2,3) (10,11) -> words 0, 4, 1, 5; chunk 1: words 2, 6, 3, 7
+    *reinterpret_cast<uint4*>(qb + (n >> 3) * kCoreRow + (2 * sp) * 128 + (n & 7) * 16) =
+        make_uint4(lo.x, hi.x, lo.y, hi.y);
+    *reinterpret_cast<uint4*>(qb + (n >> 3) * kCoreRow + (2 * sp + 1) * 128 + (n & 7) * 16) =
+        make_uint4(lo.z, hi.z, lo.w, hi.w);
   }
 }
 
@@ -220,9 +277,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   constexpr uint32_t kIdesc = umma_idesc_bf16(128, kCols);
   extern __shared__ __align__(1024) uint8_t smem[];
   const TcLayout L = tc_layout<kCols>(a.batch);
-  uint8_t* kop = smem + L.kop;
   uint8_t* vop = smem + L.vop;
-  uint8_t* pop = smem + L.pop;                    // high part; the low part follows at + kCols * 256
+  uint8_t* pop = smem + L.pop;                    // buffer b at + b * 2 * kCols * 256: high part, then low part
   uint8_t* qop = smem + L.qop;
   uint8_t* stages = smem + L.stages;
   int* meta = reinterpret_cast<int*>(smem + L.meta);
@@ -236,7 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * kRebuildWarps; ++i) mbar_init(&bars[kBarStage + i], 1);
+    for (int i = 0; i < kNumStages; ++i) mbar_init(&bars[kBarStage + i], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[kBarItemFull + b], 1);
       mbar_init(&bars[kBarItemEmpty + b], kRebuildWarps + 4);
@@ -244,17 +300,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       mbar_init(&bars[kBarSFull + b], 1);
       mbar_init(&bars[kBarSFree + b], 4);
     }
-    mbar_init(&bars[kBarKFull], kRebuildWarps);
-    mbar_init(&bars[kBarVFull], kRebuildWarps);
-    mbar_init(&bars[kBarKFree], 1);
-    mbar_init(&bars[kBarVFree], 1);
-    mbar_init(&bars[kBarPFull], 4);
-    mbar_init(&bars[kBarOFree], 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[kBarKFull + b], kHalfWarps);
+      mbar_init(&bars[kBarVFull + b], kHalfWarps);
+      mbar_init(&bars[kBarKFree + b], 1);
+    }
     mbar_init(&bars[kBarDrain], 1);
+    mbar_init(&bars[kBarOFree], 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[kBarPvDone + b], 1);
+      mbar_init(&bars[kBarPFull + b], 4);
+    }
     *abort_flag = 0;
   }
   fence_mbar_init();
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kQkWarp) tmem_alloc(tmem_slot, kTmemCols);
   tcgen05_before_sync();
   wait_prior_grid();          // inputs may come from the preceding grid
   allow_next_grid();
@@ -304,170 +364,230 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       const int n = prefix[b + 1] - prefix[b];
       a.chunk_counts[p] = a.chunk_pages > 0 ? n : n > 0 ? pair_chunks(g, HS * prefix[b] + r * n, n) : 0;
     }
-    const int r = warp;
-    uint8_t* my_stages = stages + static_cast<size_t>(r) * kWarpStages * kTcStageBytes;
-    uint64_t* my_bars = &bars[kBarStage + kWarpStages * r];
+    const bool is_v = warp >= kHalfWarps;          // warps 0-7: K rows; 8-15: V^T columns
+    // tile slot of every group: a K warp writes its rows (TMEM lanes 16 r ..) in its own lane
+    // quadrant (warp % 4), so K warp w takes slot 2 (w % 4) + w / 4
+    const int r = is_v ? warp - kHalfWarps : 2 * (warp & 3) + (warp >> 2);
+    // the barrier that group Gg's operand is announced on: one per operand buffer, so that warps
+    // running two groups ahead of the MMA warp never move it two phases past that warp's test
+    auto full_bar = [&](int Gg) { return &bars[(is_v ? kBarVFull : kBarKFull) + (Gg & 1)]; };
+    // group G's operands (one of two K and one of two V buffers) are free once S^T, respectively
+    // O^T += V^T P^T, of group G - 2 is computed
+    auto wait_operand_free = [&](int Gg) -> bool {
+      return Gg < 2 || wait_or_abort(&bars[(is_v ? kBarPvDone : kBarKFree) + (Gg & 1)], ((Gg >> 1) - 1) & 1,
+                                     abort_flag, a.status);
+    };
+    // this warp's ring of copy stages: its tiles, across items, go to stages 0, 1, .., ns-1, 0, ..
+    const int ns = is_v ? kVStages : kKStages;
+    const int first_stage = is_v ? kHalfWarps * kKStages + (warp - kHalfWarps) * kVStages : warp * kKStages;
+    uint8_t* ring = stages + static_cast<size_t>(first_stage) * kHalfStageBytes;
+    uint64_t* ring_bars = &bars[kBarStage + first_stage];
     const uint64_t policy = l2_evict_first_policy();
-    uint32_t inflight = 0, phase = 0;
-    int sidx = 0, G = 0;
-    bool prefetched = false, aborted = false;
+    uint32_t armed = 0, phase = 0;                 // per stage: a copy is in flight / parity of its next wait
+    int n_issued = 0, n_used = 0;                  // this warp's tiles started / consumed
+    int iss_k = 0, iss_u = r;                      // the next tile to start: item iss_k, unit iss_u
+    bool iss_end = false, aborted = false;
+    // Start copies while stages are free, up to the item after the one being consumed (k_cur);
+    // an item not yet published is tested, not waited for.
+    auto pump = [&](int k_cur) {
+      while (!iss_end && n_issued - n_used < ns && iss_k <= k_cur + 1) {
+        if (iss_k > k_cur && !mbar_test(&bars[kBarItemFull + (iss_k & 1)], (iss_k >> 1) & 1)) break;
+        const ItemDesc& di = desc[iss_k & 1];
+        if (di.b < 0) {
+          iss_end = true;
+          break;
+        }
+        if (iss_u >= di.units) {
+          ++iss_k;
+          iss_u = r;
+          continue;
+        }
+        const int st = n_issued % ns;
+        if (issue_half(a, di, meta + (iss_k & 1) * kMaxItemTiles, iss_u, is_v, ring + st * kHalfStageBytes,
+                       &ring_bars[st], lane, policy) != kKindInvalid)
+          armed |= 1u << st;
+        ++n_issued;
+        iss_u += 8;
+      }
+    };
+    int G = 0;
+    const ItemDesc* dcur = nullptr;
+    const int* mcur = nullptr;
+    // the fourth block of a raw half tile into the start of its stage (the first three are used)
+    auto fetch_block3 = [&](int sidx, int u) -> bool {
+      __syncwarp();
+      fetch_raw_block3(a, *dcur, mcur, u, is_v, ring + sidx * kHalfStageBytes, &ring_bars[sidx], lane, policy);
+      if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) return false;
+      phase ^= 1u << sidx;
+      return true;
+    };
     for (int k = 0; !aborted; ++k) {
       const int buf = k & 1;
       if (!wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status)) break;
       const ItemDesc d = desc[buf];
       if (d.b < 0) break;
       const int* m = meta + buf * kMaxItemTiles;
+      dcur = &d;
+      mcur = m;
       const int ng = (d.units + 7) >> 3;
-      if (!prefetched && r < d.units &&
-          issue_tile<true>(a, d, m, r, my_stages + sidx * kTcStageBytes, &my_bars[sidx], lane, policy))
-        inflight |= 1u << sidx;
-      prefetched = false;
-      for (int gl = 0; gl < ng; ++gl) {
+      pump(k);
+      for (int gl = 0; gl < ng && !aborted; ++gl) {
         const int u = 8 * gl + r;
         const int Gg = G + gl;
         if (u < d.units) {
-          const int un = u + 8, ns = sidx ^ 1;
-          uint8_t* next_stage = my_stages + ns * kTcStageBytes;
-          if (un < d.units && issue_tile<true>(a, d, m, un, next_stage, &my_bars[ns], lane, policy))
-            inflight |= 1u << ns;
-          if (inflight & (1u << sidx)) {
-            if (!wait_or_abort(&my_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) { aborted = true; break; }
+          const int sidx = n_used % ns;
+          if (armed & (1u << sidx)) {
+            if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) { aborted = true; break; }
             phase ^= 1u << sidx;
-            inflight &= ~(1u << sidx);
+            armed &= ~(1u << sidx);
           }
           const int kind = m[u] & 3;
-          uint8_t* st = my_stages + sidx * kTcStageBytes;
-          if (Gg > 0 && !wait_or_abort(&bars[kBarKFree], (Gg - 1) & 1, abort_flag, a.status)) { aborted = true; break; }
-          if (kind != kKindInvalid) write_k_tile(st, kind == kKindComp, kop, r, lane);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarKFull]);
-          const uint8_t* vsrc = st + kTcVOffset;
-          if (kind == kKindRaw) {                 // a raw tile's V half goes where its K half was
-            issue_raw_v(a, d, m, u, st, &my_bars[sidx], lane, policy);
-            if (!wait_or_abort(&my_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) {
-              inflight |= 1u << sidx;            // still in flight: waited for at the end
+          uint8_t* st = ring + sidx * kHalfStageBytes;
+          if (!wait_operand_free(Gg)) { aborted = true; break; }
+          uint8_t* op = vop + (Gg & 1) * kOpBytes;
+          const uint32_t k_tmem = tmem + (static_cast<uint32_t>(16 * r) << 16) + kTmemK + (Gg & 1) * 64;
+          if (kind == kKindInvalid) {
+            if (is_v) zero_v_tile(op, r, lane);
+          } else {
+            uint32_t keep_a = 0xFFFFFFFFu, keep_b = 0xFFFFFFFFu;
+            if (is_v) {
+              const int ntok = min(16, d.t1 - (d.t0 + 16 * u));
+              const int ti = lane & 3;
+              if (ntok < 16) {
+                keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
+                keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
+              }
+            }
+            const bool ok_half = is_v ? rebuild_half<true>(st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
+                                          return fetch_block3(sidx, u);
+                                        })
+                                      : rebuild_half<false>(st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
+                                          return fetch_block3(sidx, u);
+                                        });
+            if (!ok_half) {
+              armed |= 1u << sidx;               // still in flight: waited for at the end
               aborted = true;
               break;
             }
-            phase ^= 1u << sidx;
-            vsrc = st;
           }
-          if (Gg > 0 && !wait_or_abort(&bars[kBarVFree], (Gg - 1) & 1, abort_flag, a.status)) { aborted = true; break; }
-          if (kind != kKindInvalid) write_v_tile(vsrc, kind == kKindComp, min(16, d.t1 - (d.t0 + 16 * u)), vop, r, lane);
-          else zero_v_tile(vop, r, lane);
-          fence_proxy_async_smem();
+          if (is_v) {
+            fence_proxy_async_smem();
+          } else {
+            tmem_wait_st();
+            tcgen05_before_sync();
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarVFull]);
-          sidx ^= 1;
-          if (un >= d.units) {
-            // this warp's first tile of the next item (waiting for it only now, after this tile's
-            // operands are written: its publication waits for an item whose last MMA needs them)
-            const int nb = buf ^ 1;
-            if (!wait_or_abort(&bars[kBarItemFull + nb], ((k + 1) >> 1) & 1, abort_flag, a.status)) {
-              aborted = true;
-              break;
-            }
-            if (desc[nb].b >= 0 && r < desc[nb].units) {
-              if (issue_tile<true>(a, desc[nb], meta + nb * kMaxItemTiles, r, my_stages + sidx * kTcStageBytes,
-                                   &my_bars[sidx], lane, policy))
-                inflight |= 1u << sidx;
-              prefetched = true;
-            }
-          }
+          if (lane == 0) mbar_arrive(full_bar(Gg));
+          ++n_used;
+          pump(k);
         } else {
           // no tile in this slot of the item's last group: V^T columns zero, K rows unused
-          if (Gg > 0 && !wait_or_abort(&bars[kBarKFree], (Gg - 1) & 1, abort_flag, a.status)) { aborted = true; break; }
-          if (lane == 0) mbar_arrive(&bars[kBarKFull]);
-          if (Gg > 0 && !wait_or_abort(&bars[kBarVFree], (Gg - 1) & 1, abort_flag, a.status)) { aborted = true; break; }
-          zero_v_tile(vop, r, lane);
+          if (!wait_operand_free(Gg)) { aborted = true; break; }
+          if (is_v) zero_v_tile(vop + (Gg & 1) * kOpBytes, r, lane);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarVFull]);
+          if (lane == 0) mbar_arrive(full_bar(Gg));
         }
       }
       if (aborted) break;
       G += ng;
+      // every tile of this item was consumed, so started: the start pointer leaves the item before
+      // its descriptor buffer is released (and reused for item k + 2)
+      if (iss_k == k) {
+        iss_k = k + 1;
+        iss_u = r;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarItemEmpty + buf]);
     }
-    // copies still in flight (only after a wait gave up) must land before the CTA exits
-    for (int s = 0; s < kWarpStages; ++s)
-      if (inflight & (1u << s)) mbar_wait(&my_bars[s], (phase >> s) & 1);
-  } else if (warp == kMmaWarp) {
+    // copies still in flight (only after a wait gave up, or started for an item never reached)
+    // must land before the CTA exits
+    for (int s2 = 0; s2 < ns; ++s2)
+      if ((armed & (1u << s2)) && !mbar_wait(&ring_bars[s2], (phase >> s2) & 1)) report(a.status, ZF_DEV_TIMEOUT);
+  } else if (warp == kQkWarp) {
     // ================================================================== MMA warp
+    // One lane issues both products, whichever is ready first (non-blocking tests), so that
+    // neither waits behind the other: S^T = K Q^T of group qk_G and O^T += V^T P^T of group pv_G
+    // (pv_G < qk_G).
     if (lane == 0) {
-      struct GroupRef {
-        int buf, item, G;
-        bool first, last;
+      struct Info {
+        int item;
+        bool first;
       };
-      int k = -1, gl = 0, ng = 0, Gnext = 0;
-      // The next group in order; a group that opens an item waits for the item's publication.
-      auto advance = [&](GroupRef& x) -> bool {
-        if (gl >= ng) {
+      Info info[8];                             // groups whose S^T is issued and O^T is not yet
+      int qk_G = 0, pv_G = 0, k = -1, gl = 0, ng = 0;
+      bool end_seen = false;
+      uint64_t t_last = global_timer_ns();
+      while (true) {
+        bool progress = false;
+        if (!end_seen && gl >= ng && mbar_test(&bars[kBarItemFull + ((k + 1) & 1)], ((k + 1) >> 1) & 1)) {
           ++k;
-          if (!wait_or_abort(&bars[kBarItemFull + (k & 1)], (k >> 1) & 1, abort_flag, a.status)) return false;
           const ItemDesc d = desc[k & 1];
-          if (d.b < 0) return false;
-          ng = (d.units + 7) >> 3;
-          gl = 0;
-        }
-        x.buf = k & 1;
-        x.item = k;
-        x.G = Gnext++;
-        x.first = gl == 0;
-        x.last = gl == ng - 1;
-        ++gl;
-        return true;
-      };
-      auto issue_qk = [&](const GroupRef& x) -> bool {
-        if (!wait_or_abort(&bars[kBarKFull], x.G & 1, abort_flag, a.status)) return false;
-        if (x.G >= 2 && !wait_or_abort(&bars[kBarSFree + (x.G & 1)], ((x.G >> 1) - 1) & 1, abort_flag, a.status))
-          return false;
-        if (x.first && !wait_or_abort(&bars[kBarQFull + x.buf], (x.item >> 1) & 1, abort_flag, a.status)) return false;
-        tcgen05_after_sync();
-        const uint32_t d_tmem = tmem + (x.G & 1) * kCols;
-        const uint8_t* qb = qop + x.buf * kCols * 256;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          umma_bf16(d_tmem, umma_desc_kmajor(kop + j * 256), umma_desc_kmajor(qb + j * 256), kIdesc, j > 0);
-        umma_commit(&bars[kBarSFull + (x.G & 1)]);
-        umma_commit(&bars[kBarKFree]);
-        return true;
-      };
-      auto issue_pv = [&](const GroupRef& x) -> bool {
-        if (!wait_or_abort(&bars[kBarPFull], x.G & 1, abort_flag, a.status)) return false;
-        if (!wait_or_abort(&bars[kBarVFull], x.G & 1, abort_flag, a.status)) return false;
-        if (x.first && x.item > 0 && !wait_or_abort(&bars[kBarOFree], (x.item - 1) & 1, abort_flag, a.status))
-          return false;
-        tcgen05_after_sync();
-        const uint32_t o_tmem = tmem + 2 * kCols;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          umma_bf16(o_tmem, umma_desc_kmajor(vop + j * 256), umma_desc_kmajor(pop + j * 256), kIdesc,
-                    !(x.first && j == 0));
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          umma_bf16(o_tmem, umma_desc_kmajor(vop + j * 256), umma_desc_kmajor(pop + kCols * 256 + j * 256), kIdesc, 1);
-        umma_commit(&bars[kBarVFree]);
-        return true;
-      };
-      GroupRef cur, nxt;
-      if (advance(cur) && issue_qk(cur)) {
-        while (true) {
-          if (cur.last) {
-            // close the item before waiting for the next one to be published
-            if (!issue_pv(cur) || !advance(nxt) || !issue_qk(nxt)) break;
+          if (d.b < 0) {
+            end_seen = true;
           } else {
-            advance(nxt);                      // same item: no wait
-            if (!issue_qk(nxt) || !issue_pv(cur)) break;
+            ng = (d.units + 7) >> 3;
+            gl = 0;
           }
-          cur = nxt;
+          progress = true;
+        }
+        if (!end_seen && gl < ng && qk_G - pv_G < 8) {
+          const int G = qk_G;
+          if (mbar_test(&bars[kBarKFull + (G & 1)], (G >> 1) & 1) &&
+              (G < 2 || mbar_test(&bars[kBarSFree + (G & 1)], ((G >> 1) - 1) & 1)) &&
+              (gl != 0 || mbar_test(&bars[kBarQFull + (k & 1)], (k >> 1) & 1))) {
+            tcgen05_after_sync();
+            const uint32_t d_tmem = tmem + (G & 1) * kCols;
+            const uint32_t k_tmem = tmem + kTmemK + (G & 1) * 64;
+            const uint8_t* qb = qop + (k & 1) * kCols * 256;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              umma_bf16_ta(d_tmem, k_tmem + 8 * j, umma_desc_kmajor(qb + j * 256), kIdesc, j > 0);
+            umma_commit(&bars[kBarSFull + (G & 1)]);
+            umma_commit(&bars[kBarKFree + (G & 1)]);
+            info[G & 7] = Info{k, gl == 0};
+            ++qk_G;
+            ++gl;
+            progress = true;
+          }
+        }
+        if (pv_G < qk_G) {
+          const int G = pv_G;
+          const Info x = info[G & 7];
+          if (mbar_test(&bars[kBarPFull + (G & 1)], (G >> 1) & 1) &&
+              mbar_test(&bars[kBarVFull + (G & 1)], (G >> 1) & 1) &&
+              (!x.first || x.item == 0 || mbar_test(&bars[kBarOFree], (x.item - 1) & 1))) {
+            tcgen05_after_sync();
+            const uint32_t o_tmem = tmem + 2 * kCols;
+            const uint8_t* vb = vop + (G & 1) * kOpBytes;
+            const uint8_t* pb = pop + (G & 1) * (2 * kCols * 256);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              umma_bf16(o_tmem, umma_desc_kmajor(vb + j * 256), umma_desc_kmajor(pb + j * 256), kIdesc,
+                        !(x.first && j == 0));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              umma_bf16(o_tmem, umma_desc_kmajor(vb + j * 256), umma_desc_kmajor(pb + kCols * 256 + j * 256), kIdesc,
+                        1);
+            umma_commit(&bars[kBarPvDone + (G & 1)]);
+            ++pv_G;
+            progress = true;
+          }
+        }
+        if (end_seen && pv_G == qk_G) break;
+        if (progress) {
+          t_last = global_timer_ns();
+        } else if (__nanosleep(64), *abort_flag) {       // idle: leave the issue slots to the other warps
+          break;
+        } else if (global_timer_ns() - t_last > kWaitTimeoutNs) {
+          *abort_flag = 1;
+          report(a.status, ZF_DEV_TIMEOUT);
+          break;
         }
       }
       // every MMA issued has completed before tensor memory is released
       umma_commit(&bars[kBarDrain]);
-      mbar_wait(&bars[kBarDrain], 0);
+      if (!mbar_wait(&bars[kBarDrain], 0)) report(a.status, ZF_DEV_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -489,10 +609,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       const int ng = (d.units + 7) >> 3;
       const int causal_lim = lens[d.b] - a.tokens;   // token t of a request sees positions <= causal_lim + t
       float mcol[NJ][2], lsum[NJ][2];
+      int lim[NJ][2];                             // last position a column sees (-1: padding column)
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
         mcol[j][0] = mcol[j][1] = kNoScore;
         lsum[j][0] = lsum[j][1] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = 8 * j + 2 * ti + e;
+          lim[j][e] = col < d.nh ? causal_lim + (d.h0 + col) % a.tokens : -1;
+        }
       }
       bool stop = false;
       for (int gl = 0; gl < ng; ++gl, ++G) {
@@ -507,9 +633,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         tcgen05_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarSFree + sb]);
-        // the P operand (and the output) are free once the previous group's PV completed
-        if (G > 0) ok = wait_or_abort(&bars[kBarVFree], (G - 1) & 1, abort_flag, a.status) && ok;
-        tcgen05_after_sync();
+        // this group's P buffer is free once the PV two groups back completed
+        if (G >= 2) ok = wait_or_abort(&bars[kBarPvDone + sb], ((G >> 1) - 1) & 1, abort_flag, a.status) && ok;
         // scores in the log2 domain; hidden: past the item, unresolved pages, padding columns,
         // positions past a new token's own
         float x[2][NJ][4];
@@ -519,17 +644,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
           for (int i2 = 0; i2 < 2; ++i2) {
             const int tok = 128 * gl + 32 * q + 16 * s + gi + 8 * i2;     // token offset within the item
             const int u = tok >> 4;
-            const int pos = d.t0 + tok;
-            const bool valid = u < d.units && (mt[u] & 3) != kKindInvalid && pos < d.t1;
+            const int pos = (u < d.units && (mt[u] & 3) != kKindInvalid && d.t0 + tok < d.t1) ? d.t0 + tok : INT_MAX;
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
+            for (int j = 0; j < NJ; ++j)
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int col = 8 * j + 2 * ti + e;
-                const bool vis = valid && col < d.nh && pos <= causal_lim + (d.h0 + col) % a.tokens;
-                x[s][j][2 * i2 + e] = vis ? __uint_as_float(sr[s][4 * j + 2 * i2 + e]) * a.scale_log2 : -CUDART_INF_F;
-              }
-            }
+              for (int e = 0; e < 2; ++e)
+                x[s][j][2 * i2 + e] =
+                    pos <= lim[j][e] ? __uint_as_float(sr[s][4 * j + 2 * i2 + e]) * a.scale_log2 : -CUDART_INF_F;
           }
         }
         bool grow = false;
@@ -541,12 +662,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             grow = grow || mx > mcol[j][e] + kRescaleThreshold;
           }
         if (wg_any(grow || !ok)) {
+          // the output holds this item's earlier groups: its rescale needs the previous PV done
+          if (gl > 0) ok = wait_or_abort(&bars[kBarPvDone + (sb ^ 1)], ((G - 1) >> 1) & 1, abort_flag, a.status) && ok;
           if (wg_any(!ok)) {
             stop = true;
             break;
           }
+          tcgen05_after_sync();
           // column maxima over the warpgroup's 128 tokens, then the new running max
-          float cm[NJ][2];
 #pragma unroll
           for (int j = 0; j < NJ; ++j)
 #pragma unroll
@@ -554,14 +677,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
               float v = fmaxf(fmaxf(x[0][j][e], x[0][j][2 + e]), fmaxf(x[1][j][e], x[1][j][2 + e]));
 #pragma unroll
               for (int dd = 4; dd < 32; dd <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, dd));
-              cm[j][e] = v;
+              if (gi == 0) red_max[q * kCols + 8 * j + 2 * ti + e] = v;
             }
-          if (gi == 0) {
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) red_max[q * kCols + 8 * j + 2 * ti + e] = cm[j][e];
-          }
           wg_sync();
 #pragma unroll
           for (int j = 0; j < NJ; ++j)
@@ -577,8 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             }
           wg_sync();
           if (gl > 0) {
-            // the output holds this item's earlier groups: rescale it in tensor memory (the
-            // previous group's PV has completed)
+            // rescale the output in tensor memory
 #pragma unroll
             for (int c0 = 0; c0 < kCols; c0 += 16) {
               uint32_t o[16];
@@ -592,7 +708,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
           }
         }
         // P = 2^(x - m): BF16 high part and BF16 remainder, transposed into P^T core matrices
-        // (n-block j, k-block 4q + 2s (+1 for tokens 8-15 of the 16))
+        // (n-block j, k-block 4q + 2s (+1 for tokens 8-15 of the 16)) of buffer G & 1
+        uint8_t* pb = pop + sb * (2 * kCols * 256);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
 #pragma unroll
@@ -604,7 +721,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
             const uint32_t r01 = pack_bf16x2(p0 - bf16lo_to_f32(h01), p1 - bf16hi_to_f32(h01));
             const uint32_t r23 = pack_bf16x2(p2 - bf16lo_to_f32(h23), p3 - bf16hi_to_f32(h23));
-            uint8_t* ph = pop + j * kCoreRow + (4 * q + 2 * s) * 128 + gi * 16 + ti * 4;
+            uint8_t* ph = pb + j * kCoreRow + (4 * q + 2 * s) * 128 + gi * 16 + ti * 4;
             *reinterpret_cast<uint32_t*>(ph) = transpose8x8(h01);
             *reinterpret_cast<uint32_t*>(ph + 128) = transpose8x8(h23);
             *reinterpret_cast<uint32_t*>(ph + kCols * 256) = transpose8x8(r01);
@@ -614,11 +731,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         fence_proxy_async_smem();
         tcgen05_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarPFull]);
+        if (lane == 0) mbar_arrive(&bars[kBarPFull + sb]);   // P written (and the output rescaled)
       }
       if (stop) break;
-      // ---- the item's output: O^T / column sums (the last group's PV has completed)
-      const bool ok = wait_or_abort(&bars[kBarVFree], (G - 1) & 1, abort_flag, a.status);
+      // ---- the item's output: O^T / column sums (once the last group's PV has completed)
+      const bool ok = wait_or_abort(&bars[kBarPvDone + ((G - 1) & 1)], ((G - 1) >> 1) & 1, abort_flag, a.status);
       tcgen05_after_sync();
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
@@ -670,7 +787,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   tcgen05_before_sync();
   __syncthreads();
   tcgen05_after_sync();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -680,7 +797,7 @@ bool attention_tc_fits(int32_t batch) {
 }
 
 Plan attention_tc_plan(int batch, int hq, int hkv, int page_size, int max_pages, int num_sms) {
-  return make_plan(batch, hq, hkv, page_size, max_pages, num_sms, kRebuildWarps, kTcMaxCols);
+  return make_plan(batch, hq, hkv, page_size, max_pages, num_sms, kHalfWarps, kTcMaxCols);
 }
 
 zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t tokens, cudaStream_t stream) {
@@ -692,12 +809,8 @@ zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t token
   a.chunk_pages = p.chunk_pages;
   a.prefetch = 0;
   a.plan_first = 0;
-  const int cols = a.group < kTcMaxCols ? a.group : kTcMaxCols;   // columns of the widest slice
-  const bool narrow = cols <= 16;
-  const size_t smem = narrow ? tc_layout<16>(a.batch).total : tc_layout<32>(a.batch).total;
-  const void* kernel = narrow ? reinterpret_cast<const void*>(attn_tc_kernel<16>)
-                              : reinterpret_cast<const void*>(attn_tc_kernel<32>);
-  zf_status st = ensure_smem_limit(kernel, narrow ? 0 : 1, smem);
+  const size_t smem = tc_layout<kTcMaxCols>(a.batch).total;
+  zf_status st = ensure_smem_limit(reinterpret_cast<const void*>(attn_tc_kernel<kTcMaxCols>), 0, smem);
   if (st != ZF_OK) return st;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -709,9 +822,7 @@ zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t token
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if ((narrow ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<16>, a) : cudaLaunchKernelEx(&cfg, attn_tc_kernel<32>, a)) !=
-      cudaSuccess)
-    return ZF_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, attn_tc_kernel<kTcMaxCols>, a) != cudaSuccess) return ZF_ERR_CUDA;
   MergeArgs m{};
   m.part_o = a.part_o;
   m.part_lse = a.part_lse;

@@ -270,7 +270,7 @@ zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t
 /* Kernels zf_decode_attn_multi_kernel can be asked for. */
 #define ZF_KERNEL_AUTO 0       /* what zf_decode_attn and zf_decode_attn_multi run (below) */
 #define ZF_KERNEL_WARP_MMA 1   /* warp-level MMA, 8 query columns per pass over a kv head's tiles */
-#define ZF_KERNEL_TCGEN05 2    /* 5th-generation tensor cores, up to 32 columns per pass */
+#define ZF_KERNEL_TCGEN05 2    /* 5th-generation tensor cores, 16 columns per pass */
 
 /*
  * zf_decode_attn_multi_kernel — zf_decode_attn_multi with the attention kernel chosen by `kernel`.
@@ -280,11 +280,13 @@ zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t
  *  - ZF_KERNEL_WARP_MMA rebuilds each block in registers straight into warp-MMA (m16n8k16)
  *    fragments: 8 columns per pass, so a kv head's K/V tiles are read once per 8 columns.
  *  - ZF_KERNEL_TCGEN05 rebuilds each 16-token tile into shared-memory operands of tcgen05.mma
- *    (M = 128 tokens or channels, N = 16 or 32 columns) whose scores and output accumulate in
- *    tensor memory: up to 32 columns per pass, so tiles are read once per 32 columns.  Its shared
- *    memory holds the request lengths: batch above about 3000 returns ZF_ERR_UNSUPPORTED.
- *  - ZF_KERNEL_AUTO (what zf_decode_attn / zf_decode_attn_multi do) takes ZF_KERNEL_TCGEN05 when
- *    a kv head has more than 8 columns and the batch fits, else ZF_KERNEL_WARP_MMA.
+ *    (M = 128 tokens or channels, N = 16 columns) whose scores and output accumulate in tensor
+ *    memory: 16 columns per pass, so tiles are read once per 16 columns.  Its shared memory also
+ *    holds the request lengths: batch above 490 returns ZF_ERR_UNSUPPORTED.
+ *  - ZF_KERNEL_AUTO (what zf_decode_attn / zf_decode_attn_multi do) runs ZF_KERNEL_WARP_MMA, the
+ *    faster of the two on GB300 on every shape measured so far, even where it reads the tiles
+ *    more often (the tensor-memory kernel's 16-column pass is paced by its warps' hand-offs, not
+ *    by HBM).
  *   Both give the same results within floating-point rounding (different summation order).
  *   Workspace: zf_decode_attn_multi_workspace_size covers every kernel.  Other arguments as for
  *   zf_decode_attn_multi.  Returns ZF_ERR_INVALID_ARGUMENT for an unknown `kernel`.

@@ -383,9 +383,9 @@ def test_multi_token_full_size_sampled(zf):
 
 def test_tcgen05_full_size_sampled_two_tokens(zf):
     """Two new tokens per request on the Qwen2-7B max-batch shape (GQA 7: 14 columns per kv head),
-    one layer in the benchmark's launch configuration: the tensor-memory kernel (what the call
-    picks) on sampled (request, token, head) outputs against float64 attention, and every output
-    against the warp-MMA kernel."""
+    one layer in the benchmark's launch configuration: the tensor-memory kernel on sampled
+    (request, token, head) outputs against float64 attention, and every output against the
+    warp-MMA kernel."""
     w = I.WORKLOADS["qwen2_7b_maxbatch"]
     T = 2
     layer = I.make_layer(w, layer=0, device="cuda")
@@ -395,7 +395,8 @@ def test_tcgen05_full_size_sampled_two_tokens(zf):
     q = I.make_multi_queries(w, T, device="cuda")
     ws = zf.new_workspace(zf.workspace_size_multi(w.batch, T, w.num_q_heads, w.num_kv_heads, w.page_size,
                                                   w.max_pages))
-    out, lse = zf.decode_attn_multi(gc, q, layer.page_table, layer.seq_lens, layer.scale, workspace=ws)
+    out, lse = zf.decode_attn_multi(gc, q, layer.page_table, layer.seq_lens, layer.scale, workspace=ws,
+                                    kernel="tcgen05")
     mo, ml = zf.decode_attn_multi(gc, q, layer.page_table, layer.seq_lens, layer.scale, workspace=ws,
                                   kernel="warp_mma")
     torch.cuda.synchronize()

@@ -276,6 +276,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
       plan_ok = __all_sync(0xFFFFFFFFu, ok) && !*lengths_changed;
     }
     int k = 0;
+    if (a.publish_delay_ns) sleep_for_ns(a.publish_delay_ns);    // tests: the consumers' waits run out
     auto publish = [&](const ItemDesc& piece) -> bool {
       const int buf = k & 1;
       bool good = true;
@@ -329,7 +330,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
   uint32_t phase = 0;           // bit s: parity of the next wait on stage s
   for (int k = 0;; ++k) {
     const int buf = k & 1;
-    if (!aborted && (*abort_flag || !mbar_wait(&item_full[buf], (k >> 1) & 1u))) {
+    if (!aborted && (*abort_flag || !mbar_wait(&item_full[buf], (k >> 1) & 1u, a.wait_limit_ns))) {
       aborted = true;
       *abort_flag = 1;
       report(a.status, ZF_DEV_TIMEOUT);
@@ -370,7 +371,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         inflight |= 1u << sidx;
     }
     prefetched = false;
-    if (!aborted && (*abort_flag || !mbar_wait(&q_full[buf], (k >> 1) & 1u))) {
+    if (!aborted && (*abort_flag || !mbar_wait(&q_full[buf], (k >> 1) & 1u, a.wait_limit_ns))) {
       aborted = true;
       *abort_flag = 1;
       report(a.status, ZF_DEV_TIMEOUT);
@@ -385,7 +386,7 @@ __global__ void __maxnreg__(112) attn_kernel(const AttnArgs a) {
         if (issue_tile<kCompressed>(a, d, m, un, next_stage, &my_bars[ns], lane, policy)) inflight |= 1u << ns;
       } else {
         const int nb = buf ^ 1;       // the next item (or the end marker) is published after this one
-        if (*abort_flag || !mbar_wait(&item_full[nb], ((k + 1) >> 1) & 1u)) {
+        if (*abort_flag || !mbar_wait(&item_full[nb], ((k + 1) >> 1) & 1u, a.wait_limit_ns)) {
           aborted = true;
           *abort_flag = 1;
           report(a.status, ZF_DEV_TIMEOUT);
@@ -743,7 +744,8 @@ template <bool kCompressed>
 static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t batch, int32_t tokens, int32_t hq_in,
                                   const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
                                   float scale, float* out, float* lse, void* workspace, size_t ws_bytes,
-                                  void* stream, int32_t kernel = ZF_KERNEL_AUTO) {
+                                  void* stream, int32_t kernel = ZF_KERNEL_AUTO,
+                                  uint64_t wait_limit_ns = kWaitTimeoutNs, uint64_t publish_delay_ns = 0) {
   if (kernel != ZF_KERNEL_AUTO && kernel != ZF_KERNEL_WARP_MMA && kernel != ZF_KERNEL_TCGEN05)
     return ZF_ERR_INVALID_ARGUMENT;
   zf_status st = check_cache(c, kCompressed, true, kCompressed);
@@ -802,6 +804,8 @@ static zf_status launch_attention(const zf_cache* c, const uint16_t* q, int32_t 
   a.comp_head_bytes = static_cast<int64_t>(c->page_size / 4) * kSlotBytes;
   a.raw_head_bytes = static_cast<int64_t>(c->page_size / 4) * kRawBlockBytes;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = wait_limit_ns;
+  a.publish_delay_ns = publish_delay_ns;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (tc > 0) return launch_attention_tc(a, p, tokens, s);
@@ -905,6 +909,19 @@ extern "C" zf_status zf_decode_attn_multi_kernel(const zf_cache* cache, const ui
                                                  size_t workspace_bytes, int32_t kernel, void* stream) {
   return launch_attention<true>(cache, q, batch, tokens, num_q_heads, page_table, max_pages_per_req, seq_lens,
                                 softmax_scale, out, lse, workspace, workspace_bytes, stream, kernel);
+}
+
+extern "C" zf_status zf_decode_attn_wait_test(const zf_cache* cache, const uint16_t* q, int32_t batch, int32_t tokens,
+                                              int32_t num_q_heads, const int32_t* page_table,
+                                              int32_t max_pages_per_req, const int32_t* seq_lens,
+                                              float softmax_scale, float* out, float* lse, void* workspace,
+                                              size_t workspace_bytes, int32_t kernel, uint64_t wait_limit_ns,
+                                              uint64_t publish_delay_ns, void* stream) {
+  if (wait_limit_ns < 1000 || wait_limit_ns > kWaitTimeoutNs || publish_delay_ns > kWaitTimeoutNs)
+    return ZF_ERR_INVALID_ARGUMENT;
+  return launch_attention<true>(cache, q, batch, tokens, num_q_heads, page_table, max_pages_per_req, seq_lens,
+                                softmax_scale, out, lse, workspace, workspace_bytes, stream, kernel, wait_limit_ns,
+                                publish_delay_ns);
 }
 
 extern "C" zf_status zf_dense_decode_attn(const zf_cache* cache, const uint16_t* q, int32_t batch,

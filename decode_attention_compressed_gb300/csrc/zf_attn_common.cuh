@@ -83,6 +83,8 @@ struct AttnArgs {
   int64_t comp_head_bytes;   // bytes of one (page, kv head) K record, compressed
   int64_t raw_head_bytes;    // bytes of one (page, kv head) K record, raw
   float scale_log2;          // softmax_scale * log2(e)
+  uint64_t wait_limit_ns;    // limit of the waits for the metadata warp's items (kWaitTimeoutNs; tests shorten it)
+  uint64_t publish_delay_ns; // the metadata warp's first item is published this much later (0; tests only)
 };
 
 struct Plan {

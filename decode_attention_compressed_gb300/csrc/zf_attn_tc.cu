@@ -107,9 +107,9 @@ __host__ __device__ inline TcLayout tc_layout(int batch) {
 
 // A bounded wait that also gives up at once when another warp already has (abort flag set).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* status) {
+                                              int32_t* status, uint64_t limit_ns = kWaitTimeoutNs) {
   if (*abort_flag) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, limit_ns)) return true;
   *abort_flag = 1;
   report(status, ZF_DEV_TIMEOUT);
   return false;
@@ -328,6 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   if (warp == kMetaWarp) {
     // ================================================================== metadata warp
     int k = 0;
+    if (a.publish_delay_ns) sleep_for_ns(a.publish_delay_ns);    // tests: the other warps' waits run out
     auto publish = [&](const ItemDesc& piece) -> bool {
       const int buf = k & 1;
       bool good = true;
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     };
     for (int k = 0; !aborted; ++k) {
       const int buf = k & 1;
-      if (!wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status)) break;
+      if (!wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
       const ItemDesc d = desc[buf];
       if (d.b < 0) break;
       const int* m = meta + buf * kMaxItemTiles;
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
           t_last = global_timer_ns();
         } else if (__nanosleep(64), *abort_flag) {       // idle: leave the issue slots to the other warps
           break;
-        } else if (global_timer_ns() - t_last > kWaitTimeoutNs) {
+        } else if (global_timer_ns() - t_last > a.wait_limit_ns) {
           *abort_flag = 1;
           report(a.status, ZF_DEV_TIMEOUT);
           break;
@@ -602,7 +603,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     int G = 0;
     for (int k = 0;; ++k) {
       const int buf = k & 1;
-      const bool ok_item = wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status);
+      const bool ok_item = wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status, a.wait_limit_ns);
       const ItemDesc d = desc[buf];
       if (wg_any(!ok_item || d.b < 0)) break;
       const int* mt = meta + buf * kMaxItemTiles;

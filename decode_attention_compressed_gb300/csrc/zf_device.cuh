@@ -75,14 +75,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete.  Bounded: returns false after
 // kWaitTimeoutNs (checked at every retry), so a broken pipeline never hangs the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return false;
+}
+
+// Sleep for about `ns` nanoseconds (bounded by the argument itself).
+__device__ __forceinline__ void sleep_for_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) __nanosleep(1000);
 }
 
 // Programmatic dependent launch: wait for the preceding grid's results / let the next grid start.

@@ -74,6 +74,10 @@ SIGNATURES = {
     "zf_decode_attn_multi_kernel": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
                                                _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
                                                _c_void_p, _c_size_t, _c_int32, _c_void_p]),
+    "zf_decode_attn_wait_test": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
+                                            _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
+                                            _c_void_p, _c_size_t, _c_int32, ctypes.c_uint64, ctypes.c_uint64,
+                                            _c_void_p]),
     "zf_dense_decode_attn_multi": (_c_int32, [ctypes.POINTER(ZfCacheDesc), _c_void_p, _c_int32, _c_int32, _c_int32,
                                               _c_void_p, _c_int32, _c_void_p, _c_float, _c_void_p, _c_void_p,
                                               _c_void_p, _c_size_t, _c_void_p]),
@@ -402,6 +406,30 @@ def decode_attn_multi(cache: Cache, q, page_table, seq_lens, scale=None, out=Non
         name = "zf_dense_decode_attn_multi" if dense else "zf_decode_attn_multi"
         status = getattr(lib(), name)(*args, _stream(stream))
     _check(name, status)
+    return out, lse
+
+
+def decode_attn_wait_test(cache: Cache, q, page_table, seq_lens, scale=None, kernel="warp_mma", wait_limit_ns=1000000,
+                          publish_delay_ns=0, stream=None):
+    """zf_decode_attn_wait_test (tests of the failure path): one new token per request, the
+    kernel's waits for its metadata warp's items limited to wait_limit_ns and that warp's first
+    item published publish_delay_ns late.  Returns (out, lse); with the delay above the limit
+    the outputs are not meaningful and the cache's status word gets DEV_TIMEOUT."""
+    q = _arg(q, "q", cache, _BITS16, (None, None, HEAD_DIM))
+    B, Hq, _ = q.shape
+    page_table, seq_lens = _attn_args(cache, q, page_table, seq_lens, B)
+    max_pages = int(page_table.shape[1])
+    scale = 1.0 / math.sqrt(HEAD_DIM) if scale is None else scale
+    dev = cache.device
+    out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    workspace = new_workspace(workspace_size(B, Hq, cache.num_kv_heads, cache.page_size, max_pages), dev)
+    d = cache.desc()
+    _check("zf_decode_attn_wait_test",
+           lib().zf_decode_attn_wait_test(ctypes.byref(d), _ptr(q), B, 1, Hq, _ptr(page_table), max_pages,
+                                          _ptr(seq_lens), scale, _ptr(out), _ptr(lse), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _kernel_code(kernel, False),
+                                          int(wait_limit_ns), int(publish_delay_ns), _stream(stream)))
     return out, lse
 
 

@@ -297,6 +297,23 @@ zf_status zf_decode_attn_multi_kernel(const zf_cache* cache, const uint16_t* q, 
                                       void* workspace, size_t workspace_bytes, int32_t kernel, void* stream);
 
 /*
+ * zf_decode_attn_wait_test — for tests of the failure path: zf_decode_attn_multi_kernel with the
+ * kernel's waits for its metadata warp's items limited to wait_limit_ns (1 us .. 2 s; the normal
+ * limit is 2 s) and that warp's first item published publish_delay_ns (<= 2 s) late.  With a delay
+ * above the limit the waits run out: the call then sets ZF_DEV_TIMEOUT in the cache's status
+ * word, the CTAs wind down (copies in flight land first, tensor memory is released), no output is
+ * guaranteed, and the context and the stream stay usable for the next call.  No fault, trap or
+ * endless wait is involved.  The paper has no counterpart; it exists so that tests can exercise the
+ * bounded waits.  ZF_ERR_INVALID_ARGUMENT for limits out of range; other arguments as for
+ * zf_decode_attn_multi_kernel.
+ */
+zf_status zf_decode_attn_wait_test(const zf_cache* cache, const uint16_t* q, int32_t batch, int32_t tokens,
+                                   int32_t num_q_heads, const int32_t* page_table, int32_t max_pages_per_req,
+                                   const int32_t* seq_lens, float softmax_scale, float* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, int32_t kernel, uint64_t wait_limit_ns,
+                                   uint64_t publish_delay_ns, void* stream);
+
+/*
  * zf_dense_decode_attn — the same decode attention over an uncompressed BF16 paged cache: page
  * id p of the page table is read from raw slot p of cache->k_raw / cache->v_raw (raw block
  * layout above; zf_encode_pages with ZF_ENCODE_FORCE_RAW and raw_slots = page_ids builds it).

@@ -218,9 +218,14 @@ def test_full_size_sampled(zf, name):
     out, lse = zf.decode_attn(gc, layer.q, layer.page_table, layer.seq_lens, layer.scale)
     torch.cuda.synchronize()
     assert gc.status_word() == 0
+    # every request's first and last query head (the ends of its pairs' page ranges), plus 64 random
+    # (request, head) rows: at least 64 rows, across the CTA ranges of the balanced split
     rng = np.random.default_rng(0)
-    pairs = sorted({(int(rng.integers(w.batch)), int(rng.integers(w.num_q_heads))) for _ in range(6)}
-                   | {(0, 0), (w.batch - 1, w.num_q_heads - 1)})
+    rows = w.batch * w.num_q_heads
+    picked = rng.choice(rows, size=min(64, rows), replace=False)
+    pairs = sorted({(int(i) // w.num_q_heads, int(i) % w.num_q_heads) for i in picked}
+                   | {(b, h) for b in range(w.batch) for h in (0, w.num_q_heads - 1)})
+    assert len(pairs) >= min(64, rows)
     ref_out, ref_lse = sampled_reference(layer, pairs)
     H.compare_attention(out, lse, ref_out, ref_lse, pairs=pairs)
     # properties at any size: finite, |out| bounded by max |v| of the request's head

@@ -48,7 +48,7 @@ def read_peaks():
 
 
 # the sources the attention kernels are compiled from
-KERNEL_SOURCES = ("zf_attn.cu", "zf_device.cuh", "zf_host.h")
+KERNEL_SOURCES = ("zf_attn.cu", "zf_attn_common.cuh", "zf_device.cuh", "zf_host.h")
 
 
 def kernel_source_hash() -> str:
@@ -760,7 +760,9 @@ def run_gpu(args, rank, world, local_rank):
                   "bound": "hbm",
                   "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                   "peak_source": peak_kind, "bytes_per_launch": int(per_launch), "call_us": round(call_ms * 1e3, 3),
-                  "traffic": read_traffic(w.name) if T == 1 else None},
+                  # the committed capture is of the warp-MMA kernel, single token, full batch
+                  "traffic": read_traffic(w.name) if T == 1 and args.kernel != "tcgen05"
+                  and args.batch is None else None},
         e2e={"value": round(e2e_ms * 1e3, 3) if e2e_ms else None, "unit": "us/step", "h2d_bytes_per_step": h2d,
              "d2h_bytes_per_step": d2h},
         gpu_launches=args.steps * L * 2 + (args.steps if wb.append is not None else 0),

@@ -712,14 +712,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
   if (lane == 0) a.lse[row] = (M + fast_log2(lsum)) * kLn2;
 }
 
-// Which kernel a compressed call runs.  ZF_KERNEL_AUTO runs the warp-MMA kernel: on GB300 it is
-// the faster one on every shape measured, also where it reads a kv head's tiles twice or four
-// times (GQA-7 with 2 or 4 new tokens: 502 against 616 us, 988 against 1209 us per call).
-// Returns whether it is the tensor-memory kernel, or -1 when that kernel cannot run these sizes.
+// Which kernel a compressed call runs.  ZF_KERNEL_AUTO runs the tensor-memory kernel when a kv head
+// has more than 16 query columns (query heads per kv head x new tokens), where the warp-MMA kernel
+// would read its tiles three times or more, and the warp-MMA kernel otherwise.  Measured on GB300
+// (one call, 8192-token contexts): GQA-7 with 4 new tokens 823 against 1043 us, GQA-4 with 8 new
+// tokens 731 against 1050 us; at up to 16 columns the warp-MMA kernel is the faster one (GQA-7
+// with 2 new tokens: 548 against 588 us).  Returns whether it is the tensor-memory kernel, or -1
+// when that kernel was asked for and cannot run these sizes.
 static int pick_tc(int32_t kernel, int batch, int hq, int hkv) {
-  (void)hq;
-  (void)hkv;
-  if (kernel == ZF_KERNEL_TCGEN05) return attention_tc_fits(batch) ? 1 : -1;
+  if (kernel == ZF_KERNEL_TCGEN05) return attention_tc_fits(batch, hq, hkv) ? 1 : -1;
+  if (kernel == ZF_KERNEL_AUTO && hq / hkv > 16 && attention_tc_fits(batch, hq, hkv)) return 1;
   return 0;
 }
 
@@ -733,7 +735,7 @@ static size_t plan_workspace(int batch, int hq, int hkv, int page_size, int max_
   size_t w = make_plan(batch, hq, hkv, page_size, max_pages, num_sms, Cfg<true>::kWarps).ws_bytes;
   const size_t d = make_plan(batch, hq, hkv, page_size, max_pages, num_sms, Cfg<false>::kWarps).ws_bytes;
   w = w > d ? w : d;
-  if (attention_tc_fits(batch)) {
+  if (attention_tc_fits(batch, hq, hkv)) {
     const size_t t = attention_tc_plan(batch, hq, hkv, page_size, max_pages, num_sms).ws_bytes;
     w = w > t ? w : t;
   }

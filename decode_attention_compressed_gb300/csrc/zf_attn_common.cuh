@@ -33,7 +33,6 @@ constexpr int kWarpStages = 2;
 constexpr int kTileCompBytes = 4 * kSlotBytes;      // 3136: one 16-token tile of K (or V), compressed
 constexpr int kTileRawBytes = 4 * kRawBlockBytes;   // 4096
 constexpr int kHeadsPerSlice = 8;                   // MMA n of the warp-MMA kernel
-constexpr int kTcMaxCols = 16;                      // MMA n of the tensor-memory kernel
 constexpr int kMaxItemTiles = 512;                  // 16-token tiles per work item (metadata buffer size)
 constexpr int kMaxItemPages = 256;                  // pages per work item (page-table loads per lane: /32)
 // q rows in shared memory: channel words permuted so that lane (gi, ti) finds the four B-fragment
@@ -75,7 +74,7 @@ struct AttnArgs {
   int32_t* chunk_counts;     // [batch][hkv * slices] partials per pair, for the merge kernel
   int32_t batch, hq, hkv, group, slices, page_size, num_pages, num_raw, max_pages, max_chunks;
   int32_t tokens;            // new tokens per request T: query head qh = head * T + token (hq, group count them)
-  int32_t hps;               // query heads (MMA columns) per head slice: kHeadsPerSlice, or kTcMaxCols
+  int32_t hps;               // query heads (MMA columns) per head slice: kHeadsPerSlice, or 16 / 32
   int32_t min_range_pages;   // lower bound of the pages per CTA range
   int32_t chunk_pages;       // > 0: fixed chunks of this many pages, items dealt round-robin
   int32_t prefetch;          // prefetch the first tiles into L2 while the preceding grid drains
@@ -494,6 +493,8 @@ static Plan make_plan(int batch, int hq, int hkv, int page_size, int max_pages, 
 }
 
 // Raise a kernel's dynamic shared-memory limit once per (device, kernel); the limit only grows.
+// `which` (0-3) names the kernel among those of the calling file: each file that includes this
+// header keeps its own records, so two kernels of one file must not share a number.
 static zf_status ensure_smem_limit(const void* kernel, int which, size_t bytes) {
   static std::mutex mu;
   static size_t done[64][4] = {};
@@ -539,7 +540,9 @@ zf_status launch_merge(const MergeArgs& m, bool multi, cudaStream_t stream);
 // The tensor-memory kernel (zf_attn_tc.cu) for calls whose kv heads have more than
 // kHeadsPerSlice query columns: whether its shared memory holds the lengths of `batch` requests,
 // its plan, and its launch (attention + merge) with `base` holding every other argument.
-bool attention_tc_fits(int32_t batch);
+// columns per pass of the tensor-memory kernel for hq / hkv query columns per kv head: 16 or 32
+int attention_tc_cols(int hq, int hkv);
+bool attention_tc_fits(int32_t batch, int hq, int hkv);
 Plan attention_tc_plan(int batch, int hq, int hkv, int page_size, int max_pages, int num_sms);
 zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t tokens, cudaStream_t stream);
 

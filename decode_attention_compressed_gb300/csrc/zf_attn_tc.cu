@@ -2,8 +2,8 @@
 // (GQA groups above 8, or several new tokens per request: columns = query heads per kv head x new
 // tokens), on the 5th-generation tensor cores: the rebuilt K and V tiles go to shared memory as
 // MMA operands and the scores and the output accumulate in tensor memory, so each kv head's tiles
-// are read from HBM once for up to 32 columns (the warp-MMA kernel takes 8 columns per pass and
-// reads the tiles once per 8).
+// are read from HBM once per 16 columns (the warp-MMA kernel takes 8 columns per pass and reads the
+// tiles once per 8).
 //
 // ZipFusion §III.C (Attention over the Compressed KV Cache): compressed blocks are copied
 // HBM -> shared memory as they are and the exact BF16 values are rebuilt from them with integer
@@ -13,21 +13,25 @@
 // One CTA per SM, 22 warps:
 //  * warps 0-7 rebuild K, warps 8-15 rebuild V: warp r (mod 8) takes tile slot r of every
 //    128-token group of an item (16 tokens of one kv head).  It copies its half of the tile HBM ->
-//    its two private stages with 1-D bulk copies (the next in flight while it works on this one)
-//    and rebuilds it into the K operand (A of S^T = K Q^T: 128 tokens x 128 channels) or the V
-//    operand (A of O^T = V^T P^T: 128 channels x 128 tokens), K-major core-matrix layout, straight
-//    from the m16n8k16 fragment registers the rebuild produces (one conflict-free 32-bit store per
-//    lane fills one 8 x 16-byte core matrix).  K and V warps wait only for the MMA that last read
-//    their own operand, so the keys of the next group are rebuilt while this group's softmax runs;
+//    its private stages with 1-D bulk copies (two stages per K warp, three per V warp: the next
+//    copies are in flight while it works on this one) and rebuilds it straight from the m16n8k16
+//    fragment registers the rebuild produces: K (A of S^T = K Q^T: 128 tokens x 128 channels) into
+//    one of two tensor-memory buffers with tcgen05.st, V^T (A of O^T = V^T P^T: 128 channels x 128
+//    tokens) into one of two shared-memory buffers in the K-major core-matrix layout (one
+//    conflict-free 32-bit store per lane fills one 8 x 16-byte core matrix).  K and V warps wait
+//    only for the MMA that last read their buffer, so the keys of the next group are rebuilt while
+//    this group's softmax runs;
 //  * warps 16-19 (softmax warpgroup; warp w reads TMEM lanes 32(w%4)..): S^T comes out of tensor
 //    memory in the m16n8 accumulator layout, the online softmax runs in the log2 domain with one
 //    running max per column shared by the warpgroup (raised only when a score exceeds it by more
-//    than 8, after a warpgroup vote; the output in tensor memory is then rescaled in place), P^T
-//    (BF16 high part + BF16 remainder) is transposed with movmatrix into the P operand, and the
-//    warpgroup's first thread issues O^T += V^T P^T (2 x 8 MMAs) into tensor memory; at the end of
-//    an item it divides O^T by the column sums and writes the output or the partial;
-//  * warp 20 (QK): allocates tensor memory; one lane issues S^T = K Q^T (8 x M128 N{16,32} K16)
-//    into one of two TMEM score buffers per group, completion signalled by tcgen05.commit;
+//    than 8, after a warpgroup vote; the output in tensor memory is then rescaled in place), and
+//    P^T (BF16 high part + BF16 remainder) is transposed with movmatrix into one of two P operand
+//    buffers; at the end of an item it divides O^T by the column sums and writes the output or
+//    the partial;
+//  * warp 20 (MMA): allocates tensor memory; one lane issues both products, whichever is ready
+//    first: S^T = K Q^T (8 x M128 N16 K16, A from tensor memory) into one of two TMEM score
+//    buffers, and O^T += V^T P^T (8 MMAs of N = 32: P's high part and its remainder side by side)
+//    into the TMEM output, each completion signalled by tcgen05.commit to an mbarrier;
 //  * warp 21 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
 //    item ahead: resolves the pages through the page table and the directory and stages the
 //    item's query rows as the B operand of S^T.
@@ -45,25 +49,31 @@ namespace {
 constexpr int kHalfWarps = 8;                     // warps per half: 8 rebuild K rows, 8 rebuild V^T columns
 constexpr int kRebuildWarps = 2 * kHalfWarps;
 constexpr int kSoftmaxWarp0 = 16;                 // warps 16..19: TMEM lane quadrants 0..3
-constexpr int kQkWarp = 20;
+constexpr int kMmaWarp = 20;
 constexpr int kMetaWarp = 21;
 constexpr int kTcWarps = 22;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kHalfStageBytes = kTileCompBytes;   // one compressed K (or V) half tile; a raw half: 3 + 1 blocks
 constexpr int kOpBytes = 128 * 128 * 2;           // one 128 x 128 BF16 operand
 constexpr int kCoreRow = 2048;                    // bytes between core-matrix rows along M/N (16 along K)
-// Tensor memory: two score buffers (kCols columns each) and the output at columns 0 .. 3 kCols,
-// and two K operands (128 tokens x 128 channels as BF16 pairs: 64 columns each) from column 128.
+// Tensor memory: two score buffers (kCols columns each) at columns 0 .. 2 kCols, the output
+// (2 kCols columns: high and low parts of P) at 2 kCols .. 4 kCols, and two K operands (128 tokens
+// x 128 channels as BF16 pairs: 64 columns each) from column 128.
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemK = 128;
 constexpr int kSoftmaxBarrier = 1;                // named barrier of the softmax warpgroup
 
 // Barriers (mbarrier index in the shared array).
-// Copy stages per rebuild warp: the V warps' copies are the ones the PV products wait for, so
-// they run three deep; the K warps' two.
-constexpr int kKStages = 2;
-constexpr int kVStages = 3;
-constexpr int kNumStages = kHalfWarps * (kKStages + kVStages);
+// Copy stages per rebuild warp (measured on GB300: the K warps' copies, which the first product
+// waits for, gain most from a third stage; at 32 columns the larger operands leave room for two
+// each).  kNumStages: the stage barriers allocated (the most any width uses).
+template <int kCols>
+struct TcStages {
+  static constexpr int kK = kCols == 16 ? 3 : 2;
+  static constexpr int kV = 2;
+  static constexpr int kTotal = kHalfWarps * (kK + kV);
+};
+constexpr int kNumStages = kHalfWarps * 5;
 
 enum : int {
   kBarStage = 0,                // one per copy stage of the rebuild warps (K warps first)
@@ -93,7 +103,7 @@ __host__ __device__ inline TcLayout tc_layout(int batch) {
   s.vop = at; at += 2 * kOpBytes;                 // two V operands (groups alternate)
   s.pop = at; at += 4 * kCols * 256;              // P^T, two buffers: high part, then low part (kCols x 128 BF16 each)
   s.qop = at; at += 2 * kCols * 256;              // Q of two items (kCols x 128 BF16 each)
-  s.stages = at; at += static_cast<size_t>(kNumStages) * kHalfStageBytes;
+  s.stages = at; at += static_cast<size_t>(TcStages<kCols>::kTotal) * kHalfStageBytes;
   s.meta = at; at += 2 * kMaxItemTiles * 4;
   s.desc = at; at += 2 * 64;
   s.bars = at; at += kNumBars * 8;
@@ -274,7 +284,13 @@ __device__ __forceinline__ void tmem_ld_scores(uint32_t taddr, uint32_t (&r)[kCo
 template <int kCols>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a) {
   constexpr int NJ = kCols / 8;                   // 8-column blocks
+  static_assert(4 * kCols <= static_cast<int>(kTmemK), "scores and output must end before the K operands");
+  static_assert((kCols & (kCols - 1)) == 0 && 2 * kCols <= 256, "the PV MMA takes N = 2 kCols");
   constexpr uint32_t kIdesc = umma_idesc_bf16(128, kCols);
+  // O^T += V^T P^T takes P's high part and its remainder as 2 kCols columns of one operand: the
+  // output holds V^T P_hi^T in its first kCols columns and V^T P_lo^T in the rest, summed at the
+  // end (an MMA's issue cost does not grow with N at these sizes, so this halves the PV issues)
+  constexpr uint32_t kIdescPv = umma_idesc_bf16(128, 2 * kCols);
   extern __shared__ __align__(1024) uint8_t smem[];
   const TcLayout L = tc_layout<kCols>(a.batch);
   uint8_t* vop = smem + L.vop;
@@ -314,7 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     *abort_flag = 0;
   }
   fence_mbar_init();
-  if (warp == kQkWarp) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   tcgen05_before_sync();
   wait_prior_grid();          // inputs may come from the preceding grid
   allow_next_grid();
@@ -379,8 +395,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
                                      abort_flag, a.status);
     };
     // this warp's ring of copy stages: its tiles, across items, go to stages 0, 1, .., ns-1, 0, ..
-    const int ns = is_v ? kVStages : kKStages;
-    const int first_stage = is_v ? kHalfWarps * kKStages + (warp - kHalfWarps) * kVStages : warp * kKStages;
+    constexpr int kKSt = TcStages<kCols>::kK, kVSt = TcStages<kCols>::kV;
+    static_assert(TcStages<kCols>::kTotal <= kNumStages, "stage barriers");
+    const int ns = is_v ? kVSt : kKSt;
+    const int first_stage = is_v ? kHalfWarps * kKSt + (warp - kHalfWarps) * kVSt : warp * kKSt;
     uint8_t* ring = stages + static_cast<size_t>(first_stage) * kHalfStageBytes;
     uint64_t* ring_bars = &bars[kBarStage + first_stage];
     const uint64_t policy = l2_evict_first_policy();
@@ -505,7 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     // must land before the CTA exits
     for (int s2 = 0; s2 < ns; ++s2)
       if ((armed & (1u << s2)) && !mbar_wait(&ring_bars[s2], (phase >> s2) & 1)) report(a.status, ZF_DEV_TIMEOUT);
-  } else if (warp == kQkWarp) {
+  } else if (warp == kMmaWarp) {
     // ================================================================== MMA warp
     // One lane issues both products, whichever is ready first (non-blocking tests), so that
     // neither waits behind the other: S^T = K Q^T of group qk_G and O^T += V^T P^T of group pv_G
@@ -564,12 +582,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             const uint8_t* pb = pop + (G & 1) * (2 * kCols * 256);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              umma_bf16(o_tmem, umma_desc_kmajor(vb + j * 256), umma_desc_kmajor(pb + j * 256), kIdesc,
+              umma_bf16(o_tmem, umma_desc_kmajor(vb + j * 256), umma_desc_kmajor(pb + j * 256), kIdescPv,
                         !(x.first && j == 0));
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              umma_bf16(o_tmem, umma_desc_kmajor(vb + j * 256), umma_desc_kmajor(pb + kCols * 256 + j * 256), kIdesc,
-                        1);
             umma_commit(&bars[kBarPvDone + (G & 1)]);
             ++pv_G;
             progress = true;
@@ -696,13 +710,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
           wg_sync();
           if (gl > 0) {
             // rescale the output in tensor memory
-#pragma unroll
-            for (int c0 = 0; c0 < kCols; c0 += 16) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < 2 * kCols; c0 += 16) {      // both halves of the output
               uint32_t o[16];
               tmem_ld_32x32b_x16(tmem + lane_base + 2 * kCols + c0, o);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha_s[c0 + i]);
+              for (int i = 0; i < 16; ++i)
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha_s[(c0 + i) & (kCols - 1)]);
               tmem_st_32x32b_x16(tmem + lane_base + 2 * kCols + c0, o);
             }
             tmem_wait_st();
@@ -752,19 +767,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         }
       if (wg_any(!ok)) break;                     // also makes red_sum and m_s visible
       const int ch = 32 * q + lane;               // this thread's output channel (TMEM lane)
-#pragma unroll
-      for (int c0 = 0; c0 < kCols; c0 += 16) {
-        uint32_t o[16];
-        tmem_ld_32x32b_x16(tmem + lane_base + 2 * kCols + c0, o);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kCols; c0 += 8) {
+        uint32_t o[8], olo[8];
+        tmem_ld_32x32b_x8(tmem + lane_base + 2 * kCols + c0, o);
+        tmem_ld_32x32b_x8(tmem + lane_base + 3 * kCols + c0, olo);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const int n = c0 + i;
           if (n < d.nh) {
             const float lsum_n = red_sum[n] + red_sum[kCols + n] + red_sum[2 * kCols + n] + red_sum[3 * kCols + n];
             const float inv = lsum_n > 0.f ? 1.f / lsum_n : 0.f;
             const float lse2 = lsum_n > 0.f ? m_s[n] + log2f(lsum_n) : -CUDART_INF_F;
-            const float val = __uint_as_float(o[i]) * inv;
+            const float val = (__uint_as_float(o[i]) + __uint_as_float(olo[i])) * inv;
             if (d.single) {
               const size_t row = query_row(d.b, d.h0 + n, a.tokens, a.hq);
               a.out[row * ZF_HEAD_DIM + ch] = val;
@@ -788,30 +804,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   tcgen05_before_sync();
   __syncthreads();
   tcgen05_after_sync();
-  if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
-bool attention_tc_fits(int32_t batch) {
-  return tc_layout<kTcMaxCols>(batch).total <= 227 * 1024;
+int attention_tc_cols(int hq, int hkv) { return hq / hkv > 16 ? 32 : 16; }
+
+bool attention_tc_fits(int32_t batch, int hq, int hkv) {
+  const size_t bytes = attention_tc_cols(hq, hkv) == 32 ? tc_layout<32>(batch).total : tc_layout<16>(batch).total;
+  return bytes <= 227 * 1024;
 }
 
 Plan attention_tc_plan(int batch, int hq, int hkv, int page_size, int max_pages, int num_sms) {
-  return make_plan(batch, hq, hkv, page_size, max_pages, num_sms, kHalfWarps, kTcMaxCols);
+  return make_plan(batch, hq, hkv, page_size, max_pages, num_sms, kHalfWarps, attention_tc_cols(hq, hkv));
 }
 
-zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t tokens, cudaStream_t stream) {
+template <int kCols>
+static zf_status launch_tc(const AttnArgs& base, const Plan& p, int32_t tokens, cudaStream_t stream) {
   AttnArgs a = base;
-  a.hps = kTcMaxCols;
+  a.hps = kCols;
   a.slices = p.slices;
   a.max_chunks = p.max_chunks;
   a.min_range_pages = p.min_range_pages;
   a.chunk_pages = p.chunk_pages;
   a.prefetch = 0;
   a.plan_first = 0;
-  const size_t smem = tc_layout<kTcMaxCols>(a.batch).total;
-  zf_status st = ensure_smem_limit(reinterpret_cast<const void*>(attn_tc_kernel<kTcMaxCols>), 0, smem);
+  const size_t smem = tc_layout<kCols>(a.batch).total;
+  // one record per instantiation (16 columns: 0, 32 columns: 1)
+  zf_status st = ensure_smem_limit(reinterpret_cast<const void*>(attn_tc_kernel<kCols>), kCols / 32, smem);
   if (st != ZF_OK) return st;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -823,7 +844,7 @@ zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t token
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_tc_kernel<kTcMaxCols>, a) != cudaSuccess) return ZF_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, attn_tc_kernel<kCols>, a) != cudaSuccess) return ZF_ERR_CUDA;
   MergeArgs m{};
   m.part_o = a.part_o;
   m.part_lse = a.part_lse;
@@ -836,8 +857,13 @@ zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t token
   m.slices = a.slices;
   m.max_chunks = a.max_chunks;
   m.tokens = tokens;
-  m.hps = kTcMaxCols;
+  m.hps = kCols;
   return launch_merge(m, tokens > 1, stream);
+}
+
+zf_status launch_attention_tc(const AttnArgs& base, const Plan& p, int32_t tokens, cudaStream_t stream) {
+  return attention_tc_cols(base.hq, base.hkv) == 32 ? launch_tc<32>(base, p, tokens, stream)
+                                                   : launch_tc<16>(base, p, tokens, stream);
 }
 
 }  // namespace zf

@@ -270,7 +270,7 @@ zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t
 /* Kernels zf_decode_attn_multi_kernel can be asked for. */
 #define ZF_KERNEL_AUTO 0       /* what zf_decode_attn and zf_decode_attn_multi run (below) */
 #define ZF_KERNEL_WARP_MMA 1   /* warp-level MMA, 8 query columns per pass over a kv head's tiles */
-#define ZF_KERNEL_TCGEN05 2    /* 5th-generation tensor cores, 16 columns per pass */
+#define ZF_KERNEL_TCGEN05 2    /* 5th-generation tensor cores, 16 or 32 columns per pass */
 
 /*
  * zf_decode_attn_multi_kernel — zf_decode_attn_multi with the attention kernel chosen by `kernel`.
@@ -279,14 +279,16 @@ zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t
  * ((num_q_heads / num_kv_heads) x T).
  *  - ZF_KERNEL_WARP_MMA rebuilds each block in registers straight into warp-MMA (m16n8k16)
  *    fragments: 8 columns per pass, so a kv head's K/V tiles are read once per 8 columns.
- *  - ZF_KERNEL_TCGEN05 rebuilds each 16-token tile into shared-memory operands of tcgen05.mma
- *    (M = 128 tokens or channels, N = 16 columns) whose scores and output accumulate in tensor
- *    memory: 16 columns per pass, so tiles are read once per 16 columns.  Its shared memory also
- *    holds the request lengths: batch above 490 returns ZF_ERR_UNSUPPORTED.
- *  - ZF_KERNEL_AUTO (what zf_decode_attn / zf_decode_attn_multi do) runs ZF_KERNEL_WARP_MMA, the
- *    faster of the two on GB300 on every shape measured so far, even where it reads the tiles
- *    more often (the tensor-memory kernel's 16-column pass is paced by its warps' hand-offs, not
- *    by HBM).
+ *  - ZF_KERNEL_TCGEN05 rebuilds each 16-token tile into operands of tcgen05.mma (K in tensor
+ *    memory, V^T in shared memory; M = 128 tokens or channels) whose scores and output accumulate
+ *    in tensor memory: N = 16 columns per pass when a kv head has at most 16 columns, else 32,
+ *    so a kv head's tiles are read once per 16 or 32 columns.  Its shared memory also holds the
+ *    request lengths: batch above 1439 (16 columns) or 1423 (32 columns) returns
+ *    ZF_ERR_UNSUPPORTED.
+ *  - ZF_KERNEL_AUTO (what zf_decode_attn / zf_decode_attn_multi do) runs ZF_KERNEL_TCGEN05 when
+ *    a kv head has more than 16 columns (where the warp-MMA kernel would read its tiles three
+ *    times or more) and the batch fits it, else ZF_KERNEL_WARP_MMA (the faster one on GB300 at up
+ *    to 16 columns).
  *   Both give the same results within floating-point rounding (different summation order).
  *   Workspace: zf_decode_attn_multi_workspace_size covers every kernel.  Other arguments as for
  *   zf_decode_attn_multi.  Returns ZF_ERR_INVALID_ARGUMENT for an unknown `kernel`.

@@ -386,13 +386,29 @@ def test_multi_token_full_size_sampled(zf):
     H.compare_attention(out, lse, ref_out, ref_lse, pairs=picks)
 
 
-def test_tcgen05_full_size_sampled_two_tokens(zf):
-    """Two new tokens per request on the Qwen2-7B max-batch shape (GQA 7: 14 columns per kv head),
-    one layer in the benchmark's launch configuration: the tensor-memory kernel on sampled
-    (request, token, head) outputs against float64 attention, and every output against the
-    warp-MMA kernel."""
+@pytest.mark.parametrize("name, kernel", [("gqa16_t2", "tcgen05"), ("gqa20_t2_two_slices", "tcgen05"),
+                                          ("gqa7_t2_spikes", "warp_mma"), ("mha_t16_page64", "warp_mma")])
+def test_auto_kernel_choice(zf, name, kernel):
+    """ZF_KERNEL_AUTO runs the tensor-memory kernel above 16 columns per kv head and the warp-MMA
+    kernel up to 16: its results are bit for bit those of the kernel it picks."""
+    w, lens, T = MULTI_CASES[name]
+    layer = I.make_layer(w, seq_lens=lens)
+    gc = H.gpu_cache_from(layer, zf)
+    q = I.make_multi_queries(w, T).cuda()
+    table, sl = layer.page_table.cuda(), layer.seq_lens.cuda()
+    auto = zf.decode_attn_multi(gc, q, table, sl, layer.scale)
+    picked = zf.decode_attn_multi(gc, q, table, sl, layer.scale, kernel=kernel)
+    torch.cuda.synchronize()
+    assert torch.equal(auto[0], picked[0]) and torch.equal(auto[1], picked[1])
+
+
+@pytest.mark.parametrize("T", [2, 4])
+def test_tcgen05_full_size_sampled(zf, T):
+    """Two or four new tokens per request on the Qwen2-7B max-batch shape (GQA 7: 14 or 28
+    columns per kv head, one 16- or 32-column pass), one layer in the benchmark's launch
+    configuration: the tensor-memory kernel on sampled (request, token, head) outputs against
+    float64 attention, and every output against the warp-MMA kernel."""
     w = I.WORKLOADS["qwen2_7b_maxbatch"]
-    T = 2
     layer = I.make_layer(w, layer=0, device="cuda")
     npg = layer.num_pages
     gc = zf.Cache(npg, w.num_kv_heads, w.page_size, npg)

@@ -624,6 +624,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       const int ng = (d.units + 7) >> 3;
       const int causal_lim = lens[d.b] - a.tokens;   // token t of a request sees positions <= causal_lim + t
       float mcol[NJ][2], lsum[NJ][2];
+      float cap[NJ][2];                           // +inf: a column of the slice, -inf: padding
       int lim[NJ][2];                             // last position a column sees (-1: padding column)
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
@@ -632,9 +633,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int col = 8 * j + 2 * ti + e;
+          cap[j][e] = col < d.nh ? CUDART_INF_F : -CUDART_INF_F;
           lim[j][e] = col < d.nh ? causal_lim + (d.h0 + col) % a.tokens : -1;
         }
       }
+      // the last position every column of the slice sees: columns h0 .. h0 + nh - 1 are tokens
+      // (h0 + c) mod T, the earliest of which is 0 unless they stay within one token cycle
+      const int r0 = d.h0 % a.tokens;
+      const int lim_all = causal_lim + (r0 + d.nh > a.tokens ? 0 : r0);
       bool stop = false;
       for (int gl = 0; gl < ng; ++gl, ++G) {
         const int sb = G & 1;
@@ -652,20 +658,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         if (G >= 2) ok = wait_or_abort(&bars[kBarPvDone + sb], ((G >> 1) - 1) & 1, abort_flag, a.status) && ok;
         // scores in the log2 domain; hidden: past the item, unresolved pages, padding columns,
         // positions past a new token's own
+        // This thread's rows are tokens tok0 + {0, 8} of tile u0 and tok0 + {16, 24} of tile u0 + 1.
+        // Fast path (32 columns, where the softmax paces the kernel; at 16 it measured slower):
+        // both tiles resolved, and every row inside the item and seen by every column.
         float x[2][NJ][4];
+        const int tok0 = 128 * gl + 32 * q + gi;
+        const int u0 = tok0 >> 4;
+        const bool all_seen = kCols == 32 && u0 + 1 < d.units && (mt[u0] & 3) != kKindInvalid && (mt[u0 + 1] & 3) != kKindInvalid &&
+                              d.t0 + tok0 + 24 < d.t1 && d.t0 + tok0 + 24 <= lim_all;
+        if (all_seen) {
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-#pragma unroll
-          for (int i2 = 0; i2 < 2; ++i2) {
-            const int tok = 128 * gl + 32 * q + 16 * s + gi + 8 * i2;     // token offset within the item
-            const int u = tok >> 4;
-            const int pos = (u < d.units && (mt[u] & 3) != kKindInvalid && d.t0 + tok < d.t1) ? d.t0 + tok : INT_MAX;
+          for (int s = 0; s < 2; ++s)
 #pragma unroll
             for (int j = 0; j < NJ; ++j)
 #pragma unroll
-              for (int e = 0; e < 2; ++e)
-                x[s][j][2 * i2 + e] =
-                    pos <= lim[j][e] ? __uint_as_float(sr[s][4 * j + 2 * i2 + e]) * a.scale_log2 : -CUDART_INF_F;
+              for (int i = 0; i < 4; ++i)
+                x[s][j][i] = fminf(__uint_as_float(sr[s][4 * j + i]) * a.scale_log2, cap[j][i & 1]);
+        } else {
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+#pragma unroll
+            for (int i2 = 0; i2 < 2; ++i2) {
+              const int tok = tok0 + 16 * s + 8 * i2;     // token offset within the item
+              const int u = tok >> 4;
+              const int pos = (u < d.units && (mt[u] & 3) != kKindInvalid && d.t0 + tok < d.t1) ? d.t0 + tok : INT_MAX;
+#pragma unroll
+              for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  x[s][j][2 * i2 + e] =
+                      pos <= lim[j][e] ? __uint_as_float(sr[s][4 * j + 2 * i2 + e]) * a.scale_log2 : -CUDART_INF_F;
+            }
           }
         }
         bool grow = false;

@@ -10,7 +10,7 @@
 // operations right before the tensor-core instructions; raw blocks need no rebuild.  §IV.B: split
 // chunks are combined by a split-result merge.
 //
-// One CTA per SM, 22 warps:
+// One CTA per SM, 26 warps:
 //  * warps 0-7 rebuild K, warps 8-15 rebuild V: warp r (mod 8) takes tile slot r of every
 //    128-token group of an item (16 tokens of one kv head).  It copies its half of the tile HBM ->
 //    its private stages with 1-D bulk copies (two stages per K warp, three per V warp: the next
@@ -21,22 +21,23 @@
 //    conflict-free 32-bit store per lane fills one 8 x 16-byte core matrix).  K and V warps wait
 //    only for the MMA that last read their buffer, so the keys of the next group are rebuilt while
 //    this group's softmax runs;
-//  * warps 16-19 (softmax warpgroup; warp w reads TMEM lanes 32(w%4)..): S^T comes out of tensor
-//    memory in the m16n8 accumulator layout, the online softmax runs in the log2 domain with one
-//    running max per column shared by the warpgroup (raised only when a score exceeds it by more
-//    than 8, after a warpgroup vote; the output in tensor memory is then rescaled in place), and
-//    P^T (BF16 high part + BF16 remainder) is transposed with movmatrix into one of two P operand
-//    buffers; at the end of an item it divides O^T by the column sums and writes the output or
-//    the partial;
-//  * warp 20 (MMA): allocates tensor memory; one lane issues both products, whichever is ready
+//  * warps 16-23 (two softmax warpgroups, each owning half of the columns; warp w reads TMEM
+//    lanes 32(w%4)..): S^T comes out of tensor memory in the m16n8 accumulator layout, the online
+//    softmax runs in the log2 domain with one running max per column shared by the warpgroup
+//    (raised only when a score exceeds it by more than 8, after a warpgroup vote; the warpgroup's
+//    output columns in tensor memory are then rescaled in place), and P^T (BF16 high part + BF16
+//    remainder) is transposed with movmatrix into one of two P operand buffers; at the end of an
+//    item each warpgroup divides its O^T columns by their sums and writes the output or the
+//    partial;
+//  * warp 24 (MMA): allocates tensor memory; one lane issues both products, whichever is ready
 //    first: S^T = K Q^T (8 x M128 N16 K16, A from tensor memory) into one of two TMEM score
 //    buffers, and O^T += V^T P^T (8 MMAs of N = 32: P's high part and its remainder side by side)
 //    into the TMEM output, each completion signalled by tcgen05.commit to an mbarrier;
-//  * warp 21 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
+//  * warp 25 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
 //    item ahead: resolves the pages through the page table and the directory and stages the
 //    item's query rows as the B operand of S^T.
 // Every wait is bounded (2 s); a wait that gives up sets ZF_DEV_TIMEOUT and the CTA winds down
-// (the softmax warpgroup decides together, so its named barriers are always met).
+// (each softmax warpgroup decides together, so its named barriers are always met).
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -48,10 +49,11 @@ namespace {
 
 constexpr int kHalfWarps = 8;                     // warps per half: 8 rebuild K rows, 8 rebuild V^T columns
 constexpr int kRebuildWarps = 2 * kHalfWarps;
-constexpr int kSoftmaxWarp0 = 16;                 // warps 16..19: TMEM lane quadrants 0..3
-constexpr int kMmaWarp = 20;
-constexpr int kMetaWarp = 21;
-constexpr int kTcWarps = 22;
+constexpr int kSoftmaxWarp0 = 16;                 // warps 16..23: warpgroup (w - 16) / 4, TMEM lane quadrant w % 4
+constexpr int kSoftmaxWarps = 8;                  // two warpgroups, each owns half of the columns
+constexpr int kMmaWarp = kSoftmaxWarp0 + kSoftmaxWarps;
+constexpr int kMetaWarp = kMmaWarp + 1;
+constexpr int kTcWarps = kMetaWarp + 1;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kHalfStageBytes = kTileCompBytes;   // one compressed K (or V) half tile; a raw half: 3 + 1 blocks
 constexpr int kOpBytes = 128 * 128 * 2;           // one 128 x 128 BF16 operand
@@ -61,7 +63,7 @@ constexpr int kCoreRow = 2048;                    // bytes between core-matrix r
 // x 128 channels as BF16 pairs: 64 columns each) from column 128.
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemK = 128;
-constexpr int kSoftmaxBarrier = 1;                // named barrier of the softmax warpgroup
+constexpr int kSoftmaxBarrier = 1;                // named barriers of the softmax warpgroups: 1 and 2
 
 // Barriers (mbarrier index in the shared array).
 // Copy stages per rebuild warp (measured on GB300: the K warps' copies, which the first product
@@ -84,10 +86,10 @@ enum : int {
   kBarVFull = kBarKFull + 2,          // [2] the 8 V warps wrote a group's V operand (per V buffer)
   kBarKFree = kBarVFull + 2,          // [2] S^T = K Q^T of a group completed, per K buffer (commit)
   kBarSFull = kBarKFree + 2,          // [2] scores of a group in TMEM buffer (commit)
-  kBarSFree = kBarSFull + 2,          // [2] the softmax warpgroup read that score buffer
-  kBarPFull = kBarSFree + 2,          // [2] the softmax warpgroup wrote a group's P operand (per P buffer)
+  kBarSFree = kBarSFull + 2,          // [2] the softmax warpgroups read that score buffer
+  kBarPFull = kBarSFree + 2,          // [2] the softmax warpgroups wrote a group's P operand (per P buffer)
   kBarPvDone = kBarPFull + 2,         // [2] O^T += V^T P^T of a group completed, per V / P buffer (commit)
-  kBarOFree = kBarPvDone + 2,         // the softmax warpgroup read an item's output from tensor memory
+  kBarOFree = kBarPvDone + 2,         // the softmax warpgroups read an item's output from tensor memory
   kBarDrain = kBarOFree + 1,          // end of the CTA: every MMA issued has completed
   kNumBars = kBarDrain + 1,
 };
@@ -125,9 +127,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-// The softmax warpgroup's barrier, and the same barrier ORing a predicate over its 128 threads.
-__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kSoftmaxBarrier) : "memory"); }
-__device__ __forceinline__ bool wg_any(bool v) {
+// A softmax warpgroup's barrier (id), and the same barrier ORing a predicate over its 128 threads.
+__device__ __forceinline__ void wg_sync(uint32_t id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ bool wg_any(uint32_t id, bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
@@ -135,9 +137,22 @@ __device__ __forceinline__ bool wg_any(bool v) {
       "bar.red.or.pred q, %2, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "n"(kSoftmaxBarrier)
+      : "r"(static_cast<uint32_t>(v)), "r"(id)
       : "memory");
   return r != 0;
+}
+
+// Tensor-memory accesses of the softmax warpgroups beyond the shared set: 8 score columns
+// (16x256b.x1), and 8 output columns per lane (32x32b.x8).
+__device__ __forceinline__ void tmem_ld_16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 
 // Start the copy of the K (is_v false) or V half of tile u of an item into `stage`: a compressed
@@ -275,15 +290,15 @@ __device__ __forceinline__ void stage_q(const AttnArgs& a, const ItemDesc& d, ui
   }
 }
 
-template <int kCols>
-__device__ __forceinline__ void tmem_ld_scores(uint32_t taddr, uint32_t (&r)[kCols / 2]) {
-  if constexpr (kCols == 16) tmem_ld_16x256b_x2(taddr, r);
+template <int kN>
+__device__ __forceinline__ void tmem_ld_scores(uint32_t taddr, uint32_t (&r)[kN / 2]) {
+  if constexpr (kN == 8) tmem_ld_16x256b_x1(taddr, r);
+  else if constexpr (kN == 16) tmem_ld_16x256b_x2(taddr, r);
   else tmem_ld_16x256b_x4(taddr, r);
 }
 
 template <int kCols>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a) {
-  constexpr int NJ = kCols / 8;                   // 8-column blocks
   static_assert(4 * kCols <= static_cast<int>(kTmemK), "scores and output must end before the K operands");
   static_assert((kCols & (kCols - 1)) == 0 && 2 * kCols <= 256, "the PV MMA takes N = 2 kCols");
   constexpr uint32_t kIdesc = umma_idesc_bf16(128, kCols);
@@ -311,10 +326,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     for (int i = 0; i < kNumStages; ++i) mbar_init(&bars[kBarStage + i], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[kBarItemFull + b], 1);
-      mbar_init(&bars[kBarItemEmpty + b], kRebuildWarps + 4);
+      mbar_init(&bars[kBarItemEmpty + b], kRebuildWarps + kSoftmaxWarps);
       mbar_init(&bars[kBarQFull + b], 1);
       mbar_init(&bars[kBarSFull + b], 1);
-      mbar_init(&bars[kBarSFree + b], 4);
+      mbar_init(&bars[kBarSFree + b], kSoftmaxWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[kBarKFull + b], kHalfWarps);
@@ -322,10 +337,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       mbar_init(&bars[kBarKFree + b], 1);
     }
     mbar_init(&bars[kBarDrain], 1);
-    mbar_init(&bars[kBarOFree], 4);
+    mbar_init(&bars[kBarOFree], kSoftmaxWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[kBarPvDone + b], 1);
-      mbar_init(&bars[kBarPFull + b], 4);
+      mbar_init(&bars[kBarPFull + b], kSoftmaxWarps);
     }
     *abort_flag = 0;
   }
@@ -606,8 +621,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     }
     __syncwarp();
   } else {
-    // ================================================================== softmax warpgroup
-    const int q = warp - kSoftmaxWarp0;           // TMEM lane quadrant (warp % 4)
+    // ================================================================== softmax warpgroups
+    // Warpgroup hf owns columns hf * kHalf .. + kHalf: their running maxima, sums, P^T columns and
+    // output columns (high and low halves), so the two warpgroups never wait for each other.
+    constexpr int kHalf = kCols / 2;
+    constexpr int NJh = kHalf / 8;                // 8-column blocks of a warpgroup
+    const int q = (warp - kSoftmaxWarp0) & 3;     // TMEM lane quadrant (warp % 4)
+    const int hf = (warp - kSoftmaxWarp0) >> 2;
+    const int c0h = hf * kHalf;                   // first column of this warpgroup
+    const uint32_t nb = kSoftmaxBarrier + hf;     // its named barrier
     const int gi = lane >> 2, ti = lane & 3;
     float* red_max = red;                         // [4][kCols]
     float* red_sum = red + 4 * kCols;             // [4][kCols]
@@ -619,20 +641,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       const int buf = k & 1;
       const bool ok_item = wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status, a.wait_limit_ns);
       const ItemDesc d = desc[buf];
-      if (wg_any(!ok_item || d.b < 0)) break;
+      if (wg_any(nb, !ok_item || d.b < 0)) break;
       const int* mt = meta + buf * kMaxItemTiles;
       const int ng = (d.units + 7) >> 3;
       const int causal_lim = lens[d.b] - a.tokens;   // token t of a request sees positions <= causal_lim + t
-      float mcol[NJ][2], lsum[NJ][2];
-      float cap[NJ][2];                           // +inf: a column of the slice, -inf: padding
-      int lim[NJ][2];                             // last position a column sees (-1: padding column)
+      float mcol[NJh][2], lsum[NJh][2];
+      float cap[NJh][2];                          // +inf: a column of the slice, -inf: padding
+      int lim[NJh][2];                            // last position a column sees (-1: padding column)
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
+      for (int j = 0; j < NJh; ++j) {
         mcol[j][0] = mcol[j][1] = kNoScore;
         lsum[j][0] = lsum[j][1] = 0.f;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int col = 8 * j + 2 * ti + e;
+          const int col = c0h + 8 * j + 2 * ti + e;
           cap[j][e] = col < d.nh ? CUDART_INF_F : -CUDART_INF_F;
           lim[j][e] = col < d.nh ? causal_lim + (d.h0 + col) % a.tokens : -1;
         }
@@ -646,10 +668,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         const int sb = G & 1;
         bool ok = wait_or_abort(&bars[kBarSFull + sb], (G >> 1) & 1, abort_flag, a.status);
         tcgen05_after_sync();
-        uint32_t sr[2][kCols / 2];
+        uint32_t sr[2][kHalf / 2];
 #pragma unroll
         for (int s = 0; s < 2; ++s)
-          tmem_ld_scores<kCols>(tmem + (static_cast<uint32_t>(32 * q + 16 * s) << 16) + sb * kCols, sr[s]);
+          tmem_ld_scores<kHalf>(tmem + (static_cast<uint32_t>(32 * q + 16 * s) << 16) + sb * kCols + c0h, sr[s]);
         tmem_wait_ld();
         tcgen05_before_sync();
         __syncwarp();
@@ -661,7 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         // This thread's rows are tokens tok0 + {0, 8} of tile u0 and tok0 + {16, 24} of tile u0 + 1.
         // Fast path (32 columns, where the softmax paces the kernel; at 16 it measured slower):
         // both tiles resolved, and every row inside the item and seen by every column.
-        float x[2][NJ][4];
+        float x[2][NJh][4];
         const int tok0 = 128 * gl + 32 * q + gi;
         const int u0 = tok0 >> 4;
         const bool all_seen = kCols == 32 && u0 + 1 < d.units && (mt[u0] & 3) != kKindInvalid && (mt[u0 + 1] & 3) != kKindInvalid &&
@@ -670,7 +692,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
 #pragma unroll
           for (int s = 0; s < 2; ++s)
 #pragma unroll
-            for (int j = 0; j < NJ; ++j)
+            for (int j = 0; j < NJh; ++j)
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 x[s][j][i] = fminf(__uint_as_float(sr[s][4 * j + i]) * a.scale_log2, cap[j][i & 1]);
@@ -683,7 +705,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
               const int u = tok >> 4;
               const int pos = (u < d.units && (mt[u] & 3) != kKindInvalid && d.t0 + tok < d.t1) ? d.t0 + tok : INT_MAX;
 #pragma unroll
-              for (int j = 0; j < NJ; ++j)
+              for (int j = 0; j < NJh; ++j)
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
                   x[s][j][2 * i2 + e] =
@@ -693,36 +715,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         }
         bool grow = false;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j)
+        for (int j = 0; j < NJh; ++j)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const float mx = fmaxf(fmaxf(x[0][j][e], x[0][j][2 + e]), fmaxf(x[1][j][e], x[1][j][2 + e]));
             grow = grow || mx > mcol[j][e] + kRescaleThreshold;
           }
-        if (wg_any(grow || !ok)) {
+        if (wg_any(nb, grow || !ok)) {
           // the output holds this item's earlier groups: its rescale needs the previous PV done
           if (gl > 0) ok = wait_or_abort(&bars[kBarPvDone + (sb ^ 1)], ((G - 1) >> 1) & 1, abort_flag, a.status) && ok;
-          if (wg_any(!ok)) {
+          if (wg_any(nb, !ok)) {
             stop = true;
             break;
           }
           tcgen05_after_sync();
           // column maxima over the warpgroup's 128 tokens, then the new running max
 #pragma unroll
-          for (int j = 0; j < NJ; ++j)
+          for (int j = 0; j < NJh; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               float v = fmaxf(fmaxf(x[0][j][e], x[0][j][2 + e]), fmaxf(x[1][j][e], x[1][j][2 + e]));
 #pragma unroll
               for (int dd = 4; dd < 32; dd <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, dd));
-              if (gi == 0) red_max[q * kCols + 8 * j + 2 * ti + e] = v;
+              if (gi == 0) red_max[q * kCols + c0h + 8 * j + 2 * ti + e] = v;
             }
-          wg_sync();
+          wg_sync(nb);
 #pragma unroll
-          for (int j = 0; j < NJ; ++j)
+          for (int j = 0; j < NJh; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int c = 8 * j + 2 * ti + e;
+              const int c = c0h + 8 * j + 2 * ti + e;
               const float nm = fmaxf(fmaxf(mcol[j][e], fmaxf(red_max[c], red_max[kCols + c])),
                                      fmaxf(red_max[2 * kCols + c], red_max[3 * kCols + c]));   // finite: >= kNoScore
               const float al = fast_exp2(mcol[j][e] - nm);
@@ -730,29 +752,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
               lsum[j][e] *= al;
               if (q == 0 && gi == 0) alpha_s[c] = al;
             }
-          wg_sync();
+          wg_sync(nb);
           if (gl > 0) {
-            // rescale the output in tensor memory
+            // rescale this warpgroup's output columns in tensor memory: high halves at 2 kCols + c,
+            // low halves at 3 kCols + c
 #pragma unroll 1
-            for (int c0 = 0; c0 < 2 * kCols; c0 += 16) {      // both halves of the output
-              uint32_t o[16];
-              tmem_ld_32x32b_x16(tmem + lane_base + 2 * kCols + c0, o);
+            for (int c0 = 0; c0 < 2 * kHalf; c0 += 8) {
+              const int c = c0h + (c0 & (kHalf - 1));
+              const uint32_t col = (c0 < kHalf ? 2 * kCols : 3 * kCols) + c;
+              uint32_t o[8];
+              tmem_ld_32x32b_x8(tmem + lane_base + col, o);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha_s[(c0 + i) & (kCols - 1)]);
-              tmem_st_32x32b_x16(tmem + lane_base + 2 * kCols + c0, o);
+              for (int i = 0; i < 8; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha_s[c + i]);
+              tmem_st_32x32b_x8(tmem + lane_base + col, o);
             }
             tmem_wait_st();
           }
         }
         // P = 2^(x - m): BF16 high part and BF16 remainder, transposed into P^T core matrices
-        // (n-block j, k-block 4q + 2s (+1 for tokens 8-15 of the 16)) of buffer G & 1
-        uint8_t* pb = pop + sb * (2 * kCols * 256);
+        // (n-block c0h / 8 + j, k-block 4q + 2s (+1 for tokens 8-15 of the 16)) of buffer G & 1
+        uint8_t* pb = pop + sb * (2 * kCols * 256) + (c0h / 8) * kCoreRow;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
 #pragma unroll
-          for (int j = 0; j < NJ; ++j) {
+          for (int j = 0; j < NJh; ++j) {
             const float p0 = fast_exp2(x[s][j][0] - mcol[j][0]), p1 = fast_exp2(x[s][j][1] - mcol[j][1]);
             const float p2 = fast_exp2(x[s][j][2] - mcol[j][0]), p3 = fast_exp2(x[s][j][3] - mcol[j][1]);
             lsum[j][0] += p0 + p2;
@@ -777,21 +801,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       const bool ok = wait_or_abort(&bars[kBarPvDone + ((G - 1) & 1)], ((G - 1) >> 1) & 1, abort_flag, a.status);
       tcgen05_after_sync();
 #pragma unroll
-      for (int j = 0; j < NJ; ++j)
+      for (int j = 0; j < NJh; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           float v = lsum[j][e];
 #pragma unroll
           for (int dd = 4; dd < 32; dd <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, dd);
           if (gi == 0) {
-            red_sum[q * kCols + 8 * j + 2 * ti + e] = v;
-            if (q == 0) m_s[8 * j + 2 * ti + e] = mcol[j][e];
+            red_sum[q * kCols + c0h + 8 * j + 2 * ti + e] = v;
+            if (q == 0) m_s[c0h + 8 * j + 2 * ti + e] = mcol[j][e];
           }
         }
-      if (wg_any(!ok)) break;                     // also makes red_sum and m_s visible
+      if (wg_any(nb, !ok)) break;                 // also makes red_sum and m_s visible
       const int ch = 32 * q + lane;               // this thread's output channel (TMEM lane)
 #pragma unroll 1
-      for (int c0 = 0; c0 < kCols; c0 += 8) {
+      for (int c0 = c0h; c0 < c0h + kHalf; c0 += 8) {
         uint32_t o[8], olo[8];
         tmem_ld_32x32b_x8(tmem + lane_base + 2 * kCols + c0, o);
         tmem_ld_32x32b_x8(tmem + lane_base + 3 * kCols + c0, olo);
@@ -817,7 +841,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         }
       }
       tcgen05_before_sync();
-      wg_sync();                                  // every warp read the output and the sums
+      wg_sync(nb);                                // every warp read the output and the sums
       if (lane == 0) {
         mbar_arrive(&bars[kBarOFree]);
         mbar_arrive(&bars[kBarItemEmpty + buf]);

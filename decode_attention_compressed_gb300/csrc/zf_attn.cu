@@ -713,15 +713,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
 }
 
 // Which kernel a compressed call runs.  ZF_KERNEL_AUTO runs the tensor-memory kernel when a kv head
-// has more than 16 query columns (query heads per kv head x new tokens), where the warp-MMA kernel
-// would read its tiles three times or more, and the warp-MMA kernel otherwise.  Measured on GB300
-// (one call, 8192-token contexts): GQA-7 with 4 new tokens 823 against 1043 us, GQA-4 with 8 new
-// tokens 731 against 1050 us; at up to 16 columns the warp-MMA kernel is the faster one (GQA-7
-// with 2 new tokens: 548 against 588 us).  Returns whether it is the tensor-memory kernel, or -1
-// when that kernel was asked for and cannot run these sizes.
+// has more than 8 query columns (query heads per kv head x new tokens), where the warp-MMA kernel
+// would read its tiles twice or more, and the warp-MMA kernel otherwise.  Measured on GB300 (the
+// benchmark's CUDA-graph step, one layer of 8192-token contexts): 28-32 columns 1.70-1.82x faster
+// (GQA-7 with 4 new tokens 583 against 990 us), 16 columns 1.5-9% faster (GQA-4 with 4 new
+// tokens 315 against 339 us), 14 columns 1.3% slower (GQA-7 with 2 new tokens 510 against 503 us).
+// Returns whether it is the tensor-memory kernel, or -1 when that kernel was asked for and cannot
+// run these sizes.
 static int pick_tc(int32_t kernel, int batch, int hq, int hkv) {
   if (kernel == ZF_KERNEL_TCGEN05) return attention_tc_fits(batch, hq, hkv) ? 1 : -1;
-  if (kernel == ZF_KERNEL_AUTO && hq / hkv > 16 && attention_tc_fits(batch, hq, hkv)) return 1;
+  if (kernel == ZF_KERNEL_AUTO && hq / hkv > 8 && attention_tc_fits(batch, hq, hkv)) return 1;
   return 0;
 }
 

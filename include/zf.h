@@ -286,9 +286,8 @@ zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t
  *    request lengths: batch above 1439 (16 columns) or 1423 (32 columns) returns
  *    ZF_ERR_UNSUPPORTED.
  *  - ZF_KERNEL_AUTO (what zf_decode_attn / zf_decode_attn_multi do) runs ZF_KERNEL_TCGEN05 when
- *    a kv head has more than 16 columns (where the warp-MMA kernel would read its tiles three
- *    times or more) and the batch fits it, else ZF_KERNEL_WARP_MMA (the faster one on GB300 at up
- *    to 16 columns).
+ *    a kv head has more than 8 columns (where the warp-MMA kernel would read its tiles twice or
+ *    more) and the batch fits it, else ZF_KERNEL_WARP_MMA.
  *   Both give the same results within floating-point rounding (different summation order).
  *   Workspace: zf_decode_attn_multi_workspace_size covers every kernel.  Other arguments as for
  *   zf_decode_attn_multi.  Returns ZF_ERR_INVALID_ARGUMENT for an unknown `kernel`.

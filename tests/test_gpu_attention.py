@@ -331,6 +331,8 @@ MULTI_CASES = {
     "mha_t16_page64": (W(2, 2, 2, 64, 530, pool="random", seed=49), [530, 200], 16),
     # 40 columns: a 32-column slice and an 8-column slice
     "gqa20_t2_two_slices": (W(2, 40, 2, 16, 300, pool="random", seed=50), [300, 250], 2),
+    # one new token, GQA 12: 12 columns, which AUTO gives the tensor-memory kernel
+    "gqa12_t1": (W(2, 24, 2, 16, 333, pool="random", seed=51), [333, 50], 1),
 }
 
 
@@ -387,10 +389,11 @@ def test_multi_token_full_size_sampled(zf):
 
 
 @pytest.mark.parametrize("name, kernel", [("gqa16_t2", "tcgen05"), ("gqa20_t2_two_slices", "tcgen05"),
-                                          ("gqa7_t2_spikes", "warp_mma"), ("mha_t16_page64", "warp_mma")])
+                                          ("gqa7_t2_spikes", "tcgen05"), ("mha_t16_page64", "tcgen05"),
+                                          ("gqa12_t1", "tcgen05"), ("gqa4_t2", "warp_mma"), ("page64_t8", "warp_mma")])
 def test_auto_kernel_choice(zf, name, kernel):
-    """ZF_KERNEL_AUTO runs the tensor-memory kernel above 16 columns per kv head and the warp-MMA
-    kernel up to 16: its results are bit for bit those of the kernel it picks."""
+    """ZF_KERNEL_AUTO runs the tensor-memory kernel above 8 columns per kv head and the warp-MMA
+    kernel up to 8: its results are bit for bit those of the kernel it picks."""
     w, lens, T = MULTI_CASES[name]
     layer = I.make_layer(w, seq_lens=lens)
     gc = H.gpu_cache_from(layer, zf)

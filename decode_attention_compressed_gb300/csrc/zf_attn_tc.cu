@@ -233,11 +233,14 @@ __device__ __forceinline__ bool rebuild_half(const uint8_t* st, int kind, uint32
 #pragma unroll
     for (int j = 0; j < 4; ++j) hdr[j] = *reinterpret_cast<const uint32_t*>(st + j * kSlotBytes + kHeaderAt);
     const bool escapes = ((hdr[0] | hdr[1] | hdr[2] | hdr[3]) & kHeaderEscMask) != 0;
+    // header byte 0 (base/2) of the four blocks in one register, so that the loop below picks
+    // block j's with a byte permute rather than an indexed (local-memory) array
+    const uint32_t bases = __byte_perm(__byte_perm(hdr[0], hdr[1], 0x0040u), __byte_perm(hdr[2], hdr[3], 0x0040u), 0x5410u);
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) {
       uint32_t x[8];
       if (escapes) rebuild_lane(st + j * kSlotBytes, lane, x);
-      else rebuild_lane_noesc(st + j * kSlotBytes, lane, __byte_perm(hdr[j], 0u, 0x0000u), x);
+      else rebuild_lane_noesc(st + j * kSlotBytes, lane, __byte_perm(bases, 0u, 0x1111u * j), x);
       put(x, j);
     }
     return true;

@@ -422,6 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     const uint64_t policy = l2_evict_first_policy();
     uint32_t armed = 0, phase = 0;                 // per stage: a copy is in flight / parity of its next wait
     int n_issued = 0, n_used = 0;                  // this warp's tiles started / consumed
+    int st_issue = 0, st_use = 0;                  // their stages (n mod ns, kept without a division)
     int iss_k = 0, iss_u = r;                      // the next tile to start: item iss_k, unit iss_u
     bool iss_end = false, aborted = false;
     // Start copies while stages are free, up to the item after the one being consumed (k_cur);
@@ -439,11 +440,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
           iss_u = r;
           continue;
         }
-        const int st = n_issued % ns;
+        const int st = st_issue;
         if (issue_half(a, di, meta + (iss_k & 1) * kMaxItemTiles, iss_u, is_v, ring + st * kHalfStageBytes,
                        &ring_bars[st], lane, policy) != kKindInvalid)
           armed |= 1u << st;
         ++n_issued;
+        if (++st_issue == ns) st_issue = 0;
         iss_u += 8;
       }
     };
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         const int u = 8 * gl + r;
         const int Gg = G + gl;
         if (u < d.units) {
-          const int sidx = n_used % ns;
+          const int sidx = st_use;
           if (armed & (1u << sidx)) {
             if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) { aborted = true; break; }
             phase ^= 1u << sidx;
@@ -516,6 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(Gg));
           ++n_used;
+          if (++st_use == ns) st_use = 0;
           pump(k);
         } else {
           // no tile in this slot of the item's last group: V^T columns zero, K rows unused

@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
       const ItemDesc d = desc[buf];
       if (d.b < 0) break;
       const int* m = meta + buf * kMaxItemTiles;
-      dcur = &d;
+      dcur = &desc[buf];                           // (the shared copy: taking d's address would put d in local memory)
       mcur = m;
       const int ng = (d.units + 7) >> 3;
       pump(k);
@@ -550,11 +550,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     // neither waits behind the other: S^T = K Q^T of group qk_G and O^T += V^T P^T of group pv_G
     // (pv_G < qk_G).
     if (lane == 0) {
-      struct Info {
-        int item;
-        bool first;
-      };
-      Info info[8];                             // groups whose S^T is issued and O^T is not yet
+      // The item of a group whose S^T is issued and O^T is not yet: the current item k or the one
+      // before (item k is published only once item k - 2's outputs were read, so every O^T of
+      // item k - 2 was issued by then).  Their first groups tell which.
+      int cur_item = -1, cur_first = 0, prev_item = -1, prev_first = 0;
       int qk_G = 0, pv_G = 0, k = -1, gl = 0, ng = 0;
       bool end_seen = false;
       uint64_t t_last = global_timer_ns();
@@ -568,10 +567,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
           } else {
             ng = (d.units + 7) >> 3;
             gl = 0;
+            prev_item = cur_item;
+            prev_first = cur_first;
+            cur_item = k;
+            cur_first = qk_G;
           }
           progress = true;
         }
-        if (!end_seen && gl < ng && qk_G - pv_G < 8) {
+        if (!end_seen && gl < ng) {
           const int G = qk_G;
           if (mbar_test(&bars[kBarKFull + (G & 1)], (G >> 1) & 1) &&
               (G < 2 || mbar_test(&bars[kBarSFree + (G & 1)], ((G >> 1) - 1) & 1)) &&
@@ -585,7 +588,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
               umma_bf16_ta(d_tmem, k_tmem + 8 * j, umma_desc_kmajor(qb + j * 256), kIdesc, j > 0);
             umma_commit(&bars[kBarSFull + (G & 1)]);
             umma_commit(&bars[kBarKFree + (G & 1)]);
-            info[G & 7] = Info{k, gl == 0};
             ++qk_G;
             ++gl;
             progress = true;
@@ -593,10 +595,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         }
         if (pv_G < qk_G) {
           const int G = pv_G;
-          const Info x = info[G & 7];
+          const int x_item = G >= cur_first ? cur_item : prev_item;
+          const bool x_first = G == cur_first || G == prev_first;
           if (mbar_test(&bars[kBarPFull + (G & 1)], (G >> 1) & 1) &&
               mbar_test(&bars[kBarVFull + (G & 1)], (G >> 1) & 1) &&
-              (!x.first || x.item == 0 || mbar_test(&bars[kBarOFree], (x.item - 1) & 1))) {
+              (!x_first || x_item == 0 || mbar_test(&bars[kBarOFree], (x_item - 1) & 1))) {
             tcgen05_after_sync();
             const uint32_t o_tmem = tmem + 2 * kCols;
             const uint8_t* vb = vop + (G & 1) * kOpBytes;
@@ -604,7 +607,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               umma_bf16(o_tmem, umma_desc_kmajor(vb + j * 256), umma_desc_kmajor(pb + j * 256), kIdescPv,
-                        !(x.first && j == 0));
+                        !(x_first && j == 0));
             umma_commit(&bars[kBarPvDone + (G & 1)]);
             ++pv_G;
             progress = true;

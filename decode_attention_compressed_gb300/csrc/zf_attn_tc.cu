@@ -221,11 +221,14 @@ __device__ __forceinline__ void store_v_block(const uint32_t (&va)[8], int j, ui
 // One half tile (K or V, 4 blocks) from its stage into its operand.  kind: compressed or raw (a raw
 // half holds its first three blocks; fetch3() brings the fourth into the start of the stage and
 // returns false when its wait gave up).  Returns false only then.
-template <bool kV, typename Fetch3>
-__device__ __forceinline__ bool rebuild_half(const uint8_t* st, int kind, uint32_t keep_a, uint32_t keep_b, uint8_t* vop_g,
+// One copy of this code serves the K and the V warps (kV picks the store per block at run time):
+// measured on GB300, separate K and V copies were 1-4% slower, and the kernel is sensitive to its
+// code size (a K / V-specialised rebuild loop was 17-25% slower).
+template <typename Fetch3>
+__device__ __forceinline__ bool rebuild_half(bool kV, const uint8_t* st, int kind, uint32_t keep_a, uint32_t keep_b, uint8_t* vop_g,
                                              int p, uint32_t k_tmem, int lane, Fetch3&& fetch3) {
   auto put = [&](const uint32_t (&x)[8], int j) {
-    if constexpr (kV) store_v_block(x, j, vop_g, p, lane, keep_a, keep_b);
+    if (kV) store_v_block(x, j, vop_g, p, lane, keep_a, keep_b);
     else store_k_block(x, j, k_tmem);
   };
   if (kind == kKindComp) {
@@ -497,10 +500,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
                 keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
               }
             }
-            const bool ok_half = is_v ? rebuild_half<true>(st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
-                                          return fetch_block3(sidx, u);
-                                        })
-                                      : rebuild_half<false>(st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
+            const bool ok_half = rebuild_half(is_v, st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
                                           return fetch_block3(sidx, u);
                                         });
             if (!ok_half) {

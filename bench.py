@@ -9,7 +9,9 @@ compressed cache (the long-context workload also writes one new token per reques
 page through zf_append_tokens each step).  Inputs are resident in HBM; the per-step KV bytes exceed
 L2, so the step needs no extra flush.  Prints one JSON line on rank 0: the headline workload's
 step, and (default run, one GPU) a `per_config` object with every workload measured the same way
-plus, for each, the median of single calls timed alone after an L2 flush.  N > 1 runs N
+plus, for each, the median of single calls timed alone after an L2 flush, and a `multi_token`
+object: several new tokens per request on three shapes, with the kernel the library picks, the
+warp-MMA kernel and the dense comparator.  N > 1 runs N
 independent replicas (one per GPU, weak scaling); the step time is the maximum over ranks.  Without
 torchrun, --gpus N > 1 starts the N ranks itself.
 """
@@ -186,6 +188,9 @@ class ClockSampler:
 # Every workload the default run measures (one GPU): each is set up, timed and freed in turn.
 PER_CONFIG = ("tiny", "llama7b_mha_512", "llama7b_mha_2048", "llama7b_mha_8192", "llama3_8b_batched",
               "qwen2_7b_maxbatch", "long_ctx", "batch64_gqa4_2048", "batch64_gqa4_8192")
+# Several new tokens per request (speculative verification) in the default run: workload, tokens.
+# Columns per kv head: 14, 28 and 32 (the last two need 4 warp-MMA passes, 1 tensor-memory pass).
+MULTI_TOKEN = (("qwen2_7b_maxbatch", 2), ("qwen2_7b_maxbatch", 4), ("batch64_gqa4_8192", 8))
 MIN_TIMED_MS = 200.0          # per-config timed regions last at least this long (enough clock samples)
 ISOLATED_CALLS = 25           # single calls timed alone, each after an L2 flush
 ISOLATED_WARMUP = 3
@@ -503,6 +508,33 @@ class Workbench:
     def status(self):
         return [ent["cache"].status_word() | ent["dense"].status_word() for ent in self.layers]
 
+    # ---- one entry of multi_token
+    def multi_token_summary(self, steps, warmup, peak):
+        """T new tokens per request: the step with the kernel ZF_KERNEL_AUTO picks, with the warp-MMA
+        kernel named, and with the dense comparator (CUDA-graph replays, each timed region at least
+        MIN_TIMED_MS long)."""
+        w, L, T = self.w, len(self.layers), self.T
+        cols = w.num_q_heads // w.num_kv_heads * T
+        self.kernel = "auto"
+        ms, _, clocks, n = self.timed(self.graph("comp", lambda: self.step(False)), steps, warmup, min_ms=MIN_TIMED_MS)
+        self.kernel = "warp_mma"
+        mms, _, mclocks, _ = self.timed(self.graph("comp_mma", lambda: self.step(False)), steps, warmup,
+                                        min_ms=MIN_TIMED_MS)
+        self.kernel = "auto"
+        dms, _, dclocks, _ = self.timed(self.graph("dense", lambda: self.step(True)), steps, warmup,
+                                        min_ms=MIN_TIMED_MS)
+        comp_b, dense_b, _, ratio, _ = self.bytes()
+        if any(self.status()):
+            raise RuntimeError(f"device status word set: {self.status()}")
+        return {"workload": w.name, "tokens": T, "columns_per_kv_head": cols, "layers_per_step": L,
+                "auto_kernel": "tcgen05" if cols > 8 else "warp_mma",
+                "us_per_step": round(ms * 1e3, 3), "steps_timed": n,
+                "pct_of_hbm_peak_one_pass": round(100 * comp_b / (ms * 1e-3) / 1e9 / peak, 1),
+                "warp_mma_us_per_step": round(mms * 1e3, 3), "dense_us_per_step": round(dms * 1e3, 3),
+                "speedup_vs_warp_mma": round(mms / ms, 4), "speedup_vs_dense": round(dms / ms, 4),
+                "compression_ratio": round(ratio, 4), "clocks": clocks, "warp_mma_clocks": mclocks,
+                "dense_clocks": dclocks}
+
     # ---- one entry of per_config
     def summary(self, steps, warmup, peak):
         """The workload measured the same way as the headline (graph replays or eager appending
@@ -785,6 +817,13 @@ def run_gpu(args, rank, world, local_rank):
             torch.cuda.empty_cache()
         per["long_ctx"]["prefill_encode"] = prefill_encode(zf, I, device, peak)
         result["per_config"] = per
+        multi = {}
+        for name, T in MULTI_TOKEN:
+            mt = Workbench(zf, I, I.WORKLOADS[name], device, T, world, local_rank, max_steps)
+            multi[f"{name}_t{T}"] = mt.multi_token_summary(args.steps, args.warmup, peak)
+            del mt
+            torch.cuda.empty_cache()
+        result["multi_token"] = multi
         result["prefill_encode"] = per["long_ctx"]["prefill_encode"]
     return result
 

@@ -103,3 +103,13 @@ def test_clock_summary_from_nvidia_smi_lines(tmp_path):
     assert out["reasons"] == ["sw_power_cap"]
     assert not os.path.exists(s.path)
 
+
+
+def test_multi_token_lines_name_real_workloads_and_wide_column_sets():
+    """The default run's multi_token object times shapes whose columns per kv head (query heads per
+    kv head x new tokens) take the tensor-memory kernel (more than 8)."""
+    from decode_attention_compressed_gb300 import inputs as I
+    assert bench.MULTI_TOKEN
+    for name, T in bench.MULTI_TOKEN:
+        w = I.WORKLOADS[name]
+        assert T > 1 and w.num_q_heads // w.num_kv_heads * T > 8

@@ -1,9 +1,9 @@
 // Decode attention over the compressed paged cache when a kv head has more than 8 query columns
 // (GQA groups above 8, or several new tokens per request: columns = query heads per kv head x new
-// tokens), on the 5th-generation tensor cores: the rebuilt K and V tiles go to shared memory as
-// MMA operands and the scores and the output accumulate in tensor memory, so each kv head's tiles
-// are read from HBM once per 16 columns (the warp-MMA kernel takes 8 columns per pass and reads the
-// tiles once per 8).
+// tokens), on the 5th-generation tensor cores: the rebuilt K and V tiles become MMA operands (K in
+// tensor memory, V^T in shared memory) and the scores and the output accumulate in tensor memory,
+// so each kv head's tiles are read from HBM once per N = 16 or 32 columns (the warp-MMA kernel
+// takes 8 columns per pass and reads the tiles once per 8).
 //
 // ZipFusion §III.C (Attention over the Compressed KV Cache): compressed blocks are copied
 // HBM -> shared memory as they are and the exact BF16 values are rebuilt from them with integer
@@ -13,8 +13,9 @@
 // One CTA per SM, 26 warps:
 //  * warps 0-7 rebuild K, warps 8-15 rebuild V: warp r (mod 8) takes tile slot r of every
 //    128-token group of an item (16 tokens of one kv head).  It copies its half of the tile HBM ->
-//    its private stages with 1-D bulk copies (two stages per K warp, three per V warp: the next
-//    copies are in flight while it works on this one) and rebuilds it straight from the m16n8k16
+//    its private stages with 1-D bulk copies (at N = 16 three stages per K warp and two per V
+//    warp, at N = 32 two each: the next copies are in flight while it works on this one) and
+//    rebuilds it straight from the m16n8k16
 //    fragment registers the rebuild produces: K (A of S^T = K Q^T: 128 tokens x 128 channels) into
 //    one of two tensor-memory buffers with tcgen05.st, V^T (A of O^T = V^T P^T: 128 channels x 128
 //    tokens) into one of two shared-memory buffers in the K-major core-matrix layout (one
@@ -30,8 +31,8 @@
 //    item each warpgroup divides its O^T columns by their sums and writes the output or the
 //    partial;
 //  * warp 24 (MMA): allocates tensor memory; one lane issues both products, whichever is ready
-//    first: S^T = K Q^T (8 x M128 N16 K16, A from tensor memory) into one of two TMEM score
-//    buffers, and O^T += V^T P^T (8 MMAs of N = 32: P's high part and its remainder side by side)
+//    first: S^T = K Q^T (8 x M128 N K16, A from tensor memory) into one of two TMEM score
+//    buffers, and O^T += V^T P^T (8 MMAs of 2N: P's high part and its remainder side by side)
 //    into the TMEM output, each completion signalled by tcgen05.commit to an mbarrier;
 //  * warp 25 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
 //    item ahead: resolves the pages through the page table and the directory and stages the

@@ -227,7 +227,9 @@ size_t zf_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t
  *   workspace:  device buffer of at least zf_decode_attn_workspace_size(...) bytes, any contents;
  *               it must not be shared with a concurrent call.
  *   batch <= ZF_MAX_BATCH.  Two kernels are enqueued (attention, then merge); results are
- *   deterministic (no atomics).
+ *   deterministic (no atomics).  The attention kernel is the one ZF_KERNEL_AUTO picks (see
+ *   zf_decode_attn_multi_kernel): the warp-MMA kernel when a kv head has at most 8 query heads,
+ *   the tcgen05 kernel above that (where it fits the batch).
  *   Both are launched with programmatic stream serialisation: when the kernel ahead of them in
  *   the stream allows it (griddepcontrol.launch_dependents; this library's merge kernel does), the
  *   attention grid starts early.  Before its grid-dependency wait it only warms L2 and, for short

@@ -405,6 +405,27 @@ def test_auto_kernel_choice(zf, name, kernel):
     assert torch.equal(auto[0], picked[0]) and torch.equal(auto[1], picked[1])
 
 
+def test_batch_beyond_the_tensor_memory_kernel(zf):
+    """A batch whose request lengths do not fit the tensor-memory kernel's shared memory (more than
+    1439 requests at 16 columns): asked for by name it is refused before any launch; AUTO runs the
+    warp-MMA kernel instead, bit for bit, and both match the oracle."""
+    w = W(1500, 32, 2, 16, 40, ctx_min=1, pool="random", seed=52)        # 16 query heads per kv head
+    layer = I.make_layer(w)
+    gc = H.gpu_cache_from(layer, zf)
+    q, table, sl = layer.q.cuda(), layer.page_table.cuda(), layer.seq_lens.cuda()
+    with pytest.raises(zf.ZfError, match="unsupported"):
+        zf.decode_attn(gc, q, table, sl, layer.scale, kernel="tcgen05")
+    auto = zf.decode_attn(gc, q, table, sl, layer.scale)
+    mma = zf.decode_attn(gc, q, table, sl, layer.scale, kernel="warp_mma")
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    assert torch.equal(auto[0], mma[0]) and torch.equal(auto[1], mma[1])
+    oc = H.oracle_cache_from(layer, O)
+    ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q), oc, layer.page_table.numpy(), layer.seq_lens.numpy(),
+                                          layer.scale)
+    H.compare_attention(auto[0], auto[1], ref_out, ref_lse)
+
+
 @pytest.mark.parametrize("T", [2, 4])
 def test_tcgen05_full_size_sampled(zf, T):
     """Two or four new tokens per request on the Qwen2-7B max-batch shape (GQA 7: 14 or 28

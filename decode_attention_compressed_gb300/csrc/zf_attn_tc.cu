@@ -240,12 +240,29 @@ __device__ __forceinline__ bool rebuild_half(bool kV, const uint8_t* st, int kin
     // header byte 0 (base/2) of the four blocks in one register, so that the loop below picks
     // block j's with a byte permute rather than an indexed (local-memory) array
     const uint32_t bases = __byte_perm(__byte_perm(hdr[0], hdr[1], 0x0040u), __byte_perm(hdr[2], hdr[3], 0x0040u), 0x5410u);
+    if (escapes) {
 #pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
-      uint32_t x[8];
-      if (escapes) rebuild_lane(st + j * kSlotBytes, lane, x);
-      else rebuild_lane_noesc(st + j * kSlotBytes, lane, __byte_perm(bases, 0u, 0x1111u * j), x);
-      put(x, j);
+      for (int j = 0; j < 4; ++j) {
+        uint32_t x[8];
+        rebuild_lane(st + j * kSlotBytes, lane, x);
+        put(x, j);
+      }
+    } else {
+      // the next block's low bytes and codes are loaded while this one is rebuilt
+      uint4 lo_n = *reinterpret_cast<const uint4*>(st + 16 * lane);
+      uint2 cd_n = *reinterpret_cast<const uint2*>(st + 512 + 8 * lane);
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        const uint4 lo = lo_n;
+        const uint2 cd = cd_n;
+        const uint8_t* nx = st + (j < 3 ? j + 1 : 3) * kSlotBytes;
+        lo_n = *reinterpret_cast<const uint4*>(nx + 16 * lane);
+        cd_n = *reinterpret_cast<const uint2*>(nx + 512 + 8 * lane);
+        uint32_t h[4], x[8];
+        high_bytes(cd, __byte_perm(bases, 0u, 0x1111u * j), h);
+        interleave(lo, h, x);
+        put(x, j);
+      }
     }
     return true;
   }

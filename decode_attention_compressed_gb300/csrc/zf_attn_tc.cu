@@ -54,7 +54,8 @@ constexpr int kSoftmaxWarp0 = 16;                 // warps 16..23: warpgroup (w 
 constexpr int kSoftmaxWarps = 8;                  // two warpgroups, each owns half of the columns
 constexpr int kMmaWarp = kSoftmaxWarp0 + kSoftmaxWarps;
 constexpr int kMetaWarp = kMmaWarp + 1;
-constexpr int kTcWarps = kMetaWarp + 1;
+constexpr int kCopyWarp = kMetaWarp + 1;          // lane i keeps rebuild warp i's copy stages filled
+constexpr int kTcWarps = kCopyWarp + 1;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kHalfStageBytes = kTileCompBytes;   // one compressed K (or V) half tile; a raw half: 3 + 1 blocks
 constexpr int kOpBytes = 128 * 128 * 2;           // one 128 x 128 BF16 operand
@@ -79,8 +80,9 @@ struct TcStages {
 constexpr int kNumStages = kHalfWarps * 5;
 
 enum : int {
-  kBarStage = 0,                // one per copy stage of the rebuild warps (K warps first)
-  kBarItemFull = kNumStages,    // [2] the metadata warp published an item
+  kBarStage = 0,                // one per copy stage of the rebuild warps (K warps first): data landed
+  kBarStageEmpty = kNumStages,  // one per copy stage: its rebuild warp is done with it
+  kBarItemFull = 2 * kNumStages,      // [2] the metadata warp published an item
   kBarItemEmpty = kBarItemFull + 2,   // [2] rebuild + softmax warps are done with it
   kBarQFull = kBarItemEmpty + 2,      // [2] the item's query operand is staged
   kBarKFull = kBarQFull + 2,          // [2] the 8 K warps wrote a group's K operand (per K buffer)
@@ -96,7 +98,7 @@ enum : int {
 };
 
 struct TcLayout {
-  size_t vop, pop, qop, stages, meta, desc, bars, misc, red, prefix, lens, total;
+  size_t vop, pop, qop, stages, meta, desc, bars, misc, spar, red, prefix, lens, total;
 };
 
 template <int kCols>
@@ -111,6 +113,7 @@ __host__ __device__ inline TcLayout tc_layout(int batch) {
   s.desc = at; at += 2 * 64;
   s.bars = at; at += kNumBars * 8;
   s.misc = at; at += 16;                          // [0] abort flag, [4] TMEM base address
+  s.spar = at; at += kNumStages * 4;              // per stage: parity of its data barrier's next phase
   s.red = at; at += static_cast<size_t>(10 * kCols) * 4;   // column maxima [4][kCols], sums [4][kCols], alpha, max
   s.prefix = at; at += static_cast<size_t>(batch + 1) * 4;
   s.lens = at; at += static_cast<size_t>(batch) * 4;
@@ -325,6 +328,11 @@ template <int kCols>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a) {
   static_assert(4 * kCols <= static_cast<int>(kTmemK), "scores and output must end before the K operands");
   static_assert((kCols & (kCols - 1)) == 0 && 2 * kCols <= 256, "the PV MMA takes N = 2 kCols");
+  // At 16 columns the copy warp keeps the rebuild warps' stages filled (measured on GB300: GQA-7 x 2
+  // tokens 503 -> 466 us per call); at 32 columns, with two stages per rebuild warp, each rebuild
+  // warp starts its own copies (there the copy warp's reaction added to every copy's latency:
+  // GQA-7 x 4 tokens 567 -> 632 us).
+  constexpr bool kCopyWarpFeeds = kCols == 16;
   constexpr uint32_t kIdesc = umma_idesc_bf16(128, kCols);
   // O^T += V^T P^T takes P's high part and its remainder as 2 kCols columns of one operand: the
   // output holds V^T P_hi^T in its first kCols columns and V^T P_lo^T in the rest, summed at the
@@ -343,14 +351,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc + 4);
   float* red = reinterpret_cast<float*>(smem + L.red);
   int* prefix = reinterpret_cast<int*>(smem + L.prefix);
+  int* spar = reinterpret_cast<int*>(smem + L.spar);
   int* lens = reinterpret_cast<int*>(smem + L.lens);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int i = 0; i < kNumStages; ++i) mbar_init(&bars[kBarStage + i], 1);
+    for (int i = 0; i < kNumStages; ++i) {
+      mbar_init(&bars[kBarStage + i], 1);
+      mbar_init(&bars[kBarStageEmpty + i], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[kBarItemFull + b], 1);
-      mbar_init(&bars[kBarItemEmpty + b], kRebuildWarps + kSoftmaxWarps);
+      mbar_init(&bars[kBarItemEmpty + b], kRebuildWarps + kSoftmaxWarps + (kCopyWarpFeeds ? 1 : 0));
       mbar_init(&bars[kBarQFull + b], 1);
       mbar_init(&bars[kBarSFull + b], 1);
       mbar_init(&bars[kBarSFree + b], kSoftmaxWarps);
@@ -440,128 +452,340 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     const int first_stage = is_v ? kHalfWarps * kKSt + (warp - kHalfWarps) * kVSt : warp * kKSt;
     uint8_t* ring = stages + static_cast<size_t>(first_stage) * kHalfStageBytes;
     uint64_t* ring_bars = &bars[kBarStage + first_stage];
-    const uint64_t policy = l2_evict_first_policy();
-    uint32_t armed = 0, phase = 0;                 // per stage: a copy is in flight / parity of its next wait
-    int n_issued = 0, n_used = 0;                  // this warp's tiles started / consumed
-    int st_issue = 0, st_use = 0;                  // their stages (n mod ns, kept without a division)
-    int iss_k = 0, iss_u = r;                      // the next tile to start: item iss_k, unit iss_u
-    bool iss_end = false, aborted = false;
-    // Start copies while stages are free, up to the item after the one being consumed (k_cur);
-    // an item not yet published is tested, not waited for.
-    auto pump = [&](int k_cur) {
-      while (!iss_end && n_issued - n_used < ns && iss_k <= k_cur + 1) {
-        if (iss_k > k_cur && !mbar_test(&bars[kBarItemFull + (iss_k & 1)], (iss_k >> 1) & 1)) break;
-        const ItemDesc& di = desc[iss_k & 1];
-        if (di.b < 0) {
-          iss_end = true;
-          break;
+    if constexpr (kCopyWarpFeeds) {
+      uint64_t* ring_empty = &bars[kBarStageEmpty + first_stage];
+      const uint64_t policy = l2_evict_first_policy();
+      uint32_t phase = 0;                            // per stage: parity of its data barrier's next wait
+      int st_use = 0;                                // the stage of the next tile (its index mod ns)
+      bool aborted = false, fetch3_pending = false;
+      int G = 0;
+      const ItemDesc* dcur = nullptr;
+      const int* mcur = nullptr;
+      // the fourth block of a raw half tile into the start of its stage (the first three are used)
+      auto fetch_block3 = [&](int sidx, int u) -> bool {
+        __syncwarp();
+        fetch_raw_block3(a, *dcur, mcur, u, is_v, ring + sidx * kHalfStageBytes, &ring_bars[sidx], lane, policy);
+        if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) {
+          fetch3_pending = true;                     // still in flight: waited for at the end
+          return false;
         }
-        if (iss_u >= di.units) {
-          ++iss_k;
-          iss_u = r;
-          continue;
-        }
-        const int st = st_issue;
-        if (issue_half(a, di, meta + (iss_k & 1) * kMaxItemTiles, iss_u, is_v, ring + st * kHalfStageBytes,
-                       &ring_bars[st], lane, policy) != kKindInvalid)
-          armed |= 1u << st;
-        ++n_issued;
-        if (++st_issue == ns) st_issue = 0;
-        iss_u += 8;
-      }
-    };
-    int G = 0;
-    const ItemDesc* dcur = nullptr;
-    const int* mcur = nullptr;
-    // the fourth block of a raw half tile into the start of its stage (the first three are used)
-    auto fetch_block3 = [&](int sidx, int u) -> bool {
-      __syncwarp();
-      fetch_raw_block3(a, *dcur, mcur, u, is_v, ring + sidx * kHalfStageBytes, &ring_bars[sidx], lane, policy);
-      if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) return false;
-      phase ^= 1u << sidx;
-      return true;
-    };
-    for (int k = 0; !aborted; ++k) {
-      const int buf = k & 1;
-      if (!wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
-      const ItemDesc d = desc[buf];
-      if (d.b < 0) break;
-      const int* m = meta + buf * kMaxItemTiles;
-      dcur = &desc[buf];                           // (the shared copy: taking d's address would put d in local memory)
-      mcur = m;
-      const int ng = (d.units + 7) >> 3;
-      pump(k);
-      for (int gl = 0; gl < ng && !aborted; ++gl) {
-        const int u = 8 * gl + r;
-        const int Gg = G + gl;
-        if (u < d.units) {
-          const int sidx = st_use;
-          if (armed & (1u << sidx)) {
+        phase ^= 1u << sidx;
+        return true;
+      };
+      for (int k = 0; !aborted; ++k) {
+        const int buf = k & 1;
+        if (!wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
+        const ItemDesc d = desc[buf];
+        if (d.b < 0) break;
+        const int* m = meta + buf * kMaxItemTiles;
+        dcur = &desc[buf];                           // (the shared copy: taking d's address would put d in local memory)
+        mcur = m;
+        const int ng = (d.units + 7) >> 3;
+        for (int gl = 0; gl < ng && !aborted; ++gl) {
+          const int u = 8 * gl + r;
+          const int Gg = G + gl;
+          if (u < d.units) {
+            // every tile of this warp has a stage: its copy, or a plain arrival for a page that
+            // could not be resolved, comes from the copy warp
+            const int sidx = st_use;
             if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) { aborted = true; break; }
             phase ^= 1u << sidx;
-            armed &= ~(1u << sidx);
-          }
-          const int kind = m[u] & 3;
-          uint8_t* st = ring + sidx * kHalfStageBytes;
-          if (!wait_operand_free(Gg)) { aborted = true; break; }
-          uint8_t* op = vop + (Gg & 1) * kOpBytes;
-          const uint32_t k_tmem = tmem + (static_cast<uint32_t>(16 * r) << 16) + kTmemK + (Gg & 1) * 64;
-          if (kind == kKindInvalid) {
-            if (is_v) zero_v_tile(op, r, lane);
-          } else {
-            uint32_t keep_a = 0xFFFFFFFFu, keep_b = 0xFFFFFFFFu;
-            if (is_v) {
-              const int ntok = min(16, d.t1 - (d.t0 + 16 * u));
-              const int ti = lane & 3;
-              if (ntok < 16) {
-                keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
-                keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
+            const int kind = m[u] & 3;
+            uint8_t* st = ring + sidx * kHalfStageBytes;
+            if (!wait_operand_free(Gg)) { aborted = true; break; }
+            uint8_t* op = vop + (Gg & 1) * kOpBytes;
+            const uint32_t k_tmem = tmem + (static_cast<uint32_t>(16 * r) << 16) + kTmemK + (Gg & 1) * 64;
+            if (kind == kKindInvalid) {
+              if (is_v) zero_v_tile(op, r, lane);
+            } else {
+              uint32_t keep_a = 0xFFFFFFFFu, keep_b = 0xFFFFFFFFu;
+              if (is_v) {
+                const int ntok = min(16, d.t1 - (d.t0 + 16 * u));
+                const int ti = lane & 3;
+                if (ntok < 16) {
+                  keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
+                  keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
+                }
+              }
+              const bool ok_half = rebuild_half(is_v, st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
+                                            return fetch_block3(sidx, u);
+                                          });
+              if (!ok_half) {
+                aborted = true;
+                break;
               }
             }
-            const bool ok_half = rebuild_half(is_v, st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
-                                          return fetch_block3(sidx, u);
-                                        });
-            if (!ok_half) {
-              armed |= 1u << sidx;               // still in flight: waited for at the end
-              aborted = true;
+            // the stage is read: hand it back to the copy warp with its data barrier's next parity
+            __syncwarp();
+            if (lane == 0) {
+              spar[first_stage + sidx] = (phase >> sidx) & 1;
+              mbar_arrive(&ring_empty[sidx]);
+            }
+            if (++st_use == ns) st_use = 0;
+            if (is_v) {
+              fence_proxy_async_smem();
+            } else {
+              tmem_wait_st();
+              tcgen05_before_sync();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(Gg));
+          } else {
+            // no tile in this slot of the item's last group: V^T columns zero, K rows unused
+            if (!wait_operand_free(Gg)) { aborted = true; break; }
+            if (is_v) zero_v_tile(vop + (Gg & 1) * kOpBytes, r, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(Gg));
+          }
+        }
+        if (aborted) break;
+        G += ng;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarItemEmpty + buf]);
+      }
+      // a raw block this warp fetched itself and never waited for must land before the CTA exits
+      if (fetch3_pending && !mbar_wait(&ring_bars[st_use], (phase >> st_use) & 1)) report(a.status, ZF_DEV_TIMEOUT);
+    } else {
+      // at 32 columns each rebuild warp starts its own copies
+      const uint64_t policy = l2_evict_first_policy();
+      uint32_t armed = 0, phase = 0;                 // per stage: a copy is in flight / parity of its next wait
+      int n_issued = 0, n_used = 0;                  // this warp's tiles started / consumed
+      int st_issue = 0, st_use = 0;                  // their stages (n mod ns, kept without a division)
+      int iss_k = 0, iss_u = r;                      // the next tile to start: item iss_k, unit iss_u
+      bool iss_end = false, aborted = false;
+      // Start copies while stages are free, up to the item after the one being consumed (k_cur);
+      // an item not yet published is tested, not waited for.
+      auto pump = [&](int k_cur) {
+        while (!iss_end && n_issued - n_used < ns && iss_k <= k_cur + 1) {
+          if (iss_k > k_cur && !mbar_test(&bars[kBarItemFull + (iss_k & 1)], (iss_k >> 1) & 1)) break;
+          const ItemDesc& di = desc[iss_k & 1];
+          if (di.b < 0) {
+            iss_end = true;
+            break;
+          }
+          if (iss_u >= di.units) {
+            ++iss_k;
+            iss_u = r;
+            continue;
+          }
+          const int st = st_issue;
+          if (issue_half(a, di, meta + (iss_k & 1) * kMaxItemTiles, iss_u, is_v, ring + st * kHalfStageBytes,
+                         &ring_bars[st], lane, policy) != kKindInvalid)
+            armed |= 1u << st;
+          ++n_issued;
+          if (++st_issue == ns) st_issue = 0;
+          iss_u += 8;
+        }
+      };
+      int G = 0;
+      const ItemDesc* dcur = nullptr;
+      const int* mcur = nullptr;
+      // the fourth block of a raw half tile into the start of its stage (the first three are used)
+      auto fetch_block3 = [&](int sidx, int u) -> bool {
+        __syncwarp();
+        fetch_raw_block3(a, *dcur, mcur, u, is_v, ring + sidx * kHalfStageBytes, &ring_bars[sidx], lane, policy);
+        if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) return false;
+        phase ^= 1u << sidx;
+        return true;
+      };
+      for (int k = 0; !aborted; ++k) {
+        const int buf = k & 1;
+        if (!wait_or_abort(&bars[kBarItemFull + buf], (k >> 1) & 1, abort_flag, a.status, a.wait_limit_ns)) break;
+        const ItemDesc d = desc[buf];
+        if (d.b < 0) break;
+        const int* m = meta + buf * kMaxItemTiles;
+        dcur = &desc[buf];                           // (the shared copy: taking d's address would put d in local memory)
+        mcur = m;
+        const int ng = (d.units + 7) >> 3;
+        pump(k);
+        for (int gl = 0; gl < ng && !aborted; ++gl) {
+          const int u = 8 * gl + r;
+          const int Gg = G + gl;
+          if (u < d.units) {
+            const int sidx = st_use;
+            if (armed & (1u << sidx)) {
+              if (!wait_or_abort(&ring_bars[sidx], (phase >> sidx) & 1, abort_flag, a.status)) { aborted = true; break; }
+              phase ^= 1u << sidx;
+              armed &= ~(1u << sidx);
+            }
+            const int kind = m[u] & 3;
+            uint8_t* st = ring + sidx * kHalfStageBytes;
+            if (!wait_operand_free(Gg)) { aborted = true; break; }
+            uint8_t* op = vop + (Gg & 1) * kOpBytes;
+            const uint32_t k_tmem = tmem + (static_cast<uint32_t>(16 * r) << 16) + kTmemK + (Gg & 1) * 64;
+            if (kind == kKindInvalid) {
+              if (is_v) zero_v_tile(op, r, lane);
+            } else {
+              uint32_t keep_a = 0xFFFFFFFFu, keep_b = 0xFFFFFFFFu;
+              if (is_v) {
+                const int ntok = min(16, d.t1 - (d.t0 + 16 * u));
+                const int ti = lane & 3;
+                if (ntok < 16) {
+                  keep_a = (2 * ti < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 1 < ntok ? 0xFFFF0000u : 0u);
+                  keep_b = (2 * ti + 8 < ntok ? 0x0000FFFFu : 0u) | (2 * ti + 9 < ntok ? 0xFFFF0000u : 0u);
+                }
+              }
+              const bool ok_half = rebuild_half(is_v, st, kind, keep_a, keep_b, op, r, k_tmem, lane, [&]() {
+                                            return fetch_block3(sidx, u);
+                                          });
+              if (!ok_half) {
+                armed |= 1u << sidx;               // still in flight: waited for at the end
+                aborted = true;
+                break;
+              }
+            }
+            if (is_v) {
+              fence_proxy_async_smem();
+            } else {
+              tmem_wait_st();
+              tcgen05_before_sync();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(Gg));
+            ++n_used;
+            if (++st_use == ns) st_use = 0;
+            pump(k);
+          } else {
+            // no tile in this slot of the item's last group: V^T columns zero, K rows unused
+            if (!wait_operand_free(Gg)) { aborted = true; break; }
+            if (is_v) zero_v_tile(vop + (Gg & 1) * kOpBytes, r, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(Gg));
+          }
+        }
+        if (aborted) break;
+        G += ng;
+        // every tile of this item was consumed, so started: the start pointer leaves the item before
+        // its descriptor buffer is released (and reused for item k + 2)
+        if (iss_k == k) {
+          iss_k = k + 1;
+          iss_u = r;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarItemEmpty + buf]);
+      }
+      // copies still in flight (only after a wait gave up, or started for an item never reached)
+      // must land before the CTA exits
+      for (int s2 = 0; s2 < ns; ++s2)
+        if ((armed & (1u << s2)) && !mbar_wait(&ring_bars[s2], (phase >> s2) & 1)) report(a.status, ZF_DEV_TIMEOUT);
+    }
+  } else if (warp == kCopyWarp) {
+    if constexpr (kCopyWarpFeeds) {
+      // ================================================================== copy warp
+      // Lane w (< 16) keeps rebuild warp w's stages filled: it follows that warp's tiles (units r,
+      // r + 8, .. of every item), and as soon as a stage is handed back (and the item published) it
+      // starts the next tile's copy into it, or arrives on its data barrier for a page that could not
+      // be resolved.  It leaves an item as soon as it has started that item's last tile for its warp;
+      // the warp releases an item once every lane has left it.
+      constexpr int kKSt = TcStages<kCols>::kK, kVSt = TcStages<kCols>::kV;
+      const bool act = lane < kRebuildWarps;
+      const int w = act ? lane : 0;
+      const bool is_v = w >= kHalfWarps;
+      const int r = is_v ? w - kHalfWarps : 2 * (w & 3) + (w >> 2);
+      const int ns = is_v ? kVSt : kKSt;
+      const int first_stage = is_v ? kHalfWarps * kKSt + (w - kHalfWarps) * kVSt : w * kKSt;
+      uint8_t* ring = stages + static_cast<size_t>(first_stage) * kHalfStageBytes;
+      uint64_t* ring_bars = &bars[kBarStage + first_stage];
+      uint64_t* ring_empty = &bars[kBarStageEmpty + first_stage];
+      const uint64_t policy = l2_evict_first_policy();
+      int iss_k = 0, iss_u = r, st = 0, released = 0;
+      bool done = !act, ready = false;              // ready: item iss_k is published
+      uint32_t used = 0, epar = 0, ipar = 0;        // per stage: started once / next handback parity / last start's parity
+      uint64_t idle_since = 0;                      // start of the current run of idle iterations (0: none)
+      while (true) {
+        bool progress = false, left = false;
+        if (!done && !ready) ready = mbar_test(&bars[kBarItemFull + (iss_k & 1)], (iss_k >> 1) & 1);
+        if (ready) {
+          const ItemDesc& di = desc[iss_k & 1];
+          if (di.b < 0) {
+            done = true;
+            ready = false;
+          } else if (iss_u >= di.units) {           // no tile of this warp in the item
+            ++iss_k;
+            iss_u = r;
+            ready = false;
+            progress = left = true;
+          } else if (!((used >> st) & 1) || mbar_test(&ring_empty[st], (epar >> st) & 1)) {
+            uint32_t par = 0;
+            if ((used >> st) & 1) {
+              epar ^= 1u << st;
+              par = static_cast<uint32_t>(spar[first_stage + st]);
+            }
+            used |= 1u << st;
+            ipar = (ipar & ~(1u << st)) | (par << st);
+            const int mu = meta[(iss_k & 1) * kMaxItemTiles + iss_u];
+            const int kind = mu & 3;
+            const size_t head = static_cast<size_t>(mu >> 5) * a.hkv + di.g;
+            const int t = (mu >> 2) & 7;
+            uint8_t* dst = ring + st * kHalfStageBytes;
+            if (kind == kKindComp) {
+              mbar_arrive_expect_tx(&ring_bars[st], kTileCompBytes);
+              bulk_copy_g2s(dst, (is_v ? a.v_comp : a.k_comp) + head * a.comp_head_bytes + static_cast<size_t>(t) * kTileCompBytes,
+                            kTileCompBytes, &ring_bars[st], policy);
+            } else if (kind == kKindRaw) {
+              mbar_arrive_expect_tx(&ring_bars[st], 3 * kRawBlockBytes);
+              bulk_copy_g2s(dst, (is_v ? a.v_raw : a.k_raw) + head * a.raw_head_bytes + static_cast<size_t>(t) * kTileRawBytes,
+                            3 * kRawBlockBytes, &ring_bars[st], policy);
+            } else {
+              mbar_arrive(&ring_bars[st]);
+            }
+            if (++st == ns) st = 0;
+            iss_u += 8;
+            if (iss_u >= di.units) {                // leave the item at once: its buffer may be reused
+              ++iss_k;
+              iss_u = r;
+              ready = false;
+              left = true;
+            }
+            progress = true;
+          }
+        }
+        // items every lane has left go back to the metadata warp
+        if (__any_sync(0xFFFFFFFFu, left)) {
+          const int min_k = __reduce_min_sync(0xFFFFFFFFu, act ? iss_k : INT_MAX);
+          while (released < min_k) {
+            if (lane == 0) mbar_arrive(&bars[kBarItemEmpty + (released & 1)]);
+            ++released;
+          }
+        }
+        if (__any_sync(0xFFFFFFFFu, progress)) {
+          idle_since = 0;
+          continue;
+        }
+        if (__all_sync(0xFFFFFFFFu, done)) break;
+        if (*abort_flag) break;
+        const uint64_t now = global_timer_ns();
+        if (idle_since == 0) {
+          idle_since = now;
+        } else if (now - idle_since > a.wait_limit_ns + kWaitTimeoutNs) {
+          *abort_flag = 1;
+          report(a.status, ZF_DEV_TIMEOUT);
+          break;
+        }
+      }
+      // Every copy started must land before the CTA exits.  Normally its rebuild warp hands the stage
+      // back once it has used it; after a wait gave up (abort flag) the copy's own barrier phase is
+      // waited for instead (a rebuild warp gives up only before its handback of a stage can be
+      // preceded by its own fetch of a raw fourth block, so that phase is still the copy's).
+      if (act) {
+        const uint64_t t0 = global_timer_ns();
+        for (int s2 = 0; s2 < ns; ++s2) {
+          if (!((used >> s2) & 1)) continue;
+          while (!mbar_test(&ring_empty[s2], (epar >> s2) & 1)) {
+            if (*abort_flag) {
+              if (!mbar_wait(&ring_bars[s2], (ipar >> s2) & 1)) report(a.status, ZF_DEV_TIMEOUT);
+              break;
+            }
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+              report(a.status, ZF_DEV_TIMEOUT);
               break;
             }
           }
-          if (is_v) {
-            fence_proxy_async_smem();
-          } else {
-            tmem_wait_st();
-            tcgen05_before_sync();
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full_bar(Gg));
-          ++n_used;
-          if (++st_use == ns) st_use = 0;
-          pump(k);
-        } else {
-          // no tile in this slot of the item's last group: V^T columns zero, K rows unused
-          if (!wait_operand_free(Gg)) { aborted = true; break; }
-          if (is_v) zero_v_tile(vop + (Gg & 1) * kOpBytes, r, lane);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full_bar(Gg));
         }
       }
-      if (aborted) break;
-      G += ng;
-      // every tile of this item was consumed, so started: the start pointer leaves the item before
-      // its descriptor buffer is released (and reused for item k + 2)
-      if (iss_k == k) {
-        iss_k = k + 1;
-        iss_u = r;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarItemEmpty + buf]);
     }
-    // copies still in flight (only after a wait gave up, or started for an item never reached)
-    // must land before the CTA exits
-    for (int s2 = 0; s2 < ns; ++s2)
-      if ((armed & (1u << s2)) && !mbar_wait(&ring_bars[s2], (phase >> s2) & 1)) report(a.status, ZF_DEV_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ================================================================== MMA warp
     // One lane issues both products, whichever is ready first (non-blocking tests), so that

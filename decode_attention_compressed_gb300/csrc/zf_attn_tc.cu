@@ -10,12 +10,12 @@
 // operations right before the tensor-core instructions; raw blocks need no rebuild.  §IV.B: split
 // chunks are combined by a split-result merge.
 //
-// One CTA per SM, 26 warps:
+// One CTA per SM, 27 warps:
 //  * warps 0-7 rebuild K, warps 8-15 rebuild V: warp r (mod 8) takes tile slot r of every
-//    128-token group of an item (16 tokens of one kv head).  It copies its half of the tile HBM ->
-//    its private stages with 1-D bulk copies (at N = 16 three stages per K warp and two per V
-//    warp, at N = 32 two each: the next copies are in flight while it works on this one) and
-//    rebuilds it straight from the m16n8k16
+//    128-token group of an item (16 tokens of one kv head).  Its half of the tile comes HBM ->
+//    its private stages by 1-D bulk copies (at N = 16 three stages per K warp and two per V warp,
+//    started by the copy warp; at N = 32 two each, started by the warp itself: the next copies are
+//    in flight while it works on this one), and it rebuilds the half straight from the m16n8k16
 //    fragment registers the rebuild produces: K (A of S^T = K Q^T: 128 tokens x 128 channels) into
 //    one of two tensor-memory buffers with tcgen05.st, V^T (A of O^T = V^T P^T: 128 channels x 128
 //    tokens) into one of two shared-memory buffers in the K-major core-matrix layout (one
@@ -36,7 +36,8 @@
 //    into the TMEM output, each completion signalled by tcgen05.commit to an mbarrier;
 //  * warp 25 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
 //    item ahead: resolves the pages through the page table and the directory and stages the
-//    item's query rows as the B operand of S^T.
+//    item's query rows as the B operand of S^T;
+//  * warp 26 (copy, N = 16): lane w starts rebuild warp w's copies as soon as it hands a stage back.
 // Every wait is bounded (2 s); a wait that gives up sets ZF_DEV_TIMEOUT and the CTA winds down
 // (each softmax warpgroup decides together, so its named barriers are always met).
 #include <cuda_runtime.h>

@@ -31,9 +31,10 @@
 //    item each warpgroup divides its O^T columns by their sums and writes the output or the
 //    partial;
 //  * warp 24 (MMA): allocates tensor memory; the warp runs the issue loop and one elected lane
-//    issues both products, whichever is ready first: S^T = K Q^T (8 x M128 N K16, A from tensor memory) into one of two TMEM score
-//    buffers, and O^T += V^T P^T (8 MMAs of 2N: P's high part and its remainder side by side)
-//    into the TMEM output, each completion signalled by tcgen05.commit to an mbarrier;
+//    issues both products, whichever is ready first: S^T = K Q^T (8 x M128 N K16, A from tensor
+//    memory) into one of two TMEM score buffers, and O^T += V^T P^T (8 MMAs of 2N: P's high part
+//    and its remainder side by side) into the TMEM output, each completion signalled by
+//    tcgen05.commit to an mbarrier;
 //  * warp 25 (metadata): walks the CTA's items (the warp-MMA kernel's planner and page walk), one
 //    item ahead: resolves the pages through the page table and the directory and stages the
 //    item's query rows as the B operand of S^T;

@@ -285,7 +285,7 @@ zf_status zf_decode_attn_multi(const zf_cache* cache, const uint16_t* q, int32_t
  *    memory, V^T in shared memory; M = 128 tokens or channels) whose scores and output accumulate
  *    in tensor memory: N = 16 columns per pass when a kv head has at most 16 columns, else 32,
  *    so a kv head's tiles are read once per 16 or 32 columns.  Its shared memory also holds the
- *    request lengths: batch above 1439 (16 columns) or 1423 (32 columns) returns
+ *    request lengths: batch above 1379 (16 columns) or 1363 (32 columns) returns
  *    ZF_ERR_UNSUPPORTED.
  *  - ZF_KERNEL_AUTO (what zf_decode_attn / zf_decode_attn_multi do) runs ZF_KERNEL_TCGEN05 when
  *    a kv head has more than 8 columns (where the warp-MMA kernel would read its tiles twice or

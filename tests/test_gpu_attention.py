@@ -407,7 +407,7 @@ def test_auto_kernel_choice(zf, name, kernel):
 
 def test_batch_beyond_the_tensor_memory_kernel(zf):
     """A batch whose request lengths do not fit the tensor-memory kernel's shared memory (more than
-    1439 requests at 16 columns): asked for by name it is refused before any launch; AUTO runs the
+    1379 requests at 16 columns): asked for by name it is refused before any launch; AUTO runs the
     warp-MMA kernel instead, bit for bit, and both match the oracle."""
     w = W(1500, 32, 2, 16, 40, ctx_min=1, pool="random", seed=52)        # 16 query heads per kv head
     layer = I.make_layer(w)
@@ -424,6 +424,29 @@ def test_batch_beyond_the_tensor_memory_kernel(zf):
     ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q), oc, layer.page_table.numpy(), layer.seq_lens.numpy(),
                                           layer.scale)
     H.compare_attention(auto[0], auto[1], ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("hq, limit", [(32, 1379), (64, 1363)])
+def test_tensor_memory_kernel_batch_limit(zf, hq, limit):
+    """The largest batch whose request lengths fit the tensor-memory kernel's shared memory: 1379
+    requests at 16 columns per kv head, 1363 at 32.  At the limit the kernel runs (AUTO picks it, bit
+    for bit) and matches the oracle; one request more is refused by name before any launch."""
+    w = W(limit + 1, hq, 2, 16, 24, ctx_min=1, pool="random", seed=53)
+    layer = I.make_layer(w)
+    gc = H.gpu_cache_from(layer, zf)
+    q, table, sl = layer.q.cuda(), layer.page_table.cuda(), layer.seq_lens.cuda()
+    with pytest.raises(zf.ZfError, match="unsupported"):
+        zf.decode_attn(gc, q, table, sl, layer.scale, kernel="tcgen05")
+    q, table, sl = q[:limit], table[:limit], sl[:limit]
+    tc = zf.decode_attn(gc, q, table, sl, layer.scale, kernel="tcgen05")
+    auto = zf.decode_attn(gc, q, table, sl, layer.scale)
+    torch.cuda.synchronize()
+    assert gc.status_word() == 0
+    assert torch.equal(auto[0], tc[0]) and torch.equal(auto[1], tc[1])
+    oc = H.oracle_cache_from(layer, O)
+    ref_out, ref_lse = O.decode_attention(H.np_bits(layer.q[:limit]), oc, layer.page_table[:limit].numpy(),
+                                          layer.seq_lens[:limit].numpy(), layer.scale)
+    H.compare_attention(tc[0], tc[1], ref_out, ref_lse)
 
 
 @pytest.mark.parametrize("T", [2, 4])

@@ -715,9 +715,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeArgs
 // Which kernel a compressed call runs.  ZF_KERNEL_AUTO runs the tensor-memory kernel when a kv head
 // has more than 8 query columns (query heads per kv head x new tokens), where the warp-MMA kernel
 // would read its tiles twice or more, and the warp-MMA kernel otherwise.  Measured on GB300 (the
-// benchmark's CUDA-graph step, one layer of 8192-token contexts): 28-32 columns 1.70-1.82x faster
-// (GQA-7 with 4 new tokens 583 against 990 us), 16 columns 1.5-9% faster (GQA-4 with 4 new
-// tokens 315 against 339 us), 14 columns 1.3% slower (GQA-7 with 2 new tokens 510 against 503 us).
+// benchmark's CUDA-graph step, one layer of 8192-token contexts): 28-32 columns 1.88-2.00x faster
+// (GQA-7 with 4 new tokens 526 against 990 us), 14-16 columns 1.18-1.26x faster (GQA-7 with 2 new
+// tokens 427 against 503 us, GQA-4 with 4 new tokens 274 against 340 us).
 // Returns whether it is the tensor-memory kernel, or -1 when that kernel was asked for and cannot
 // run these sizes.
 static int pick_tc(int32_t kernel, int batch, int hq, int hkv) {

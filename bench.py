@@ -312,6 +312,23 @@ def replica_requests(batch: int, rank: int, world: int):
     return list(range(start, start + per + (1 if rank < extra else 0)))
 
 
+def arm_config(w, tokens: int, kernel: str, world: int) -> dict:
+    """The `config` object of a bench line, the same for this library's arm and the reference arm.
+    The L2 note uses a lower bound on the KV bytes a step reads: every request's shortest possible
+    context, all of it in compressed pages."""
+    from decode_attention_compressed_gb300 import accounting as A
+    min_bytes = w.batch * w.num_kv_heads * (w.ctx_min or w.ctx) * A.compressed_bytes_per_token_head() * w.layers
+    if min_bytes > L2_BYTES:
+        l2 = (f"no flush: every step reads at least {min_bytes / 1e9:.2f} GB of compressed KV "
+              f"(> {L2_BYTES / 2**20:.0f} MiB L2)")
+    else:
+        l2 = f"no flush: a step reads from {min_bytes / 1e6:.1f} MB of KV, which may stay in the {L2_BYTES / 2**20:.0f} MiB L2"
+    return {"workload": w.name, "note": w.note, "batch": w.batch, "q_heads": w.num_q_heads,
+            "kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": w.page_size, "ctx": w.ctx,
+            "layers_per_step": w.layers, "new_tokens_per_request": tokens, "kernel": kernel,
+            "parallelism": "replicas" if world > 1 else "single", "l2": l2}
+
+
 def workload_of(args):
     from decode_attention_compressed_gb300 import inputs as I
     w = I.WORKLOADS[args.workload]
@@ -763,12 +780,7 @@ def run_gpu(args, rank, world, local_rank):
         metric=METRIC, value=round(ms_step * 1e3, 3), unit="us/step", n_gpus=world, steps=args.steps,
         warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=False, scaling="weak",
         vs_baseline=None, dtype="bf16", data="synthetic (seeded, distributions of the workload)",
-        config={"workload": w.name, "note": w.note, "batch": w.batch, "q_heads": w.num_q_heads,
-                "kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": w.page_size, "ctx": w.ctx,
-                "layers_per_step": w.layers, "new_tokens_per_request": T, "kernel": args.kernel,
-                "parallelism": "replicas" if world > 1 else "single",
-                "l2": f"no flush: {comp_bytes / 1e9:.2f} GB of compressed KV read per step "
-                      f"(> {L2_BYTES / 2**20:.0f} MiB L2)"},
+        config=arm_config(w, T, args.kernel, world),
         kv_gbs_compressed=round(comp_bytes / (ms_step * 1e-3) / 1e9, 1),
         kv_gbs_effective_uncompressed=round(uncompressed / (ms_step * 1e-3) / 1e9, 1),
         pct_of_hbm_peak=round(100 * comp_bytes / (ms_step * 1e-3) / 1e9 / peak, 1),
@@ -836,13 +848,15 @@ def usable_cores() -> int:
         return os.cpu_count() or 1
 
 
-def _oracle_head_inputs(w, heads, out_dir):
-    """Request 0 of layer 0: for each of `heads` kv heads, its BF16 keys, values, query rows and
-    length, saved under out_dir (one .npz per head) for the oracle worker processes."""
+def _oracle_head_inputs(w, heads, out_dir, tokens=1):
+    """Request 0 of layer 0: for each of `heads` kv heads, its BF16 keys, values, query rows (of
+    `tokens` new tokens) and length, saved under out_dir (one .npz per head) for the oracle worker
+    processes."""
     import numpy as np
     import torch
     from decode_attention_compressed_gb300 import inputs as I
     layer = I.make_layer(w, layer=0, device="cpu")
+    qm = I.make_multi_queries(w, tokens, layer=0) if tokens > 1 else None
     P = w.page_size
     L = int(layer.seq_lens[0])
     pages = layer.page_table[0, : -(-L // P)].to(torch.long)
@@ -853,7 +867,8 @@ def _oracle_head_inputs(w, heads, out_dir):
         np.savez(path, k=layer.k_pages[pages][:, g:g + 1].numpy().view(np.uint16),
                  v=layer.v_pages[pages][:, g:g + 1].numpy().view(np.uint16),
                  n_valid=layer.n_valid[pages].numpy(),
-                 q=layer.q[:1, g * w.group:(g + 1) * w.group].numpy().view(np.uint16),
+                 q=(qm[:1, :, g * w.group:(g + 1) * w.group] if tokens > 1
+                    else layer.q[:1, g * w.group:(g + 1) * w.group]).numpy().view(np.uint16),
                  L=np.array([L]), P=np.array([P]), scale=np.array([layer.scale]))
         paths.append(path)
     return paths
@@ -871,17 +886,18 @@ def _oracle_worker(path, barrier, queue, target_s, reps):
     O.encode_pages(oc, d["k"], d["v"], list(range(npg)), d["n_valid"], list(range(npg)))
     table = np.arange(npg, dtype=np.int32)[None]
     lens, q, scale = np.array([L]), d["q"], float(d["scale"][0])
-    O.decode_attention(q, oc, table, lens, scale)          # untimed warm-up
+    attend = O.decode_attention_multi if q.ndim == 4 else O.decode_attention   # [1][T][heads][128]: T tokens
+    attend(q, oc, table, lens, scale)                      # untimed warm-up
     barrier.wait(timeout=900)
     t0 = time.perf_counter()
     n = 0
     while (reps and n < reps) or (not reps and (n == 0 or time.perf_counter() - t0 < target_s)):
-        O.decode_attention(q, oc, table, lens, scale)
+        attend(q, oc, table, lens, scale)
         n += 1
     queue.put((n, time.perf_counter() - t0))
 
 
-def oracle_pool(w, workers, target_s=0.0, reps=0, warm_reps=0):
+def oracle_pool(w, workers, target_s=0.0, reps=0, warm_reps=0, tokens=1):
     """Run the oracle on `workers` host cores at once (one process per core, one kv head of request
     0 each, spawn start method).  Returns (head-calls per second, calls per worker, wall seconds)."""
     import multiprocessing as mp
@@ -889,7 +905,7 @@ def oracle_pool(w, workers, target_s=0.0, reps=0, warm_reps=0):
     ctx = mp.get_context("spawn")
     tmp = tempfile.mkdtemp(prefix="zf_oracle_")
     try:
-        paths = _oracle_head_inputs(w, range(workers), tmp)
+        paths = _oracle_head_inputs(w, range(workers), tmp, tokens)
         barrier, queue = ctx.Barrier(workers), ctx.Queue()
         procs = [ctx.Process(target=_oracle_worker, args=(p, barrier, queue, target_s, reps)) for p in paths]
         for p in procs:
@@ -915,18 +931,19 @@ def oracle_pool(w, workers, target_s=0.0, reps=0, warm_reps=0):
     return calls / wall, [n for n, _ in res], wall
 
 
-def cpu_baseline(w, target_s=12.0):
+def cpu_baseline(w, target_s=12.0, tokens=1):
     """Time the oracle (as it stands) on the host cores on a bounded sample — one kv head of
     request 0, layer 0, per core, for about target_s seconds — and scale to microseconds per full
     decode step (all requests, kv heads and layers)."""
     cores = usable_cores()
-    rate, calls, wall = oracle_pool(w, cores, target_s=target_s)
+    rate, calls, wall = oracle_pool(w, cores, target_s=target_s, tokens=tokens)
     head_calls = w.batch * w.num_kv_heads * w.layers
     lens_note = "request 0" if w.ctx_min is None else "request 0 (lengths vary; scaled by batch)"
     return {"value": round(head_calls / rate * 1e6, 1), "unit": "us/step", "cores": cores, "kind": "oracle",
             "extrapolated": True,
             "sample": f"{cores} processes (one per core), each the oracle's decode attention of one kv head "
-                      f"({w.group} query heads) of {lens_note}, layer 0 of {w.name}, {sum(calls)} calls in "
+                      f"({w.group} query heads, {tokens} new token{'s' if tokens > 1 else ''}) of {lens_note}, "
+                      f"layer 0 of {w.name}, {sum(calls)} calls in "
                       f"{wall:.1f} s; scaled x{head_calls} head-calls to the full step"}
 
 
@@ -937,20 +954,20 @@ def run_reference(args, rank):
     cores = usable_cores()
     # each step: every core runs the oracle for one kv head (request 0, layer 0); the full step's
     # time is that sample's time scaled by the head-calls of the step over the cores' heads
-    rate, calls, wall = oracle_pool(w, cores, reps=args.steps + args.warmup)
+    rate, calls, wall = oracle_pool(w, cores, reps=args.steps + args.warmup, tokens=args.tokens)
     head_calls = w.batch * w.num_kv_heads * w.layers
     per = head_calls / rate
     v = round(per * 1e6, 1)
     return dict(metric=METRIC, value=v, unit="us/step", n_gpus=0, steps=args.steps, warmup=args.warmup,
                 ms_per_step=round(per * 1e3, 3), higher_is_better=False, scaling="weak", vs_baseline=None,
                 dtype="f64", data="synthetic (seeded, distributions of the workload)",
-                config={"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
-                        "page_size": w.page_size, "ctx": w.ctx, "layers_per_step": w.layers},
+                config=arm_config(w, args.tokens, args.kernel, int(os.environ.get("WORLD_SIZE", "1"))),
                 impl="reference", extrapolated=True,
                 sample_wall_s=round(wall, 2),
                 cpu_baseline={"value": v, "unit": "us/step", "cores": cores, "kind": "oracle",
                               "sample": f"each step: {cores} processes, each the oracle's decode attention of one "
-                                        f"kv head ({w.group} query heads) of request 0, layer 0 ({sum(calls)} calls "
+                                        f"kv head ({w.group} query heads, {args.tokens} new token"
+                                        f"{'s' if args.tokens > 1 else ''}) of request 0, layer 0 ({sum(calls)} calls "
                                         f"incl. warm-up in {wall:.1f} s); scaled x{head_calls} head-calls over "
                                         f"{cores} cores to the full step: an extrapolation, not a full step run"},
                 e2e={"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
@@ -1014,7 +1031,7 @@ def main():
     res = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(workload_of(args))
+            res["cpu_baseline"] = cpu_baseline(workload_of(args), tokens=args.tokens)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -113,3 +113,27 @@ def test_multi_token_lines_name_real_workloads_and_wide_column_sets():
     for name, T in bench.MULTI_TOKEN:
         w = I.WORKLOADS[name]
         assert T > 1 and w.num_q_heads // w.num_kv_heads * T > 8
+
+
+@pytest.mark.parametrize("tokens", [1, 3])
+def test_reference_arm_line_has_this_arms_config(tokens, monkeypatch):
+    """The reference arm (the oracle on the host cores) prints the same `config` object as this
+    library's arm for the same arguments, so the two lines compare like for like; with several new
+    tokens per request its sample runs the multi-token oracle."""
+    monkeypatch.setattr(bench, "usable_cores", lambda: 2)
+    args = bench.argparse.Namespace(workload="tiny", layers=None, batch=None, steps=1, warmup=3,
+                                    tokens=tokens, kernel="auto")
+    res = bench.run_reference(args, 0)
+    w = bench.workload_of(args)
+    assert res["config"] == bench.arm_config(w, tokens, "auto", 1)
+    assert res["impl"] == "reference" and res["extrapolated"] is True
+    assert f"{tokens} new token" in res["cpu_baseline"]["sample"]
+    assert res["value"] > 0 and res["e2e"]["value"] == res["value"]
+    assert bench.run_reference(args, 1) is None          # only rank 0 runs it
+
+
+def test_l2_note_follows_the_smallest_step():
+    big = bench.arm_config(I.WORKLOADS["llama7b_mha_8192"], 1, "auto", 1)["l2"]
+    small = bench.arm_config(I.WORKLOADS["tiny"], 1, "auto", 1)["l2"]
+    assert "at least 3.29 GB" in big and "> 129 MiB L2" in big
+    assert "may stay in the 129 MiB L2" in small

@@ -72,7 +72,7 @@ def kernel_source_hash() -> str:
 def read_traffic(workload: str):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it was
     taken on the current kernel sources (same source hash); else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    path = os.path.join(ROOT, "profiles", "attn_kernel_dram_traffic_by_workload.txt")
     if not os.path.exists(path):
         return None
     want = kernel_source_hash()

@@ -78,7 +78,7 @@ def test_traffic_is_read_only_for_the_current_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "profiles").mkdir()
     h = bench.kernel_source_hash()
-    (tmp_path / "profiles" / "traffic.txt").write_text(
+    (tmp_path / "profiles" / "attn_kernel_dram_traffic_by_workload.txt").write_text(
         "# workload launches bytes hash\n"
         f"wl_a 3 123456 {h}\n"
         "wl_b 3 999 0000000000000000\n")
